@@ -1,0 +1,396 @@
+/*
+ * spv_oracle.c -- ORACLE for the speculative-sampling verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, double-precision CPU
+ * restatement of what the verify step computes.  It exists so that the tests,
+ * the smoke check and the benchmark's CPU-baseline leg can check the CUDA
+ * library against something written independently of it.  It shares no code,
+ * header, table or constant generator with the CUDA library, and nothing in
+ * the library links, loads or calls it.
+ *
+ * Sources (web pages this follows; the section names are the pages' own):
+ *   [SD]  "Speculative Decoding: How Draft-Model Parallelism Cuts LLM
+ *         Inference Latency" -- sections "The four-phase loop" (steps 2-4),
+ *         "The acceptance criterion and why it is exact", "The proof of
+ *         exactness", "Acceptance rate equals 1 minus total variation
+ *         distance" (Theorem 3.5).
+ *   [SPD] "Speculative Pipeline Decoding: Higher-Accuracy Drafting with Hidden
+ *         Latency via Pipeline Parallelism" -- the streaming-verification
+ *         section (greedy: exact argmax match; sampling: standard rejection
+ *         sampling) and "Evaluation" (temperature T).
+ *   [SSD] "Speculative Speculative Decoding" (review of arXiv 2603.03251) --
+ *         Figure 2 / "Core Technical Barrier" (geometric fan-out
+ *         F_k = F_0 * a_p^(k/(1+r)), top-ranked draft tokens excluding the
+ *         token already sent for verification).
+ *
+ * Readings where the pages leave a step open (each is listed in the design doc):
+ *   - Accept test: accept x_i iff p_i(x_i) > 0 and r_i * q_i(x_i) <= p_i(x_i),
+ *     r_i in (0,1].  This is [SD] step 3 "r_i <= min(1, p/q)" without the
+ *     division; p = 0 always rejects, q == p always accepts.
+ *   - "Sample from" ([SD] step 4) is realised by an exponential race, which
+ *     draws exactly from the stated distribution:
+ *       * tokens are grouped in blocks of SPVO_BLOCK ids; block beta wins the
+ *         block race if E_beta / W_beta is smallest (W_beta = the block's
+ *         probability mass, E_beta ~ Exp(1)); then token x of the winning
+ *         block wins if E_x / P(x) is smallest.  P(x) = W_beta/Z * P(x)/W_beta.
+ *       * The residual norm(max(0, p - q)) is drawn by rejection: draw x from
+ *         p by the race above, accept it with probability max(0, 1 - q/p)
+ *         (i.e. iff q(x) <= (1 - v) p(x)); accepted draws have density
+ *         proportional to p * (1 - q/p)+ = (p - q)+.  After SPVO_MAX_TRIALS
+ *         failed trials the residual is drawn directly by the same race over
+ *         the residual masses, so the output stays exact.
+ *     Every exponential comes from E = -ln U, U = ((w >> 40) + 1) * 2^-24,
+ *     w one 64-bit word of Philox4x64-10 keyed by the sequence's key.
+ *   - Ties in a race, in an argmax and in the fan-out order go to the lower
+ *     index; -0.0 ranks equal to +0.0.
+ *   - NaN or +inf in any row read, a row without a finite entry, or a draft
+ *     token outside [0, V) make the sequence a bad row (status 4).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define SPVO_BLOCK 1024
+#define SPVO_MAX_TRIALS 64
+
+/* Stream tags: the second counter word of every Philox draw. */
+#define SPVO_STREAM_BLOCK 1u
+#define SPVO_STREAM_TOKEN 2u
+#define SPVO_STREAM_ACCEPT 3u
+#define SPVO_STREAM_FB_BLOCK 4u
+#define SPVO_STREAM_FB_TOKEN 5u
+
+#define SPVO_OK 0
+#define SPVO_BAD_ROW 4
+
+/* ------------------------------------------------------------------------ */
+/* Philox4x64-10, from its published definition (Salmon, Moraes, Dror, Shaw,
+ * "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): ten rounds of two
+ * 64x64->128 multiplies, with the key bumped by two Weyl constants between
+ * rounds. */
+static void mulhilo64(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo)
+{
+    unsigned __int128 p = (unsigned __int128)a * (unsigned __int128)b;
+    *hi = (uint64_t)(p >> 64);
+    *lo = (uint64_t)p;
+}
+
+void spvo_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
+{
+    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint64_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B97F4A7C15ull;
+            k1 += 0xBB67AE8584CAA73Bull;
+        }
+        uint64_t hi0, lo0, hi1, lo1;
+        mulhilo64(0xD2E7470EE14C6C93ull, c0, &hi0, &lo0);
+        mulhilo64(0xCA5A826395121157ull, c2, &hi1, &lo1);
+        uint64_t n0 = hi1 ^ c1 ^ k0;
+        uint64_t n1 = lo1;
+        uint64_t n2 = hi0 ^ c3 ^ k1;
+        uint64_t n3 = lo0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Uniform in (0,1] for draw n of (stream, trial, position) of one sequence:
+ * counter = (n / 4, stream, trial, position), key = (seq_key, 0), word n % 4. */
+double spvo_uniform(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t pos, uint64_t n)
+{
+    uint64_t ctr[4] = { n >> 2, (uint64_t)stream, (uint64_t)trial, (uint64_t)pos };
+    uint64_t key[2] = { seq_key, 0 };
+    uint64_t out[4];
+    spvo_philox4x64_10(ctr, key, out);
+    uint64_t w = out[n & 3u];
+    return (double)((w >> 40) + 1u) * ldexp(1.0, -24);
+}
+
+/* Exp(1) variate from the same draw: E = -ln U. */
+static double expo(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t pos, uint64_t n)
+{
+    return -log(spvo_uniform(seq_key, stream, trial, pos, n));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Compensated (Neumaier) running sum. */
+typedef struct { double s, c; } ksum;
+static void ksum_add(ksum *k, double x)
+{
+    double t = k->s + x;
+    if (fabs(k->s) >= fabs(x)) k->c += (k->s - t) + x;
+    else k->c += (x - t) + k->s;
+    k->s = t;
+}
+static double ksum_val(const ksum *k) { return k->s + k->c; }
+
+/* Temperature softmax of one row, [SD] step 2 ("probability distributions
+ * p_1 ... p_{gamma+1}") with [SPD] "Evaluation" temperature T > 0:
+ * y = z / T, M = max y, S = sum exp(y - M), P(x) = exp(y_x - M) / S.
+ * Returns 0, or SPVO_BAD_ROW if the row holds NaN or +inf or no finite entry. */
+int spvo_softmax_stats(const float *z, int V, double T, double *M_out, double *S_out)
+{
+    double M = -INFINITY;
+    for (int x = 0; x < V; ++x) {
+        double zx = (double)z[x];
+        if (isnan(zx) || (isinf(zx) && zx > 0)) return SPVO_BAD_ROW;
+        double y = zx / T;
+        if (y > M) M = y;
+    }
+    if (isinf(M)) return SPVO_BAD_ROW; /* every entry is -inf */
+    ksum S = { 0, 0 };
+    for (int x = 0; x < V; ++x) ksum_add(&S, exp((double)z[x] / T - M));
+    *M_out = M;
+    *S_out = ksum_val(&S);
+    return SPVO_OK;
+}
+
+static double prob(const float *z, int x, double T, double M, double S)
+{
+    return exp((double)z[x] / T - M) / S;
+}
+
+/* Margin bookkeeping: the smallest decision margin seen for a sequence. */
+static void note_margin(double *margin, double m)
+{
+    if (m < *margin) *margin = m;
+}
+
+/* Race winner among arrivals a[0..n): smallest arrival, ties to the lower
+ * index.  Records ln(second) - ln(first) as the decision margin. */
+static int race_winner(const double *a, int n, double *margin)
+{
+    int best = -1;
+    double a1 = INFINITY, a2 = INFINITY;
+    for (int i = 0; i < n; ++i) {
+        if (a[i] < a1) { a2 = a1; a1 = a[i]; best = i; }
+        else if (a[i] < a2) a2 = a[i];
+    }
+    double m;
+    if (isinf(a2)) m = INFINITY;
+    else if (a1 == 0.0) m = (a2 == 0.0) ? 0.0 : INFINITY;
+    else m = log(a2) - log(a1);
+    note_margin(margin, m);
+    return best;
+}
+
+/* Draw one token from the distribution with (unnormalised) masses w[0..V)
+ * by the two-level exponential race described in the header.
+ * bstream / tstream are the block-race and token-race stream tags. */
+static int race_sample(const double *w, int V, uint64_t key, uint32_t bstream, uint32_t tstream,
+                       uint32_t trial, uint32_t pos, double *margin)
+{
+    int nb = (V + SPVO_BLOCK - 1) / SPVO_BLOCK;
+    double *arr = (double *)malloc(sizeof(double) * (size_t)(nb > SPVO_BLOCK ? nb : SPVO_BLOCK));
+    for (int b = 0; b < nb; ++b) {
+        int lo = b * SPVO_BLOCK, hi = lo + SPVO_BLOCK < V ? lo + SPVO_BLOCK : V;
+        ksum W = { 0, 0 };
+        for (int x = lo; x < hi; ++x) ksum_add(&W, w[x]);
+        double Wb = ksum_val(&W);
+        arr[b] = Wb > 0 ? expo(key, bstream, trial, pos, (uint64_t)b) / Wb : INFINITY;
+    }
+    int bw = race_winner(arr, nb, margin);
+    int lo = bw * SPVO_BLOCK, hi = lo + SPVO_BLOCK < V ? lo + SPVO_BLOCK : V;
+    for (int x = lo; x < hi; ++x)
+        arr[x - lo] = w[x] > 0 ? expo(key, tstream, trial, pos, (uint64_t)x) / w[x] : INFINITY;
+    int xw = lo + race_winner(arr, hi - lo, margin);
+    free(arr);
+    return xw;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Greedy verify (T = 0), [SPD] streaming verification: "under greedy
+ * decoding we require an exact argmax match".  a_i = argmax z_i (lowest id on
+ * ties), accept x_i iff x_i == a_i, stop at the first mismatch and emit a_k
+ * there, or the bonus a_gamma when every draft matched. */
+static int argmax_row(const float *z, int V, int *a)
+{
+    int best = -1;
+    double bv = -INFINITY;
+    for (int x = 0; x < V; ++x) {
+        double v = (double)z[x];
+        if (isnan(v) || (isinf(v) && v > 0)) return SPVO_BAD_ROW;
+        if (best < 0 || v > bv) { best = x; bv = v; }
+    }
+    *a = best;
+    return SPVO_OK;
+}
+
+int spvo_verify_greedy_seq(const float *tgt, const int32_t *tok, int gamma, int V,
+                           int32_t *k_out, int32_t *tokens_out)
+{
+    for (int i = 0; i <= gamma; ++i) tokens_out[i] = -1;
+    *k_out = -1;
+    int a[64 + 1];
+    for (int i = 0; i < gamma; ++i)
+        if (tok[i] < 0 || tok[i] >= V) return SPVO_BAD_ROW;
+    for (int i = 0; i <= gamma; ++i)
+        if (argmax_row(tgt + (size_t)i * V, V, &a[i]) != SPVO_OK) return SPVO_BAD_ROW;
+    int k = 0;
+    while (k < gamma && tok[k] == a[k]) ++k;
+    for (int i = 0; i < k; ++i) tokens_out[i] = tok[i];
+    tokens_out[k] = a[k];
+    *k_out = k;
+    return SPVO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Chain verify for one sequence, T > 0.  [SD] "The four-phase loop":
+ *   step 3: for each draft token x_i draw r_i and accept if
+ *           r_i <= min(1, p_i(x_i)/q_i(x_i)); stop at the first rejection.
+ *   step 4: all accepted -> bonus token from p_{gamma+1}; rejected at j ->
+ *           resample from norm(max(0, p_j - q_j)).
+ * Inputs : tgt [(gamma+1) * V], drf [gamma * V] (row-major), tok [gamma],
+ *          r [gamma], seq_key, T > 0.
+ * Outputs: k, tokens [gamma+1] (k+1 ids then -1), pq [2*gamma] (p_i(x_i),
+ *          q_i(x_i)), Z (sum of the residual at the rejected position, or 1
+ *          for the bonus; only if Z_out != NULL), margin (smallest decision
+ *          margin along the decisive path), trials (residual trials used;
+ *          SPVO_MAX_TRIALS + 1 means the direct fallback ran).
+ * Returns SPVO_OK or SPVO_BAD_ROW. */
+int spvo_verify_chain_seq(const float *tgt, const float *drf, const int32_t *tok, const float *r,
+                          uint64_t seq_key, int gamma, int V, double T,
+                          int32_t *k_out, int32_t *tokens_out, double *pq_out, double *Z_out,
+                          double *margin_out, int32_t *trials_out)
+{
+    for (int i = 0; i <= gamma; ++i) tokens_out[i] = -1;
+    for (int i = 0; i < 2 * gamma; ++i) pq_out[i] = NAN;
+    *k_out = -1;
+    *margin_out = INFINITY;
+    *trials_out = 0;
+    if (Z_out) *Z_out = NAN;
+    for (int i = 0; i < gamma; ++i)
+        if (tok[i] < 0 || tok[i] >= V) return SPVO_BAD_ROW;
+
+    /* step 2: the gamma+1 target distributions and the gamma draft ones */
+    double Mt[65], St[65], Md[64], Sd[64];
+    for (int i = 0; i <= gamma; ++i)
+        if (spvo_softmax_stats(tgt + (size_t)i * V, V, T, &Mt[i], &St[i]) != SPVO_OK) return SPVO_BAD_ROW;
+    for (int i = 0; i < gamma; ++i)
+        if (spvo_softmax_stats(drf + (size_t)i * V, V, T, &Md[i], &Sd[i]) != SPVO_OK) return SPVO_BAD_ROW;
+
+    /* step 3: accept / reject, stop at the first rejection */
+    int k = gamma;
+    double margin = INFINITY;
+    for (int i = 0; i < gamma; ++i) {
+        const float *ti = tgt + (size_t)i * V, *di = drf + (size_t)i * V;
+        double p = prob(ti, tok[i], T, Mt[i], St[i]);
+        double q = prob(di, tok[i], T, Md[i], Sd[i]);
+        pq_out[2 * i] = p;
+        pq_out[2 * i + 1] = q;
+        int acc = (p > 0) && ((double)r[i] * q <= p);
+        if (i < k) { /* decisions up to the first rejection decide the output */
+            double m = (q > 0) ? fabs((double)r[i] - p / q) : INFINITY;
+            note_margin(&margin, m);
+            if (!acc) k = i;
+        }
+    }
+
+    /* step 4 */
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    int emitted;
+    if (k == gamma) {
+        const float *tb = tgt + (size_t)gamma * V;
+        for (int x = 0; x < V; ++x) w[x] = prob(tb, x, T, Mt[gamma], St[gamma]);
+        emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_TOKEN, 0, (uint32_t)gamma, &margin);
+        if (Z_out) *Z_out = 1.0;
+    } else {
+        const float *tj = tgt + (size_t)k * V, *dj = drf + (size_t)k * V;
+        for (int x = 0; x < V; ++x) w[x] = prob(tj, x, T, Mt[k], St[k]);
+        emitted = -1;
+        int t;
+        for (t = 0; t < SPVO_MAX_TRIALS; ++t) {
+            int x = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_TOKEN, (uint32_t)t, (uint32_t)k, &margin);
+            double v = spvo_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
+            double p = w[x], q = prob(dj, x, T, Md[k], Sd[k]);
+            note_margin(&margin, fabs((1.0 - v) - q / p));
+            if (q <= (1.0 - v) * p) { emitted = x; break; }
+        }
+        *trials_out = (emitted >= 0) ? t + 1 : SPVO_MAX_TRIALS + 1;
+        /* residual masses max(0, p - q) (also the fallback's race weights) */
+        for (int x = 0; x < V; ++x) {
+            double d = w[x] - prob(dj, x, T, Md[k], Sd[k]);
+            w[x] = d > 0 ? d : 0.0;
+        }
+        if (emitted < 0)
+            emitted = race_sample(w, V, seq_key, SPVO_STREAM_FB_BLOCK, SPVO_STREAM_FB_TOKEN, 0, (uint32_t)k, &margin);
+        if (Z_out) {
+            ksum Z = { 0, 0 };
+            for (int x = 0; x < V; ++x) ksum_add(&Z, w[x]);
+            *Z_out = ksum_val(&Z);
+        }
+    }
+    free(w);
+    for (int i = 0; i < k; ++i) tokens_out[i] = tok[i];
+    tokens_out[k] = emitted;
+    *k_out = k;
+    *margin_out = margin;
+    return SPVO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Fan-out, [SSD] Figure 2: at each position k the F_k top-ranked draft
+ * tokens by draft logit, excluding the token already sent for verification
+ * there.  Order: logit descending (-0.0 equal to +0.0), then id ascending. */
+typedef struct { double v; int id; } vid;
+static int cmp_vid(const void *a, const void *b)
+{
+    const vid *x = (const vid *)a, *y = (const vid *)b;
+    if (x->v > y->v) return -1;
+    if (x->v < y->v) return 1;
+    return (x->id > y->id) - (x->id < y->id);
+}
+
+int spvo_fanout_row(const float *d, int V, int exclude, int F, int32_t *ids_out)
+{
+    for (int i = 0; i < F; ++i) ids_out[i] = -1;
+    vid *all = (vid *)malloc(sizeof(vid) * (size_t)V);
+    int n = 0;
+    for (int x = 0; x < V; ++x) {
+        double v = (double)d[x];
+        if (isnan(v)) { free(all); return SPVO_BAD_ROW; }
+        if (x == exclude) continue;
+        all[n].v = v + 0.0; /* -0.0 + 0.0 == +0.0 */
+        all[n].id = x;
+        ++n;
+    }
+    qsort(all, (size_t)n, sizeof(vid), cmp_vid);
+    for (int i = 0; i < F && i < n; ++i) ids_out[i] = all[i].id;
+    free(all);
+    return SPVO_OK;
+}
+
+/* [SSD] "Core Technical Barrier" (Theorem 12): F_k = F_0 * a_p^(k/(1+r)). */
+double spvo_fanout_size(int F0, double a, double r, int k)
+{
+    return (double)F0 * pow(a, (double)k / (1.0 + r));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Batch loops over sequences [b0, b1): the same per-sequence functions, so a
+ * caller can split a batch across threads without per-sequence overhead. */
+void spvo_verify_chain_batch(const float *tgt, const float *drf, const int32_t *tok, const float *r,
+                             const uint64_t *keys, int b0, int b1, int gamma, int V, double T,
+                             int32_t *k_out, int32_t *tokens_out, double *pq_out, double *Z_out,
+                             double *margin_out, int32_t *trials_out, int32_t *status_out)
+{
+    for (int b = b0; b < b1; ++b) {
+        status_out[b] = spvo_verify_chain_seq(
+            tgt + (size_t)b * (size_t)(gamma + 1) * (size_t)V, drf + (size_t)b * (size_t)gamma * (size_t)V,
+            tok + (size_t)b * gamma, r + (size_t)b * gamma, keys[b], gamma, V, T, &k_out[b],
+            tokens_out + (size_t)b * (gamma + 1), pq_out + (size_t)b * 2 * gamma, Z_out ? &Z_out[b] : 0,
+            &margin_out[b], &trials_out[b]);
+    }
+}
+
+void spvo_verify_greedy_batch(const float *tgt, const int32_t *tok, int b0, int b1, int gamma, int V,
+                              int32_t *k_out, int32_t *tokens_out, int32_t *status_out)
+{
+    for (int b = b0; b < b1; ++b)
+        status_out[b] = spvo_verify_greedy_seq(tgt + (size_t)b * (size_t)(gamma + 1) * (size_t)V,
+                                               tok + (size_t)b * gamma, gamma, V, &k_out[b],
+                                               tokens_out + (size_t)b * (gamma + 1));
+}

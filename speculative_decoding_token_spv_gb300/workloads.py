@@ -1,0 +1,140 @@
+"""Seeded synthetic inputs for the verify step (shared by tests, bench and smoke).
+
+This module only draws inputs: logits with the shapes and value distributions of
+the workloads below, draft tokens, accept uniforms r and per-sequence sampling
+keys.  It holds none of the verify step's arithmetic.  The draft tokens stand
+in for a draft model's sampler: they are drawn from softmax(draft / T) with
+``torch.multinomial`` (T > 0) or taken as the draft argmax (T = 0).
+
+Workloads (stand-ins for the pages' evaluation sets, which are not used):
+  tiny    B=1,  gamma=4, V=1000,    fp32: z ~ N(0, 2^2); d = z + N(0, 0.5^2)
+  spd     B=64, gamma=1, V=151936,  bf16: z ~ N(0, 3^2) with 20 peak ids per
+          target row raised by +8; d = z + N(0, 1^2)
+  eagle   B=32, gamma in {7, 15}, V=128256, bf16: z ~ N(0, 2.5^2);
+          d = 0.8 z + N(0, 1.5^2)
+  fanout  draft [8, 5, 128256] fp32 ~ N(0, 2^2); exclude[b,k] drawn from
+          softmax(d[b,k]) for k < 4, -1 at k = 4; F = round(8 * 0.8^(k/1.5))
+  sweep   the spd distributions at gamma=4, V=151936, fp32 / bf16,
+          B in {1, 8, 64, 128, 256}
+All draws are fp32 from seeded ``torch.Generator`` s on the requested device,
+then cast to the workload dtype; V is the last, contiguous axis.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import torch
+
+SEEDS = dict(tiny=(100, 101, 0, 1), spd=(200, 201, 0, 1), eagle=(300, 301, 2, 3), sweep=(200, 201, 0, 1))
+PEAK_SEED = 202
+FANOUT_SEEDS = (400, 4)
+
+
+@dataclass
+class ChainInputs:
+    name: str
+    target: torch.Tensor          # [B, gamma+1, V]
+    draft: torch.Tensor           # [B, gamma, V]
+    tokens: torch.Tensor          # [B, gamma] int32
+    r: torch.Tensor               # [B, gamma] fp32 in (0, 1]
+    keys: torch.Tensor            # [B] int64 holding uint64 bit patterns
+    temperature: float
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def B(self):
+        return self.target.shape[0]
+
+    @property
+    def gamma(self):
+        return self.target.shape[1] - 1
+
+    @property
+    def V(self):
+        return self.target.shape[2]
+
+
+@dataclass
+class FanoutInputs:
+    name: str
+    draft: torch.Tensor           # [B, K+1, V]
+    exclude: torch.Tensor         # [B, K+1] int32, -1 = none
+    fanout: list                  # K+1 ints
+
+
+def _gen(device, seed):
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def _draft_tokens(d: torch.Tensor, temperature: float, seed: int, device) -> torch.Tensor:
+    B, g, V = d.shape
+    if g == 0:
+        return torch.zeros(B, 0, dtype=torch.int32, device=device)
+    flat = d.float().reshape(B * g, V)
+    if temperature == 0:
+        return flat.argmax(dim=1).to(torch.int32).reshape(B, g)
+    probs = torch.softmax(flat / temperature, dim=1)
+    return torch.multinomial(probs, 1, generator=_gen(device, seed)).to(torch.int32).reshape(B, g)
+
+
+def _uniforms_and_keys(B, g, seed, device):
+    gen = _gen(device, seed)
+    r = 1.0 - torch.rand(B, g, generator=gen, device=device, dtype=torch.float32)
+    keys = torch.randint(-(2 ** 63), 2 ** 63 - 1, (B,), generator=gen, device=device, dtype=torch.int64)
+    return r, keys
+
+
+def chain_from_params(name, B, gamma, V, dtype, temperature, z_std, d_scale, d_std, peaks, seeds,
+                      device="cpu") -> ChainInputs:
+    """Generic generator: z ~ N(0, z_std^2) [B, gamma+1, V] (+8 on `peaks` ids
+    per target row), d = d_scale * z[:, :gamma] + N(0, d_std^2)."""
+    s_z, s_d, s_tok, s_u = seeds
+    z = torch.randn(B, gamma + 1, V, generator=_gen(device, s_z), device=device) * z_std
+    if peaks:
+        score = torch.rand(B, gamma + 1, V, generator=_gen(device, PEAK_SEED), device=device)
+        idx = score.topk(peaks, dim=2).indices
+        z.scatter_add_(2, idx, torch.full(idx.shape, 8.0, device=device))
+        del score, idx
+    d = torch.randn(B, gamma, V, generator=_gen(device, s_d), device=device) * d_std
+    d.add_(z[:, :gamma], alpha=d_scale)
+    target = z.to(dtype)
+    del z
+    draft = d.to(dtype)
+    del d
+    tokens = _draft_tokens(draft, temperature, s_tok, device)
+    r, keys = _uniforms_and_keys(B, gamma, s_u, device)
+    return ChainInputs(name, target, draft, tokens, r, keys, float(temperature),
+                       dict(B=B, gamma=gamma, V=V, dtype=str(dtype).replace("torch.", ""),
+                            T=float(temperature)))
+
+
+def tiny(device="cpu", temperature=1.0) -> ChainInputs:
+    return chain_from_params("tiny", 1, 4, 1000, torch.float32, temperature, 2.0, 1.0, 0.5, 0,
+                             SEEDS["tiny"], device)
+
+
+def spd(device="cpu", temperature=1.0, B=64) -> ChainInputs:
+    return chain_from_params("spd", B, 1, 151936, torch.bfloat16, temperature, 3.0, 1.0, 1.0, 20,
+                             SEEDS["spd"], device)
+
+
+def eagle(gamma=7, device="cpu", temperature=1.0, B=32) -> ChainInputs:
+    return chain_from_params(f"eagle_g{gamma}", B, gamma, 128256, torch.bfloat16, temperature, 2.5, 0.8,
+                             1.5, 0, SEEDS["eagle"], device)
+
+
+def sweep(B=64, dtype=torch.float32, device="cpu", temperature=1.0, V=151936, gamma=4) -> ChainInputs:
+    return chain_from_params(f"sweep_B{B}_{str(dtype).replace('torch.', '')}", B, gamma, V, dtype,
+                             temperature, 3.0, 1.0, 1.0, 20, SEEDS["sweep"], device)
+
+
+def fanout(device="cpu", B=8, K=4, V=128256, fanout_sizes=(8, 7, 6, 5, 4)) -> FanoutInputs:
+    s_d, s_x = FANOUT_SEEDS
+    d = torch.randn(B, K + 1, V, generator=_gen(device, s_d), device=device) * 2.0
+    ex = torch.full((B, K + 1), -1, dtype=torch.int32, device=device)
+    if K > 0:
+        probs = torch.softmax(d[:, :K].reshape(B * K, V), dim=1)
+        ex[:, :K] = torch.multinomial(probs, 1, generator=_gen(device, s_x)).to(torch.int32).reshape(B, K)
+    return FanoutInputs("fanout", d, ex, list(fanout_sizes))

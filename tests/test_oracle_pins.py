@@ -1,0 +1,452 @@
+"""Pins for the oracle: checks against what the pages and mathematics fix.
+
+None of these re-types the oracle's own formulas.  Each pin comes from a
+library routine (numpy's Philox, torch/scipy softmax, numpy argmax/lexsort), a
+closed form the pages state (acceptance = 1 - TVD, Theorem 3.5; expected
+tokens per iteration, Theorem 3.8 with c = 0; alpha^K all-accept rate; the
+geometric fan-out), an exactness property (the emitted token is distributed as
+the target p), or a special case the pages name (p >= q always accepts,
+identical models accept everything, p(x) = 0 always rejects).
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+from scipy import stats
+from scipy.special import softmax
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+RNG_SEED = 12345
+
+
+def _read_golden(name):
+    rows = []
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if line and not line.startswith("#"):
+                rows.append(line.split())
+    return rows
+
+
+def _chi2_ok(counts, probs, min_p=1e-6):
+    """Chi-square goodness of fit; merges cells with expected count < 5."""
+    counts = np.asarray(counts, float)
+    n = counts.sum()
+    exp = np.asarray(probs, float) * n
+    keep = exp >= 5
+    obs_k, exp_k = counts[keep], exp[keep]
+    obs_rest, exp_rest = counts[~keep].sum(), exp[~keep].sum()
+    if exp_rest > 0:
+        obs_k = np.append(obs_k, obs_rest)
+        exp_k = np.append(exp_k, exp_rest)
+    exp_k = exp_k * obs_k.sum() / exp_k.sum()
+    p = stats.chisquare(obs_k, exp_k).pvalue
+    return p > min_p, p
+
+
+# ----------------------------------------------------------------- Philox
+def test_philox_matches_numpy_bitgenerator():
+    """Philox4x64-10 against numpy.random.Philox (numpy steps the counter
+    before each block, so numpy(counter=c-1) yields the block for c)."""
+    rng = np.random.default_rng(RNG_SEED)
+    for _ in range(20):
+        ctr = [int(x) for x in rng.integers(1, 2 ** 63, 4, dtype=np.int64)]
+        key = [int(x) for x in rng.integers(0, 2 ** 63, 2, dtype=np.int64)]
+        bg = np.random.Philox(key=key, counter=[ctr[0] - 1] + ctr[1:])
+        ref = bg.random_raw(4)
+        got = oracle.philox4x64_10(ctr, key)
+        assert np.array_equal(ref.astype(np.uint64), got)
+
+
+def test_uniform_word_mapping():
+    """uniform(n) takes word n % 4 of the block at counter (n/4, stream, trial, pos)."""
+    key = 0x1234_5678_9ABC_DEF0
+    for n in range(9):
+        # numpy steps the 256-bit counter before each block, with carry:
+        # (2^64-1, s-1, t, p) steps to (0, s, t, p).
+        c0 = n >> 2
+        ctr = [c0 - 1, 3, 7, 2] if c0 > 0 else [2 ** 64 - 1, 2, 7, 2]
+        bg = np.random.Philox(key=np.array([key, 0], np.uint64), counter=np.array(ctr, np.uint64))
+        w = bg.random_raw(4)[n & 3]
+        u = oracle.uniform(key, 3, 7, 2, n)
+        assert u == ((int(w) >> 40) + 1) * 2.0 ** -24
+        assert 0 < u <= 1
+
+
+# ----------------------------------------------------------------- softmax
+@pytest.mark.parametrize("T", [1.0, 0.7, 2.5])
+def test_softmax_stats_vs_torch(T):
+    rng = np.random.default_rng(RNG_SEED)
+    z = (rng.normal(0, 3, 5000)).astype(np.float32)
+    z[17] = -np.inf
+    M, S = oracle.softmax_stats(z, T)
+    p = np.exp(z.astype(np.float64) / T - M) / S
+    ref = torch.softmax(torch.from_numpy(z.astype(np.float64)) / T, dim=0).numpy()
+    np.testing.assert_allclose(p, ref, rtol=1e-12, atol=1e-300)
+    assert abs(p.sum() - 1.0) < 1e-12
+    assert p[17] == 0.0
+
+
+def test_softmax_bad_rows():
+    z = np.zeros(10, np.float32)
+    for bad in (np.nan, np.inf):
+        zz = z.copy()
+        zz[3] = bad
+        assert oracle.softmax_stats(zz, 1.0) is None
+    assert oracle.softmax_stats(np.full(10, -np.inf, np.float32), 1.0) is None
+
+
+# ----------------------------------------------------------------- helpers
+def _chain(p_logits_rows, q_logits_rows, tokens, r, keys, T=1.0, want_Z=False):
+    return oracle.verify_chain(np.asarray(p_logits_rows, np.float32), np.asarray(q_logits_rows, np.float32),
+                               tokens, r, keys, T, want_Z=want_Z)
+
+
+def _logits_from_probs(p):
+    with np.errstate(divide="ignore"):
+        return np.log(np.asarray(p, np.float64)).astype(np.float32)
+
+
+def _probs(logits, T=1.0):
+    return softmax(np.asarray(logits, np.float64) / T)
+
+
+def _keys(n, seed=RNG_SEED):
+    return np.random.default_rng(seed).integers(0, 2 ** 63, n, dtype=np.int64).astype(np.uint64)
+
+
+# ----------------------------------------------------------------- special cases
+def test_identical_models_accept_everything():
+    """q == p: every draft token accepted, for any r in (0, 1] (TVD = 0, alpha = 1)."""
+    rng = np.random.default_rng(1)
+    B, g, V = 64, 4, 300
+    z = rng.normal(0, 2, (B, g + 1, V)).astype(np.float32)
+    d = z[:, :g].copy()
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    r = np.ones((B, g), np.float32)
+    r[::2] = rng.random((B // 2, g)).astype(np.float32) + np.float32(1e-6)
+    out = _chain(z, d, tok, np.minimum(r, 1), _keys(B))
+    assert (out["status"] == 0).all()
+    assert (out["accept_count"] == g).all()
+    assert (out["out_tokens"][:, :g] == tok).all()
+
+
+def test_zero_target_prob_always_rejects():
+    """p_i(x_i) = 0 rejects even with the smallest r."""
+    rng = np.random.default_rng(2)
+    B, g, V = 32, 3, 200
+    z = rng.normal(0, 1, (B, g + 1, V)).astype(np.float32)
+    d = z[:, :g].copy()
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    z[np.arange(B), 1, tok[:, 1]] = -np.inf
+    r = np.full((B, g), 2.0 ** -24, np.float32)
+    out = _chain(z, d, tok, r, _keys(B))
+    assert (out["accept_count"] == 1).all()
+    assert (out["out_tokens"][:, 1] != tok[:, 1]).all()
+    assert (out["pq"][:, 1, 0] == 0).all()
+
+
+def test_target_above_draft_always_accepts():
+    """p(x) >= q(x): always accept (the pages' first case), even with r = 1."""
+    rng = np.random.default_rng(3)
+    B, g, V = 40, 2, 100
+    z = rng.normal(0, 1, (B, g + 1, V)).astype(np.float32)
+    d = rng.normal(0, 1, (B, g, V)).astype(np.float32)
+    tok = np.zeros((B, g), np.int32)
+    for b in range(B):
+        for i in range(g):
+            p, q = _probs(z[b, i]), _probs(d[b, i])
+            tok[b, i] = int(np.argmax(p - q))  # a token with p > q
+    r = np.ones((B, g), np.float32)
+    out = _chain(z, d, tok, r, _keys(B))
+    assert (out["accept_count"] == g).all()
+
+
+def test_output_length_and_padding():
+    rng = np.random.default_rng(4)
+    B, g, V = 200, 5, 64
+    z = rng.normal(0, 2, (B, g + 1, V)).astype(np.float32)
+    d = (z[:, :g] + rng.normal(0, 1.5, (B, g, V))).astype(np.float32)
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    out = _chain(z, d, tok, r, _keys(B))
+    k = out["accept_count"]
+    assert ((k >= 0) & (k <= g)).all()
+    for b in range(B):
+        row = out["out_tokens"][b]
+        assert (row[: k[b] + 1] >= 0).all() and (row[: k[b] + 1] < V).all()
+        assert (row[k[b] + 1:] == -1).all()
+        assert (row[: k[b]] == tok[b, : k[b]]).all()
+        # the rejected token is never re-emitted: its residual mass is zero
+        if k[b] < g:
+            assert row[k[b]] != tok[b, k[b]]
+    assert (k < g).any() and (k == g).any()
+
+
+def test_bad_rows():
+    rng = np.random.default_rng(5)
+    B, g, V = 4, 2, 50
+    z = rng.normal(0, 1, (B, g + 1, V)).astype(np.float32)
+    d = z[:, :g].copy()
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    tok[0, 1] = V          # out of range
+    z[1, 2, 7] = np.nan    # NaN in the bonus row
+    d[2, 0, 3] = np.inf    # +inf in a draft row
+    out = _chain(z, d, tok, np.ones((B, g), np.float32), _keys(B))
+    assert list(out["status"]) == [4, 4, 4, 0]
+    assert (out["accept_count"][:3] == -1).all() and (out["out_tokens"][:3] == -1).all()
+
+
+# ----------------------------------------------------------------- statistics
+def _iid_case(rng, V, g, B, T=1.0, z_std=1.5, noise=1.0):
+    z1 = rng.normal(0, z_std, V).astype(np.float32)
+    d1 = (z1 + rng.normal(0, noise, V)).astype(np.float32)
+    z = np.broadcast_to(z1, (B, g + 1, V)).astype(np.float32)
+    d = np.broadcast_to(d1, (B, g, V)).astype(np.float32)
+    q = _probs(d1, T)
+    tok = rng.choice(V, size=(B, g), p=q).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    return z, d, tok, r, _probs(z1, T), q
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_acceptance_rate_is_one_minus_tvd(T):
+    """Theorem 3.5: alpha = sum_x min(p, q) = 1 - TVD(p, q)."""
+    rng = np.random.default_rng(6)
+    B, V = 30000, 40
+    z, d, tok, r, p, q = _iid_case(rng, V, 1, B, T)
+    out = _chain(z, d, tok, r, _keys(B), T=T)
+    alpha = np.minimum(p, q).sum()
+    assert abs(alpha - (1 - 0.5 * np.abs(p - q).sum())) < 1e-12
+    emp = (out["accept_count"] == 1).mean()
+    sigma = np.sqrt(alpha * (1 - alpha) / B)
+    assert abs(emp - alpha) < 5 * sigma, (emp, alpha, sigma)
+
+
+def test_expected_tokens_per_iteration():
+    """Theorem 3.8 with c = 0: E[tokens] = (1 - alpha^(g+1)) / (1 - alpha)."""
+    rng = np.random.default_rng(7)
+    B, V, g = 30000, 30, 4
+    z, d, tok, r, p, q = _iid_case(rng, V, g, B)
+    out = _chain(z, d, tok, r, _keys(B))
+    alpha = np.minimum(p, q).sum()
+    n = out["accept_count"] + 1
+    expect = (1 - alpha ** (g + 1)) / (1 - alpha)
+    assert abs(n.mean() - expect) < 5 * n.std() / np.sqrt(B), (n.mean(), expect)
+    assert n.max() <= g + 1 and n.min() >= 1
+
+
+def test_all_accept_rate_alpha_pow_K():
+    """alpha^K all-accept rate with K = 5, alpha = 0.8 (the SSD review's 33%)."""
+    gold = dict((r[0], float(r[1])) for r in _read_golden("all_accept_ssd.txt"))
+    K, a = int(gold["K"]), gold["alpha"]
+    assert abs(a ** K - gold["p_all_accept"]) < 1e-12 and round(a ** K, 2) == gold["page_rounded"]
+    # p uniform on 5 tokens, q puts 0.16 on each of them and 0.2 on a sixth: sum min = 0.8
+    V = 10
+    p = np.zeros(V); p[:5] = 0.2
+    q = np.zeros(V); q[:5] = 0.16; q[5] = 0.2
+    zl, dl = _logits_from_probs(p), _logits_from_probs(q)
+    pp, qq = _probs(zl), _probs(dl)
+    alpha = np.minimum(pp, qq).sum()
+    assert abs(alpha - a) < 1e-6
+    rng = np.random.default_rng(8)
+    B = 40000
+    z = np.broadcast_to(zl, (B, K + 1, V)).astype(np.float32)
+    d = np.broadcast_to(dl, (B, K, V)).astype(np.float32)
+    tok = rng.choice(V, size=(B, K), p=qq).astype(np.int32)
+    r = (1 - rng.random((B, K))).astype(np.float32)
+    out = _chain(z, d, tok, r, _keys(B))
+    emp = (out["accept_count"] == K).mean()
+    target = alpha ** K
+    assert abs(emp - target) < 5 * np.sqrt(target * (1 - target) / B), (emp, target)
+
+
+def _sparse_multiblock_case(rng, V=2100, n_support=12):
+    """p and q with a few tokens of mass spread over several 1024-id blocks."""
+    ids = np.sort(rng.choice(V, n_support, replace=False))
+    zl = np.full(V, -np.inf, np.float32)
+    dl = np.full(V, -np.inf, np.float32)
+    zl[ids] = rng.normal(0, 1.0, n_support)
+    dl[ids] = zl[ids] + rng.normal(0, 1.0, n_support)
+    return ids, zl.astype(np.float32), dl.astype(np.float32)
+
+
+def test_first_token_is_distributed_as_target():
+    """Exactness: P(emitted first token = x) = p_1(x) for any p, q (the pages' proof)."""
+    rng = np.random.default_rng(9)
+    ids, zl, dl = _sparse_multiblock_case(rng)
+    V, B = zl.size, 24000
+    z = np.broadcast_to(np.stack([zl, zl]), (B, 2, V)).astype(np.float32)
+    d = np.broadcast_to(dl, (B, 1, V)).astype(np.float32)
+    q = _probs(dl)
+    tok = rng.choice(V, size=(B, 1), p=q).astype(np.int32)
+    r = (1 - rng.random((B, 1))).astype(np.float32)
+    out = _chain(z, d, tok, r, _keys(B, 99))
+    first = out["out_tokens"][:, 0]
+    p = _probs(zl)
+    counts = np.bincount(first, minlength=V)[ids]
+    ok, pv = _chi2_ok(counts, p[ids])
+    assert counts.sum() == B and ok, pv
+    assert (out["accept_count"] == 0).any() and (out["accept_count"] == 1).any()
+
+
+def test_residual_distribution_on_forced_rejection():
+    """A rejected position emits from norm(max(0, p - q)); Z = TVD(p, q)."""
+    rng = np.random.default_rng(10)
+    ids, zl, dl = _sparse_multiblock_case(rng)
+    V, B = zl.size, 20000
+    p, q = _probs(zl), _probs(dl)
+    x_rej = int(ids[np.argmax(q[ids] - p[ids])])
+    assert q[x_rej] > p[x_rej]
+    z = np.broadcast_to(np.stack([zl, zl]), (B, 2, V)).astype(np.float32)
+    d = np.broadcast_to(dl, (B, 1, V)).astype(np.float32)
+    tok = np.full((B, 1), x_rej, np.int32)
+    r = np.ones((B, 1), np.float32)          # r * q = q > p: always rejected
+    out = _chain(z, d, tok, r, _keys(B, 7), want_Z=True)
+    assert (out["accept_count"] == 0).all()
+    w = np.maximum(0, p - q)
+    np.testing.assert_allclose(out["Z"], 0.5 * np.abs(p - q).sum(), rtol=1e-12)
+    counts = np.bincount(out["out_tokens"][:, 0], minlength=V)[ids]
+    ok, pv = _chi2_ok(counts, w[ids] / w.sum())
+    assert counts.sum() == B and ok, pv
+    assert counts[w[ids] == 0].sum() == 0
+
+
+def test_residual_fallback_is_exact():
+    """Nearly identical p and q (small Z) exhaust the rejection trials; the
+    direct fallback must still draw from norm(max(0, p - q))."""
+    rng = np.random.default_rng(11)
+    V, B = 1500, 10000
+    zl = rng.normal(0, 1, V).astype(np.float32)
+    dl = zl.copy()
+    hot = rng.choice(V, 6, replace=False)
+    dl[hot[:3]] += np.float32(0.05)
+    dl[hot[3:]] -= np.float32(0.05)
+    p, q = _probs(zl), _probs(dl)
+    x_rej = int(np.argmax(q - p))
+    z = np.broadcast_to(np.stack([zl, zl]), (B, 2, V)).astype(np.float32)
+    d = np.broadcast_to(dl, (B, 1, V)).astype(np.float32)
+    tok = np.full((B, 1), x_rej, np.int32)
+    out = _chain(z, d, tok, np.ones((B, 1), np.float32), _keys(B, 3), want_Z=True)
+    Z = 0.5 * np.abs(p - q).sum()
+    frac_fb = (out["trials"] == oracle.MAX_TRIALS + 1).mean()
+    assert abs(frac_fb - (1 - Z) ** oracle.MAX_TRIALS) < 5 * np.sqrt(frac_fb * (1 - frac_fb) / B) + 1e-3
+    assert frac_fb > 0.5
+    w = np.maximum(0, p - q)
+    counts = np.bincount(out["out_tokens"][:, 0], minlength=V)
+    ok, pv = _chi2_ok(counts, w / w.sum())
+    assert ok, pv
+    assert counts[w == 0].sum() == 0
+
+
+def test_bonus_is_distributed_as_last_target_row():
+    """All accepted (q == p): the bonus token ~ p_{gamma+1}."""
+    rng = np.random.default_rng(12)
+    ids, zl, _ = _sparse_multiblock_case(rng)
+    zb = np.full_like(zl, -np.inf)
+    zb[ids] = rng.normal(0, 1, ids.size)
+    V, B = zl.size, 20000
+    z = np.broadcast_to(np.stack([zl, zb.astype(np.float32)]), (B, 2, V)).astype(np.float32)
+    d = np.broadcast_to(zl, (B, 1, V)).astype(np.float32)
+    tok = np.full((B, 1), ids[0], np.int32)
+    out = _chain(z, d, tok, np.ones((B, 1), np.float32), _keys(B, 5), want_Z=True)
+    assert (out["accept_count"] == 1).all() and (out["Z"] == 1).all()
+    pb = _probs(zb)
+    counts = np.bincount(out["out_tokens"][:, 1], minlength=V)[ids]
+    ok, pv = _chi2_ok(counts, pb[ids])
+    assert ok, pv
+
+
+def test_race_keys_are_independent_and_deterministic():
+    rng = np.random.default_rng(13)
+    B, g, V = 16, 3, 3000
+    z = rng.normal(0, 2, (B, g + 1, V)).astype(np.float32)
+    d = (z[:, :g] + rng.normal(0, 1, (B, g, V))).astype(np.float32)
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    a = _chain(z, d, tok, r, _keys(B))
+    b = _chain(z, d, tok, r, _keys(B))
+    assert np.array_equal(a["out_tokens"], b["out_tokens"])
+    c = _chain(z, d, tok, r, _keys(B, 4242))
+    assert not np.array_equal(a["out_tokens"], c["out_tokens"])
+
+
+# ----------------------------------------------------------------- greedy
+def test_greedy_matches_numpy_argmax():
+    """T = 0: exact argmax match (first occurrence on ties, as numpy.argmax)."""
+    rng = np.random.default_rng(14)
+    B, g, V = 50, 4, 777
+    z = rng.integers(-4, 4, (B, g + 1, V)).astype(np.float32)  # many ties
+    a = z.argmax(axis=2)
+    tok = a[:, :g].astype(np.int32).copy()
+    flip = rng.random((B, g)) < 0.3
+    tok[flip] = rng.integers(0, V, flip.sum())
+    out = oracle.verify_greedy(z, tok)
+    for b in range(B):
+        k = 0
+        while k < g and tok[b, k] == a[b, k]:
+            k += 1
+        assert out["accept_count"][b] == k
+        assert list(out["out_tokens"][b, :k + 1]) == list(tok[b, :k]) + [a[b, k]]
+        assert (out["out_tokens"][b, k + 1:] == -1).all()
+    # chain entry at T = 0 routes to greedy
+    out2 = oracle.verify_chain(z, z[:, :g], tok, np.ones((B, g), np.float32), _keys(B), 0.0)
+    assert np.array_equal(out2["out_tokens"], out["out_tokens"])
+
+
+def test_greedy_negative_zero_ties_and_bad_rows():
+    z = np.zeros((3, 2, 8), np.float32)
+    z[0, 0, 2] = -0.0
+    z[0, 0, 5] = 1.0
+    z[0, 0, 6] = 1.0
+    z[0, 1, :] = -0.0
+    z[1, 0, 3] = np.nan
+    z[2, 1, 4] = np.inf
+    tok = np.array([[5], [0], [0]], np.int32)
+    out = oracle.verify_greedy(z, tok)
+    assert list(out["status"]) == [0, 4, 4]
+    assert list(out["out_tokens"][0]) == [5, 0]
+
+
+# ----------------------------------------------------------------- fan-out
+def test_fanout_sizes_golden():
+    rows = _read_golden("fanout_sizes_ssd.txt")
+    vals = [(int(r[0]), float(r[1]), int(r[2])) for r in rows if r[0] != "sum"]
+    total = [int(r[1]) for r in rows if r[0] == "sum"][0]
+    for k, f, fr in vals:
+        assert abs(oracle.fanout_size(8, 0.8, 0.5, k) - f) < 5e-6
+    sizes = oracle.fanout_sizes(8, 0.8, 0.5, 4, 128256)
+    assert sizes == [v[2] for v in vals] and sum(sizes) == total
+    # the fan-out shrinks geometrically: ratio a^(1/(1+r)) between neighbours
+    for k in range(4):
+        ratio = oracle.fanout_size(8, 0.8, 0.5, k + 1) / oracle.fanout_size(8, 0.8, 0.5, k)
+        assert abs(ratio - 0.8 ** (1 / 1.5)) < 1e-12
+
+
+@pytest.mark.parametrize("levels", [None, 8])
+def test_fanout_vs_numpy_lexsort(levels):
+    rng = np.random.default_rng(15)
+    B, K1, V = 3, 5, 3000
+    d = rng.normal(0, 2, (B, K1, V)).astype(np.float32)
+    if levels:
+        d = np.round(d * levels / 4).astype(np.float32)  # heavy ties
+        d[d == 0] = np.where(rng.random((d == 0).sum()) < 0.5, -0.0, 0.0)
+    ex = rng.integers(-1, V, (B, K1)).astype(np.int32)
+    F = [8, 7, 6, 5, 64]
+    out = oracle.fanout_topk(d, ex, F)
+    offs = np.concatenate([[0], np.cumsum(F)])
+    for b in range(B):
+        for k in range(K1):
+            v = d[b, k].astype(np.float64) + 0.0
+            ids = np.arange(V)
+            keep = ids != ex[b, k]
+            order = np.lexsort((ids[keep], -v[keep]))
+            ref = ids[keep][order][: F[k]]
+            assert list(out["ids"][b, offs[k]:offs[k + 1]]) == list(ref)
+    d[1, 2, 9] = np.nan
+    out = oracle.fanout_topk(d, ex, F)
+    assert out["status"][1, 2] == 4 and (out["status"].sum() == 4)

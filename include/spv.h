@@ -1,0 +1,165 @@
+/*
+ * spv.h -- speculative-sampling verify step on one GB300 (sm_103a).
+ *
+ * C ABI of libspv.so.  All tensors are caller-owned DEVICE memory; the
+ * library allocates nothing and frees nothing.  Every compute call is
+ * asynchronous on the caller's CUDA stream (a cudaStream_t passed as void*;
+ * NULL = legacy default stream) and returns after the launch.  Argument
+ * errors are found on the host before anything is launched.
+ *
+ * Sources (web pages; section names are the pages' own):
+ *   [SD]  "Speculative Decoding: How Draft-Model Parallelism Cuts LLM
+ *         Inference Latency", section "The four-phase loop" steps 2-4 and
+ *         "The acceptance criterion and why it is exact".
+ *   [SPD] "Speculative Pipeline Decoding: Higher-Accuracy Drafting with
+ *         Hidden Latency via Pipeline Parallelism", streaming verification
+ *         (one in-flight token per cycle: gamma = 1; greedy = exact argmax
+ *         match; sampling = standard rejection sampling).
+ *   [SSD] "Speculative Speculative Decoding" (review of arXiv 2603.03251),
+ *         Figure 2 and "Core Technical Barrier": geometric fan-out
+ *         F_k = F_0 * a_p^(k/(1+r)) of bonus-token candidates taken from the
+ *         top ranks of the draft logits, excluding the sampled token.
+ *
+ * Layouts are row-major with the vocabulary axis V contiguous.  A "row" is
+ * one V-vector of logits.  Logits are fp32 or bf16 (spv_dtype).
+ */
+#ifndef SPV_H
+#define SPV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    SPV_OK = 0,
+    SPV_ERR_INVALID_ARG = 1, /* bad pointer, size, dtype, temperature, workspace */
+    SPV_ERR_CUDA = 2,        /* a CUDA runtime call or launch failed */
+    SPV_ERR_UNSUPPORTED = 3, /* valid request outside what the build supports */
+    SPV_ERR_BAD_ROW = 4,     /* per-sequence: NaN/+inf logits, an all -inf row,
+                                or a draft token outside [0, V) */
+    SPV_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (workspace word) */
+} spv_status;
+
+typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
+
+/* Limits of this build. */
+#define SPV_MAX_GAMMA 32     /* draft tokens per sequence */
+#define SPV_MAX_FANOUT 64    /* F_k per position */
+#define SPV_MAX_FANOUT_ROWS 64 /* K + 1 positions in the fan-out */
+#define SPV_SAMPLER_BLOCK 1024 /* tokens per sampler block (part of the sampling rule) */
+#define SPV_MAX_TRIALS 64    /* residual rejection trials before the direct draw */
+
+/*
+ * spv_verify_chain -- [SD] steps 3 and 4 for B independent sequences.
+ *
+ * For each sequence b and draft position i = 0..gamma-1:
+ *   p_i = softmax(target[b,i,:] / T), q_i = softmax(draft[b,i,:] / T);
+ *   x_i = draft_tokens[b,i] is accepted iff p_i(x_i) > 0 and
+ *   r[b,i] * q_i(x_i) <= p_i(x_i)   ([SD] "accept if r_i <= min(1, p/q)").
+ * k = number of leading accepted tokens (stop at the first rejection).
+ * Emitted: x_0..x_{k-1}, then one more token:
+ *   k <  gamma: a draw from norm(max(0, p_k - q_k))   (residual, [SD] step 4)
+ *   k == gamma: a draw from p_gamma                   (bonus, [SD] step 4)
+ * T == 0 selects greedy semantics ([SPD]): identical to spv_verify_greedy;
+ * draft_logits, r and sample_keys are then not read and may be NULL.
+ *
+ * Sampling rule (exact for the stated distributions; both the library and
+ * any independent checker follow it): ids are grouped in blocks of
+ * SPV_SAMPLER_BLOCK; a draw from a distribution P picks the block with the
+ * smallest E_beta / P(block) and then the id of that block with the smallest
+ * E_x / P(x) (an exponential race; E = -ln U).  The residual is drawn by up
+ * to SPV_MAX_TRIALS rejection trials (draw x from p_k, accept iff
+ * q_k(x) <= (1 - v) p_k(x)), then, if none is accepted, by the race over
+ * max(0, p_k - q_k) directly.  Each U is ((w >> 40) + 1) * 2^-24 for one
+ * 64-bit word w of Philox4x64-10 with key (sample_keys[b], 0) and counter
+ * (n / 4, stream, trial, position), word n % 4; streams 1 block race,
+ * 2 token race, 3 trial acceptance, 4 / 5 the direct residual race.
+ *
+ * Arguments (all device pointers unless noted):
+ *   target_logits  [B, gamma+1, V] dtype
+ *   draft_logits   [B, gamma, V]   dtype            (T > 0)
+ *   draft_tokens   [B, gamma] int32
+ *   r              [B, gamma] fp32, values in (0, 1] (T > 0)
+ *   sample_keys    [B] uint64, one key per sequence (T > 0)
+ *   B >= 1, 1 <= gamma <= SPV_MAX_GAMMA, V >= 2, temperature >= 0 finite.
+ *   accept_count   [B] int32 out: k, or -1 for a bad row
+ *   out_tokens     [B, gamma+1] int32 out: k+1 ids, then -1
+ *   out_pq         [B, gamma, 2] fp32 out, optional: p_i(x_i), q_i(x_i)
+ *   out_resid_norm [B] fp32 out, optional: sum_x max(0, p_k - q_k) when
+ *                  k < gamma, 1 for the bonus.  Costs one extra read of the
+ *                  rejected row pair per sequence; pass NULL on the hot path.
+ *   row_status     [B] int32 out, optional: SPV_OK or SPV_ERR_BAD_ROW
+ *   workspace      device scratch of >= spv_chain_workspace_bytes(B,gamma,V)
+ *                  bytes, 256-byte aligned, ZERO-FILLED before its first use;
+ *                  every call leaves it zero-filled again.  One workspace
+ *                  must not be shared by calls that may overlap on the GPU.
+ *   stream         cudaStream_t (void*).
+ * Bad rows do not stop the launch: their outputs are -1 and row_status is
+ * SPV_ERR_BAD_ROW.  Returns SPV_OK once the work is enqueued.
+ */
+spv_status spv_verify_chain(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                            const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
+                            int B, int gamma, int V, float temperature,
+                            int32_t *accept_count, int32_t *out_tokens, float *out_pq,
+                            float *out_resid_norm, int32_t *row_status,
+                            void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes spv_verify_chain needs (also valid for T == 0). */
+size_t spv_chain_workspace_bytes(int B, int gamma, int V);
+
+/*
+ * spv_verify_greedy -- T = 0 ([SPD] "under greedy decoding we require an
+ * exact argmax match").  a_i = argmax_x target[b,i,x] (lowest id on ties,
+ * -0.0 equal to +0.0); x_i accepted iff x_i == a_i; stop at the first
+ * mismatch k and emit a_k there (a_gamma when all matched).  Draft logits are
+ * not needed.  Arguments as in spv_verify_chain; workspace of
+ * >= spv_greedy_workspace_bytes(B, gamma, V) bytes, zero-filled before first
+ * use and left zero-filled.
+ */
+spv_status spv_verify_greedy(const void *target_logits, spv_dtype dtype, const int32_t *draft_tokens,
+                             int B, int gamma, int V,
+                             int32_t *accept_count, int32_t *out_tokens, int32_t *row_status,
+                             void *workspace, size_t workspace_bytes, void *stream);
+
+size_t spv_greedy_workspace_bytes(int B, int gamma, int V);
+
+/*
+ * spv_fanout_topk -- [SSD] Figure 2: for each sequence b and position
+ * k = 0..K, the F_k ids with the largest draft logit draft[b,k,:], skipping
+ * exclude[b,k] (-1 = skip nothing).  Order: logit descending, then id
+ * ascending; -0.0 equals +0.0.
+ *   draft_logits [B, K+1, V] dtype (device)
+ *   exclude      [B, K+1] int32 (device)
+ *   fanout       K+1 ints, HOST array, 0 <= F_k <= min(SPV_MAX_FANOUT, V-1)
+ *   K+1 <= SPV_MAX_FANOUT_ROWS
+ *   out_ids      [B, sum_k F_k] int32 out (device), k-major then rank
+ *   row_status   [B, K+1] int32 out, optional: SPV_ERR_BAD_ROW for NaN rows
+ *                (their ids are -1)
+ *   workspace    >= spv_fanout_workspace_bytes(B, K, V, max F_k) bytes,
+ *                zero-filled before first use and left zero-filled.
+ */
+spv_status spv_fanout_topk(const void *draft_logits, spv_dtype dtype, const int32_t *exclude,
+                           const int32_t *fanout, int B, int K, int V,
+                           int32_t *out_ids, int32_t *row_status,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+size_t spv_fanout_workspace_bytes(int B, int K, int V, int max_fanout);
+
+/* [SSD] "Core Technical Barrier" (Theorem 12): F_0 * a^(k/(1+r)); the caller
+ * rounds (the fan-out workload rounds half away from zero). */
+double spv_fanout_size(int F0, double a, double r, int k);
+
+/* Reads the device error word of a workspace (synchronises `stream`):
+ * SPV_OK, or SPV_ERR_TIMEOUT if a bounded wait in an earlier call gave up. */
+spv_status spv_workspace_status(const void *workspace, void *stream);
+
+/* Human-readable name of a status code (static string). */
+const char *spv_status_string(spv_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SPV_H */

@@ -43,8 +43,9 @@
  *     w one 64-bit word of Philox4x64-10 keyed by the sequence's key.
  *   - Ties in a race, in an argmax and in the fan-out order go to the lower
  *     index; -0.0 ranks equal to +0.0.
- *   - NaN or +inf in any row read, a row without a finite entry, or a draft
- *     token outside [0, V) make the sequence a bad row (status 4).
+ *   - NaN or +inf in any row read, a row without a finite entry (in the
+ *     greedy case too), or a draft token outside [0, V) make the sequence a
+ *     bad row (status 4).
  */
 #include <math.h>
 #include <stdint.h>
@@ -215,6 +216,7 @@ static int argmax_row(const float *z, int V, int *a)
         if (isnan(v) || (isinf(v) && v > 0)) return SPVO_BAD_ROW;
         if (best < 0 || v > bv) { best = x; bv = v; }
     }
+    if (isinf(bv)) return SPVO_BAD_ROW; /* every entry is -inf */
     *a = best;
     return SPVO_OK;
 }

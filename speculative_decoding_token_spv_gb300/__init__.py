@@ -1,0 +1,237 @@
+"""Speculative-sampling verify step on GB300: Python binding of libspv.
+
+Thin ctypes marshalling over the C ABI in ``include/spv.h`` -- the functions
+keep the C names.  Tensors are torch CUDA tensors (contiguous, row-major);
+outputs and the zero-filled workspace are allocated with torch when the caller
+does not pass them.  Every step of the verify step runs in libspv's kernels on
+the tensors' device, on torch's current CUDA stream (or ``stream``).  There is
+no CPU fallback: calls fail loudly if libspv.so is missing or the tensors are
+not on a CUDA device.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspv.so")
+
+SPV_OK, SPV_ERR_INVALID_ARG, SPV_ERR_CUDA, SPV_ERR_UNSUPPORTED, SPV_ERR_BAD_ROW, SPV_ERR_TIMEOUT = range(6)
+SPV_F32, SPV_BF16 = 0, 1
+SPV_MAX_GAMMA = 32
+SPV_MAX_FANOUT = 64
+SPV_MAX_FANOUT_ROWS = 64
+SPV_SAMPLER_BLOCK = 1024
+SPV_MAX_TRIALS = 64
+
+_lib = None
+
+
+class SpvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {spv_status_string(status)} ({status})")
+        self.status = status
+
+
+def load_library():
+    """Load libspv.so (built by ``speculative_decoding_token_spv_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libspv.so not found at {LIB_PATH}: run speculative_decoding_token_spv_gb300.build "
+                           "(or __graft_entry__.build()) first")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    lib.spv_verify_chain.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, P, P, P, P, S, P]
+    lib.spv_verify_chain.restype = I
+    lib.spv_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, S, P]
+    lib.spv_verify_greedy.restype = I
+    lib.spv_fanout_topk.argtypes = [P, I, P, P, I, I, I, P, P, P, S, P]
+    lib.spv_fanout_topk.restype = I
+    lib.spv_chain_workspace_bytes.argtypes = [I, I, I]
+    lib.spv_chain_workspace_bytes.restype = S
+    lib.spv_greedy_workspace_bytes.argtypes = [I, I, I]
+    lib.spv_greedy_workspace_bytes.restype = S
+    lib.spv_fanout_workspace_bytes.argtypes = [I, I, I, I]
+    lib.spv_fanout_workspace_bytes.restype = S
+    lib.spv_fanout_size.argtypes = [I, ctypes.c_double, ctypes.c_double, I]
+    lib.spv_fanout_size.restype = ctypes.c_double
+    lib.spv_workspace_status.argtypes = [P, P]
+    lib.spv_workspace_status.restype = I
+    lib.spv_status_string.argtypes = [I]
+    lib.spv_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def spv_status_string(status: int) -> str:
+    return load_library().spv_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return SPV_F32
+    if t.dtype == torch.bfloat16:
+        return SPV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(status: int, what: str):
+    if status != SPV_OK:
+        raise SpvError(status, what)
+
+
+def spv_chain_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return load_library().spv_chain_workspace_bytes(B, gamma, V)
+
+
+def spv_greedy_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return load_library().spv_greedy_workspace_bytes(B, gamma, V)
+
+
+def spv_fanout_workspace_bytes(B: int, K: int, V: int, max_fanout: int) -> int:
+    return load_library().spv_fanout_workspace_bytes(B, K, V, max_fanout)
+
+
+def spv_fanout_size(F0: int, a: float, r: float, k: int) -> float:
+    return load_library().spv_fanout_size(int(F0), float(a), float(r), int(k))
+
+
+def new_workspace(nbytes: int, device) -> torch.Tensor:
+    """A zero-filled byte workspace (torch allocations are 512-byte aligned)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def spv_workspace_status(workspace: torch.Tensor, stream=None) -> int:
+    """Device error word of a workspace (synchronises the stream)."""
+    return load_library().spv_workspace_status(_ptr(workspace), _stream(stream, workspace.device))
+
+
+def spv_verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature: float, *,
+                     workspace=None, out=None, want_pq: bool = True, want_resid_norm: bool = False,
+                     want_status: bool = True, stream=None) -> dict:
+    """Chain verify (T > 0) or greedy (T == 0).  See spv_verify_chain in spv.h.
+
+    target_logits [B, g+1, V] and draft_logits [B, g, V] (fp32 or bf16, same
+    dtype), draft_tokens [B, g] int32, r [B, g] float32, sample_keys [B] int64
+    holding uint64 bit patterns.  Returns dict(accept_count, out_tokens, and
+    pq / resid_norm / row_status when requested)."""
+    target_logits = _cuda(target_logits, "target_logits")
+    dev = target_logits.device
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, gamma+1, V]")
+    B, g1, V = target_logits.shape
+    g = g1 - 1
+    greedy = float(temperature) == 0.0
+    dt = _dtype_code(target_logits)
+    draft_tokens = _cuda(draft_tokens, "draft_tokens", torch.int32)
+    if tuple(draft_tokens.shape) != (B, g):
+        raise ValueError("draft_tokens must be [B, gamma]")
+    if not greedy:
+        draft_logits = _cuda(draft_logits, "draft_logits", target_logits.dtype)
+        r = _cuda(r, "r", torch.float32)
+        sample_keys = _cuda(sample_keys, "sample_keys", torch.int64)
+        if tuple(draft_logits.shape) != (B, g, V) or tuple(r.shape) != (B, g) or tuple(sample_keys.shape) != (B,):
+            raise ValueError("draft_logits [B,g,V], r [B,g], sample_keys [B] expected")
+    else:
+        draft_logits = r = sample_keys = None
+    lib = load_library()
+    need = lib.spv_chain_workspace_bytes(B, g, V)
+    if workspace is None:
+        workspace = new_workspace(need, dev)
+    out = dict(out or {})
+    out.setdefault("accept_count", torch.empty(B, dtype=torch.int32, device=dev))
+    out.setdefault("out_tokens", torch.empty(B, g + 1, dtype=torch.int32, device=dev))
+    if want_pq and not greedy:
+        out.setdefault("pq", torch.empty(B, g, 2, dtype=torch.float32, device=dev))
+    if want_resid_norm and not greedy:
+        out.setdefault("resid_norm", torch.empty(B, dtype=torch.float32, device=dev))
+    if want_status:
+        out.setdefault("row_status", torch.empty(B, dtype=torch.int32, device=dev))
+    st = lib.spv_verify_chain(_ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(r),
+                              _ptr(sample_keys), B, g, V, float(temperature), _ptr(out["accept_count"]),
+                              _ptr(out["out_tokens"]), _ptr(out.get("pq")), _ptr(out.get("resid_norm")),
+                              _ptr(out.get("row_status")), _ptr(workspace), workspace.numel(),
+                              _stream(stream, dev))
+    _check(st, "spv_verify_chain")
+    return out
+
+
+def spv_verify_greedy(target_logits, draft_tokens, *, workspace=None, out=None, want_status: bool = True,
+                      stream=None) -> dict:
+    """Greedy (T = 0) verify: argmax agreement.  target_logits [B, g+1, V]."""
+    target_logits = _cuda(target_logits, "target_logits")
+    dev = target_logits.device
+    B, g1, V = target_logits.shape
+    g = g1 - 1
+    draft_tokens = _cuda(draft_tokens, "draft_tokens", torch.int32)
+    if tuple(draft_tokens.shape) != (B, g):
+        raise ValueError("draft_tokens must be [B, gamma]")
+    lib = load_library()
+    if workspace is None:
+        workspace = new_workspace(lib.spv_greedy_workspace_bytes(B, g, V), dev)
+    out = dict(out or {})
+    out.setdefault("accept_count", torch.empty(B, dtype=torch.int32, device=dev))
+    out.setdefault("out_tokens", torch.empty(B, g + 1, dtype=torch.int32, device=dev))
+    if want_status:
+        out.setdefault("row_status", torch.empty(B, dtype=torch.int32, device=dev))
+    st = lib.spv_verify_greedy(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft_tokens), B, g, V,
+                               _ptr(out["accept_count"]), _ptr(out["out_tokens"]), _ptr(out.get("row_status")),
+                               _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(st, "spv_verify_greedy")
+    return out
+
+
+def spv_fanout_topk(draft_logits, exclude, fanout, *, workspace=None, out=None, want_status: bool = True,
+                    stream=None) -> dict:
+    """Top-F_k ids per (b, k) of draft_logits [B, K+1, V], skipping exclude[b, k]."""
+    draft_logits = _cuda(draft_logits, "draft_logits")
+    dev = draft_logits.device
+    B, K1, V = draft_logits.shape
+    exclude = _cuda(exclude, "exclude", torch.int32)
+    F = [int(f) for f in fanout]
+    if len(F) != K1 or tuple(exclude.shape) != (B, K1):
+        raise ValueError("fanout needs K+1 entries and exclude [B, K+1]")
+    lib = load_library()
+    Fmax = max(F) if F else 0
+    if workspace is None:
+        workspace = new_workspace(lib.spv_fanout_workspace_bytes(B, K1 - 1, V, Fmax), dev)
+    out = dict(out or {})
+    out.setdefault("ids", torch.empty(B, sum(F), dtype=torch.int32, device=dev))
+    if want_status:
+        out.setdefault("row_status", torch.empty(B, K1, dtype=torch.int32, device=dev))
+    f_host = (ctypes.c_int32 * max(K1, 1))(*F)
+    st = lib.spv_fanout_topk(_ptr(draft_logits), _dtype_code(draft_logits), _ptr(exclude),
+                             ctypes.cast(f_host, ctypes.c_void_p), B, K1 - 1, V, _ptr(out["ids"]),
+                             _ptr(out.get("row_status")), _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(st, "spv_fanout_topk")
+    return out
+
+
+def fanout_sizes(F0: int, a: float, r: float, K: int, V: int) -> list:
+    """F_k = round(F0 * a^(k/(1+r))) for k = 0..K, half away from zero, clamped to [0, V-1]."""
+    import math
+    return [max(0, min(V - 1, int(math.floor(spv_fanout_size(F0, a, r, k) + 0.5)))) for k in range(K + 1)]

@@ -1,0 +1,175 @@
+// spv_api.cu -- the C ABI of libspv (declared in include/spv.h): argument
+// checks on the host, workspace sizing, and dispatch to the kernels.
+#include "spv.h"
+#include "spv_internal.h"
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+int elem_bytes(spv_dtype d) { return d == SPV_F32 ? 4 : 2; }
+bool dtype_ok(spv_dtype d) { return d == SPV_F32 || d == SPV_BF16; }
+
+// Every logit index must fit an int; the largest row offset must fit size_t.
+bool sizes_ok(int B, int rows_per_seq, int V)
+{
+    if (B < 1 || rows_per_seq < 1 || V < 2) return false;
+    const double total = static_cast<double>(B) * rows_per_seq * V;
+    return total < 9.0e15;
+}
+
+spv_status cuda_status(cudaError_t e) { return e == cudaSuccess ? SPV_OK : SPV_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+size_t spv_chain_workspace_bytes(int B, int gamma, int V)
+{
+    if (B < 1 || gamma < 1 || gamma > SPV_MAX_GAMMA || V < 2) return 0;
+    return spv::chain_ws_bytes(B, gamma, V);
+}
+
+size_t spv_greedy_workspace_bytes(int B, int gamma, int V)
+{
+    if (B < 1 || gamma < 1 || gamma > SPV_MAX_GAMMA || V < 2) return 0;
+    return spv::greedy_ws_bytes(B, gamma, V);
+}
+
+size_t spv_fanout_workspace_bytes(int B, int K, int V, int max_fanout)
+{
+    if (B < 1 || K < 0 || K + 1 > SPV_MAX_FANOUT_ROWS || V < 2 || max_fanout < 0 || max_fanout > SPV_MAX_FANOUT)
+        return 0;
+    return spv::fanout_ws_bytes(B, K + 1, V, max_fanout);
+}
+
+spv_status spv_verify_chain(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                            const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys, int B,
+                            int gamma, int V, float temperature, int32_t *accept_count, int32_t *out_tokens,
+                            float *out_pq, float *out_resid_norm, int32_t *row_status, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    if (!dtype_ok(dtype) || !target_logits || !draft_tokens || !accept_count || !out_tokens || !workspace)
+        return SPV_ERR_INVALID_ARG;
+    if (gamma < 1 || gamma > SPV_MAX_GAMMA || !sizes_ok(B, 2 * gamma + 1, V)) return SPV_ERR_INVALID_ARG;
+    if (!(temperature >= 0.0f) || std::isinf(temperature)) return SPV_ERR_INVALID_ARG;
+    if (!aligned256(workspace)) return SPV_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.0f;
+    const size_t need = greedy ? spv::greedy_ws_bytes(B, gamma, V) : spv::chain_ws_bytes(B, gamma, V);
+    if (workspace_bytes < need) return SPV_ERR_INVALID_ARG;
+    if (!greedy && (!draft_logits || !r || !sample_keys)) return SPV_ERR_INVALID_ARG;
+    if (!greedy && !(1.0f / temperature < INFINITY)) return SPV_ERR_INVALID_ARG;  // T too small to invert
+
+    spv::ChainLaunch L{};
+    L.target = target_logits;
+    L.draft = draft_logits;
+    L.dtype = dtype == SPV_F32 ? 0 : 1;
+    L.tokens = draft_tokens;
+    L.r = r;
+    L.keys = sample_keys;
+    L.B = B;
+    L.gamma = gamma;
+    L.V = V;
+    L.T = temperature;
+    L.accept_count = accept_count;
+    L.out_tokens = out_tokens;
+    L.out_pq = out_pq;
+    L.out_Z = out_resid_norm;
+    L.row_status = row_status;
+    L.ws = workspace;
+    const bool rows16 = (static_cast<size_t>(V) * elem_bytes(dtype)) % 16 == 0;
+    L.tma = rows16 && aligned16(target_logits) && (greedy || aligned16(draft_logits));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(greedy ? spv::launch_greedy(L, st) : spv::launch_chain(L, st));
+}
+
+spv_status spv_verify_greedy(const void *target_logits, spv_dtype dtype, const int32_t *draft_tokens, int B,
+                             int gamma, int V, int32_t *accept_count, int32_t *out_tokens, int32_t *row_status,
+                             void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!dtype_ok(dtype) || !target_logits || !draft_tokens || !accept_count || !out_tokens || !workspace)
+        return SPV_ERR_INVALID_ARG;
+    if (gamma < 1 || gamma > SPV_MAX_GAMMA || !sizes_ok(B, gamma + 1, V)) return SPV_ERR_INVALID_ARG;
+    if (!aligned256(workspace) || workspace_bytes < spv::greedy_ws_bytes(B, gamma, V)) return SPV_ERR_INVALID_ARG;
+    spv::ChainLaunch L{};
+    L.target = target_logits;
+    L.dtype = dtype == SPV_F32 ? 0 : 1;
+    L.tokens = draft_tokens;
+    L.B = B;
+    L.gamma = gamma;
+    L.V = V;
+    L.accept_count = accept_count;
+    L.out_tokens = out_tokens;
+    L.row_status = row_status;
+    L.ws = workspace;
+    L.tma = (static_cast<size_t>(V) * elem_bytes(dtype)) % 16 == 0 && aligned16(target_logits);
+    return cuda_status(spv::launch_greedy(L, static_cast<cudaStream_t>(stream)));
+}
+
+spv_status spv_fanout_topk(const void *draft_logits, spv_dtype dtype, const int32_t *exclude, const int32_t *fanout,
+                           int B, int K, int V, int32_t *out_ids, int32_t *row_status, void *workspace,
+                           size_t workspace_bytes, void *stream)
+{
+    if (!dtype_ok(dtype) || !draft_logits || !exclude || !fanout || !out_ids || !workspace)
+        return SPV_ERR_INVALID_ARG;
+    if (K < 0 || K + 1 > SPV_MAX_FANOUT_ROWS || !sizes_ok(B, K + 1, V)) return SPV_ERR_INVALID_ARG;
+    if (spv::blocks_per_row(V) > 8 * 32 * 4) return SPV_ERR_UNSUPPORTED;  // V > 1,048,576
+    spv::FanoutLaunch L{};
+    L.K1 = K + 1;
+    L.off[0] = 0;
+    L.Fmax = 0;
+    for (int k = 0; k <= K; ++k) {
+        const int f = fanout[k];
+        if (f < 0 || f > SPV_MAX_FANOUT || f > V - 1) return SPV_ERR_INVALID_ARG;
+        L.F[k] = f;
+        L.off[k + 1] = L.off[k] + f;
+        if (f > L.Fmax) L.Fmax = f;
+    }
+    if (!aligned256(workspace) || workspace_bytes < spv::fanout_ws_bytes(B, K + 1, V, L.Fmax))
+        return SPV_ERR_INVALID_ARG;
+    L.draft = draft_logits;
+    L.dtype = dtype == SPV_F32 ? 0 : 1;
+    L.exclude = exclude;
+    L.B = B;
+    L.V = V;
+    L.out_ids = out_ids;
+    L.row_status = row_status;
+    L.ws = workspace;
+    L.tma = (static_cast<size_t>(V) * elem_bytes(dtype)) % 16 == 0 && aligned16(draft_logits);
+    return cuda_status(spv::launch_fanout(L, static_cast<cudaStream_t>(stream)));
+}
+
+double spv_fanout_size(int F0, double a, double r, int k)
+{
+    return static_cast<double>(F0) * std::pow(a, static_cast<double>(k) / (1.0 + r));
+}
+
+spv_status spv_workspace_status(const void *workspace, void *stream)
+{
+    if (!workspace) return SPV_ERR_INVALID_ARG;
+    unsigned word = 0;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return SPV_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return SPV_ERR_CUDA;
+    return word == 0 ? SPV_OK : static_cast<spv_status>(word);
+}
+
+const char *spv_status_string(spv_status s)
+{
+    switch (s) {
+    case SPV_OK: return "SPV_OK";
+    case SPV_ERR_INVALID_ARG: return "SPV_ERR_INVALID_ARG";
+    case SPV_ERR_CUDA: return "SPV_ERR_CUDA";
+    case SPV_ERR_UNSUPPORTED: return "SPV_ERR_UNSUPPORTED";
+    case SPV_ERR_BAD_ROW: return "SPV_ERR_BAD_ROW";
+    case SPV_ERR_TIMEOUT: return "SPV_ERR_TIMEOUT";
+    }
+    return "SPV_ERR_UNKNOWN";
+}
+
+}  // extern "C"

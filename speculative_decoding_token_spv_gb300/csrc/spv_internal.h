@@ -1,0 +1,54 @@
+// spv_internal.h -- host-side launch interface between spv_api.cu and the
+// per-op kernel files.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace spv {
+
+// Workspace header: word 0 is the device error word (SPV_OK or
+// SPV_ERR_TIMEOUT); sections start at multiples of 256 bytes.
+constexpr size_t WS_HEADER = 256;
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline int blocks_per_row(int V) { return (V + 1023) / 1024; }
+inline int chunks_per_row(int V) { return (V + 8191) / 8192; }
+
+struct ChainLaunch {
+    const void *target, *draft;
+    int dtype;  // 0 fp32, 1 bf16
+    const int32_t *tokens;
+    const float *r;
+    const uint64_t *keys;
+    int B, gamma, V;
+    float T;
+    int32_t *accept_count, *out_tokens;
+    float *out_pq, *out_Z;
+    int32_t *row_status;
+    void *ws;
+    bool tma;  // rows are 16-byte aligned and V * elem_bytes % 16 == 0
+};
+
+struct FanoutLaunch {
+    const void *draft;
+    int dtype;
+    const int32_t *exclude;
+    int F[64];
+    int off[65];
+    int Fmax;
+    int B, K1, V;
+    int32_t *out_ids, *row_status;
+    void *ws;
+    bool tma;
+};
+
+size_t chain_ws_bytes(int B, int gamma, int V);
+size_t greedy_ws_bytes(int B, int gamma, int V);
+size_t fanout_ws_bytes(int B, int K1, int V, int Fmax);
+
+cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st);
+cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st);
+cudaError_t launch_fanout(const FanoutLaunch &L, cudaStream_t st);
+
+}  // namespace spv

@@ -1,0 +1,398 @@
+// spv_stream.cuh -- device building blocks of libspv (sm_103a).
+//
+// * A streaming pipeline that reads every logit row of a call exactly once:
+//   rows are cut into work items of SPV_CHUNK contiguous logits; a producer
+//   warp stages items in a ring of shared-memory buffers with TMA bulk copies
+//   (cp.async.bulk, global -> shared, completion on an mbarrier), and eight
+//   consumer warps reduce one sampler block (1024 logits) each.  Per-block
+//   partial results go to a small workspace; the CTA that completes the last
+//   item of a sequence (or row) merges them and writes the outputs
+//   (threadfence + atomic counter, no spinning on other CTAs).
+// * Philox4x64-10 and the uniform / exponential variates of the sampling rule.
+// * Warp reductions and order-preserving float keys.
+//
+// Every wait on an mbarrier is bounded; a wait that gives up records
+// SPV_ERR_TIMEOUT in the workspace error word and the CTA stops cleanly.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spv {
+
+constexpr int G = 1024;                       // sampler block: tokens per block
+constexpr int CHUNK_BLOCKS = 8;               // sampler blocks per work item
+constexpr int CHUNK = G * CHUNK_BLOCKS;       // logits per work item
+constexpr int NCW = 8;                        // consumer warps (one block each)
+constexpr int THREADS = (NCW + 1) * 32;       // + one producer warp
+constexpr int STAGE_BYTES_BUDGET = 96 * 1024; // ring size: two CTAs fit on an SM
+constexpr uint32_t WAIT_LIMIT = 1u << 22;     // try_wait polls before giving up
+constexpr int MAX_TRIALS = 64;                // residual rejection trials
+constexpr int STATUS_BAD_ROW = 4;
+constexpr int STATUS_TIMEOUT = 5;
+
+// Philox stream tags (second counter word).
+constexpr uint64_t STREAM_BLOCK = 1, STREAM_TOKEN = 2, STREAM_ACCEPT = 3, STREAM_FB_BLOCK = 4,
+                   STREAM_FB_TOKEN = 5;
+
+template <int DT> struct DType;
+template <> struct DType<0> {  // fp32
+    using T = float;
+    static constexpr int BYTES = 4;
+    __device__ static __forceinline__ float load(const void *p, long long i) {
+        return __ldg(reinterpret_cast<const float *>(p) + i);
+    }
+};
+template <> struct DType<1> {  // bf16
+    using T = __nv_bfloat16;
+    static constexpr int BYTES = 2;
+    __device__ static __forceinline__ float load(const void *p, long long i) {
+        unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(p) + i);
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+};
+
+template <int DT> constexpr int stages()
+{
+    return STAGE_BYTES_BUDGET / (CHUNK * DType<DT>::BYTES);
+}
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait for the phase of `parity` to complete; false if it gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// TMA bulk copy global -> shared of `bytes` (multiple of 16, both addresses
+// 16-byte aligned), completing on `bar` with `bytes` transaction count.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory");
+}
+
+__device__ __forceinline__ float fast_exp2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ------------------------------------------------------------------ warp reductions
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// argmax of (score, index): larger score wins, ties go to the lower index.
+__device__ __forceinline__ void warp_argmax(float &s, int &i)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        if (s2 > s || (s2 == s && i2 < i)) {
+            s = s2;
+            i = i2;
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t warp_max_u64(uint64_t v)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        uint64_t w = __shfl_xor_sync(0xffffffffu, v, o);
+        v = w > v ? w : v;
+    }
+    return v;
+}
+
+// Order-preserving 32-bit key of a float (NaN excluded by the caller);
+// -0.0 maps like +0.0.  Every key of a non-NaN float is >= 0x007FFFFF.
+__device__ __forceinline__ uint32_t float_key(float x)
+{
+    uint32_t b = __float_as_uint(x);
+    if (b == 0x80000000u) b = 0u;
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// ------------------------------------------------------------------ Philox4x64-10
+// Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
+// (SC'11): ten rounds; each multiplies counter words 0 and 2 by two fixed
+// 64-bit constants and mixes the halves with the other words and the key,
+// which is bumped by two Weyl constants between rounds.
+__device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64_t k1)
+{
+    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
+    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        if (round) {
+            k0 += W0;
+            k1 += W1;
+        }
+        const uint64_t lo0 = M0 * c[0], hi0 = __umul64hi(M0, c[0]);
+        const uint64_t lo1 = M1 * c[2], hi1 = __umul64hi(M1, c[2]);
+        const uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        c[0] = n0;
+        c[1] = lo1;
+        c[2] = n2;
+        c[3] = lo0;
+    }
+}
+
+// The four words of draw group `grp` (draws 4*grp .. 4*grp+3) of one stream.
+__device__ __forceinline__ void philox_group(uint64_t w[4], uint64_t key, uint64_t stream, uint32_t trial,
+                                             uint32_t pos, uint64_t grp)
+{
+    w[0] = grp;
+    w[1] = stream;
+    w[2] = trial;
+    w[3] = pos;
+    philox4x64_10(w, key, 0);
+}
+
+// U = ((w >> 40) + 1) * 2^-24 in (0, 1], exact in fp32.
+__device__ __forceinline__ float uniform24(uint64_t w)
+{
+    return static_cast<float>(static_cast<uint32_t>(w >> 40) + 1u) * 0x1p-24f;
+}
+
+// ln E for E = -ln U; -inf when U == 1 (E == 0: an arrival at time zero).
+__device__ __forceinline__ float log_expo(uint64_t w)
+{
+    const float u = uniform24(w);
+    if (u == 1.0f) return -INFINITY;
+    return logf(-logf(u));
+}
+
+// ------------------------------------------------------------------ block loads
+// Lane `lane` owns 32 logits of a 1024-logit block; element e of the lane is
+// block index idx(e).  fp32: 8 x float4 at j*128 + lane*4; bf16: 4 x 8 at
+// j*256 + lane*8.  Both orders rise with e.
+template <int DT> __device__ __forceinline__ int lane_index(int lane, int e)
+{
+    if (DT == 0) return (e >> 2) * 128 + lane * 4 + (e & 3);
+    return (e >> 3) * 256 + lane * 8 + (e & 7);
+}
+
+// From shared memory (16-byte vector loads; the block starts 16-byte aligned).
+template <int DT> __device__ __forceinline__ void load_block_smem(float v[32], const unsigned char *blk, int lane)
+{
+    if (DT == 0) {
+        const float4 *p = reinterpret_cast<const float4 *>(blk);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float4 t = p[j * 32 + lane];
+            v[4 * j] = t.x;
+            v[4 * j + 1] = t.y;
+            v[4 * j + 2] = t.z;
+            v[4 * j + 3] = t.w;
+        }
+    } else {
+        const uint4 *p = reinterpret_cast<const uint4 *>(blk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint4 t = p[j * 32 + lane];
+            const uint32_t w[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                v[8 * j + 2 * h] = __uint_as_float(w[h] << 16);
+                v[8 * j + 2 * h + 1] = __uint_as_float(w[h] & 0xffff0000u);
+            }
+        }
+    }
+}
+
+// From global memory, scalar loads (any alignment); elements >= valid are -inf.
+template <int DT>
+__device__ __forceinline__ void load_block_global(float v[32], const void *blk, int lane, int valid)
+{
+#pragma unroll
+    for (int e = 0; e < 32; ++e) {
+        const int i = lane_index<DT>(lane, e);
+        v[e] = i < valid ? DType<DT>::load(blk, i) : -INFINITY;
+    }
+}
+
+// ------------------------------------------------------------------ the pipeline
+// Op supplies:
+//   struct Params  -- with total_items, nc (items per row), nb (blocks per
+//                     row), V, counter, err fields;
+//   row_ptr(P, row)                 global address of a row;
+//   block(P, row, beta, v, valid, lane)  per-warp reduction of one block;
+//   group(P, row), items_per_group(P)    counter slot and its item count;
+//   finalize(P, g, sm, warp, lane)      merge + outputs for a finished group;
+//   struct Smem                     shared scratch of finalize.
+template <class Op, int DT, bool TMA> __global__ void __launch_bounds__(THREADS, 2) stream_kernel(const typename Op::Params P)
+{
+    constexpr int EB = DType<DT>::BYTES;
+    constexpr int S = stages<DT>();
+    constexpr int CHUNK_BYTES = CHUNK * EB;
+    extern __shared__ __align__(128) unsigned char ring[];
+    __shared__ __align__(8) uint64_t full_bar[S];
+    __shared__ __align__(8) uint64_t empty_bar[S];
+    __shared__ int sh_group;
+    __shared__ volatile int sh_abort;
+    __shared__ typename Op::Smem sm;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], NCW);
+        }
+        sh_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    const long long total = P.total_items;
+    const int nc = P.nc;
+
+    if (warp == NCW) {  // ---------------- producer
+        if (TMA && lane == 0) {
+            const uint64_t pol = l2_evict_first_policy();
+            int i = 0;
+            for (long long it = blockIdx.x; it < total; it += gridDim.x, ++i) {
+                const int s = i % S;
+                const uint32_t ph = (i / S) & 1;
+                if (!mbar_wait(&empty_bar[s], ph ^ 1u)) {
+                    atomicExch(P.err, STATUS_TIMEOUT);
+                    sh_abort = 1;
+                    break;
+                }
+                if (sh_abort) break;
+                const long long row = it / nc;
+                const int c = static_cast<int>(it - row * nc);
+                const int n = min(CHUNK, P.V - c * CHUNK);
+                const unsigned char *src =
+                    reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) + static_cast<size_t>(c) * CHUNK_BYTES;
+                mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(n * EB));
+                bulk_g2s(ring + s * CHUNK_BYTES, src, static_cast<uint32_t>(n * EB), &full_bar[s], pol);
+            }
+            // No copy may still be writing this CTA's shared memory at exit.
+            for (int k = max(0, i - S); k < i; ++k) mbar_wait(&full_bar[k % S], (k / S) & 1);
+        }
+        return;
+    }
+
+    // ---------------- consumers
+    int i = 0;
+    for (long long it = blockIdx.x; it < total; it += gridDim.x, ++i) {
+        const int s = i % S;
+        const uint32_t ph = (i / S) & 1;
+        bool ok = true;
+        if (TMA) {
+            ok = mbar_wait(&full_bar[s], ph);
+            if (!ok) {
+                atomicExch(P.err, STATUS_TIMEOUT);
+                sh_abort = 1;
+            }
+        }
+        const long long row = it / nc;
+        const int c = static_cast<int>(it - row * nc);
+        const int beta = c * CHUNK_BLOCKS + warp;
+        if (ok && beta < P.nb) {
+            const int valid = min(G, P.V - beta * G);
+            float v[32];
+            if (TMA) {
+                load_block_smem<DT>(v, ring + s * CHUNK_BYTES + warp * G * EB, lane);
+                if (valid < G) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (lane_index<DT>(lane, e) >= valid) v[e] = -INFINITY;
+                }
+            } else {
+                const unsigned char *blk = reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) +
+                                           static_cast<size_t>(beta) * G * EB;
+                load_block_global<DT>(v, blk, lane, valid);
+            }
+            Op::block(P, row, beta, v, valid, lane);
+        }
+        if (TMA) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[s]);
+        }
+        consumer_sync();
+        if (sh_abort) break;
+        if (threadIdx.x == 0) {
+            __threadfence();
+            const int g = Op::group(P, row);
+            const unsigned old = atomicAdd(&P.counter[g], 1u);
+            sh_group = (old == static_cast<unsigned>(Op::items_per_group(P) - 1)) ? g : -1;
+        }
+        consumer_sync();
+        const int g = sh_group;
+        if (g >= 0) {
+            __threadfence();
+            Op::finalize(P, g, sm, warp, lane);
+        }
+    }
+}
+
+}  // namespace spv

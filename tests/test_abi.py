@@ -1,0 +1,97 @@
+"""Host-side checks of libspv that need no GPU: it builds, loads, exports every
+function spv.h declares, sizes workspaces, and rejects bad arguments on the
+host before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_token_spv_gb300 import build
+    build.build_library()
+    import speculative_decoding_token_spv_gb300 as spv
+    return spv.load_library()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "spv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(spv_[a-z_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared_functions()
+    assert {"spv_verify_chain", "spv_verify_greedy", "spv_fanout_topk"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_sizes(lib):
+    import speculative_decoding_token_spv_gb300 as spv
+    a = spv.spv_chain_workspace_bytes(64, 4, 151936)
+    g = spv.spv_greedy_workspace_bytes(64, 4, 151936)
+    f = spv.spv_fanout_workspace_bytes(8, 4, 128256, 8)
+    assert a >= g > 0 and f > 0
+    nb = (151936 + 1023) // 1024
+    assert a >= 64 * 9 * nb * 8
+    assert spv.spv_chain_workspace_bytes(0, 4, 100) == 0
+    assert spv.spv_chain_workspace_bytes(1, 33, 100) == 0
+    assert spv.spv_fanout_workspace_bytes(1, 64, 100, 1) == 0
+
+
+def test_fanout_size_and_status_strings(lib):
+    import speculative_decoding_token_spv_gb300 as spv
+    assert spv.fanout_sizes(8, 0.8, 0.5, 4, 128256) == [8, 7, 6, 5, 4]
+    assert abs(spv.spv_fanout_size(8, 0.8, 0.5, 3) - 5.12) < 1e-12
+    for code in range(6):
+        assert spv.spv_status_string(code).startswith("SPV_")
+
+
+def test_invalid_arguments_rejected_on_host(lib):
+    """Each of these fails validation before the library touches CUDA."""
+    P = ctypes.c_void_p
+    fake = P(4096)   # never dereferenced: validation fails first
+    ws = P(1 << 20)
+    big = 1 << 40
+    INV = 1
+    chain = lib.spv_verify_chain
+    ok_args = dict(t=fake, d=fake, dt=0, tok=fake, r=fake, keys=fake, B=4, g=4, V=1000, T=1.0, k=fake,
+                   out=fake, pq=None, z=None, st=None, ws=ws, wsb=big, stream=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return chain(a["t"], a["d"], a["dt"], a["tok"], a["r"], a["keys"], a["B"], a["g"], a["V"],
+                     ctypes.c_float(a["T"]), a["k"], a["out"], a["pq"], a["z"], a["st"], a["ws"], a["wsb"],
+                     a["stream"])
+
+    assert call(t=None) == INV
+    assert call(tok=None) == INV
+    assert call(dt=7) == INV
+    assert call(B=0) == INV
+    assert call(g=0) == INV
+    assert call(g=33) == INV
+    assert call(V=1) == INV
+    assert call(T=-1.0) == INV
+    assert call(T=float("nan")) == INV
+    assert call(T=float("inf")) == INV
+    assert call(T=1e-45) == INV          # 1/T overflows
+    assert call(d=None) == INV           # T > 0 needs draft logits, r and keys
+    assert call(r=None) == INV
+    assert call(keys=None) == INV
+    assert call(wsb=16) == INV           # workspace too small
+    assert call(ws=P((1 << 20) + 8)) == INV  # workspace not 256-byte aligned
+    greedy = lib.spv_verify_greedy
+    assert greedy(fake, 0, fake, 4, 0, 1000, fake, fake, None, ws, big, None) == INV
+    assert greedy(fake, 0, None, 4, 2, 1000, fake, fake, None, ws, big, None) == INV
+    fan = lib.spv_fanout_topk
+    f_bad = (ctypes.c_int32 * 2)(3, 65)
+    f_big = (ctypes.c_int32 * 2)(3, 10)
+    assert fan(fake, 0, fake, ctypes.cast(f_bad, P), 2, 1, 1000, fake, None, ws, big, None) == INV
+    assert fan(fake, 0, fake, ctypes.cast(f_big, P), 2, 1, 10, fake, None, ws, big, None) == INV   # F > V-1
+    assert fan(fake, 0, fake, ctypes.cast(f_big, P), 2, 64, 1000, fake, None, ws, big, None) == INV
+    assert fan(fake, 0, fake, ctypes.cast(f_big, P), 2, 1, 2_000_000, fake, None, ws, big, None) == 3

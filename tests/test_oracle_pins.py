@@ -399,16 +399,17 @@ def test_greedy_matches_numpy_argmax():
 
 
 def test_greedy_negative_zero_ties_and_bad_rows():
-    z = np.zeros((3, 2, 8), np.float32)
+    z = np.zeros((4, 2, 8), np.float32)
     z[0, 0, 2] = -0.0
     z[0, 0, 5] = 1.0
     z[0, 0, 6] = 1.0
     z[0, 1, :] = -0.0
     z[1, 0, 3] = np.nan
     z[2, 1, 4] = np.inf
-    tok = np.array([[5], [0], [0]], np.int32)
+    z[3, 1, :] = -np.inf
+    tok = np.array([[5], [0], [0], [0]], np.int32)
     out = oracle.verify_greedy(z, tok)
-    assert list(out["status"]) == [0, 4, 4]
+    assert list(out["status"]) == [0, 4, 4, 4]
     assert list(out["out_tokens"][0]) == [5, 0]
 
 

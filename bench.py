@@ -100,6 +100,13 @@ def dist_sum(x: float, world: int) -> float:
     return float(t.item())
 
 
+def aggregate(rows_local: float, ms_local: float, world: int):
+    """Whole-job throughput: rows of all ranks over the slowest rank's time."""
+    ms_max = dist_max(ms_local, world)
+    total_rows = dist_sum(rows_local, world)
+    return total_rows / (ms_max * 1e-3), ms_max, total_rows
+
+
 # ----------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
@@ -259,7 +266,8 @@ def run_spv(args, rank, world):
     with ClockSampler(local) as clk:
         ms = time_device(step, args.steps, args.warmup, stream)
     dist_barrier(world)
-    ms_max = dist_max(ms, world)
+    rows = B * (g + 1)
+    value, ms_max, total_rows = aggregate(float(rows), ms, world)
     clocks = clk.summary()
     assert spv.spv_workspace_status(ws) == spv.SPV_OK
 
@@ -287,9 +295,6 @@ def run_spv(args, rank, world):
     ms_e2e = time_device(e2e_step, e2e_steps, 2, stream)
     ms_e2e_max = dist_max(ms_e2e, world)
 
-    rows = B * (g + 1)
-    total_rows = dist_sum(float(rows), world)
-    value = total_rows / (ms_max * 1e-3)
     peak, peak_kind = measured_peaks()
     achieved = algo / (ms * 1e-3) / 1e9
     line = {
@@ -436,6 +441,35 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def profile_case(args):
+    """Run one workload `--iters` times with no timing (a small command for ncu)."""
+    import torch
+
+    import speculative_decoding_token_spv_gb300 as spv
+    from speculative_decoding_token_spv_gb300 import build as spv_build
+    from speculative_decoding_token_spv_gb300 import workloads
+    spv_build.build_library()
+    dev = torch.device("cuda", 0)
+    name, dt, B, T = args.profile_case, getattr(torch, args.dtype), args.B, args.T
+    if name == "fanout":
+        fw = workloads.fanout(device=dev)
+        ws = spv.new_workspace(spv.spv_fanout_workspace_bytes(fw.draft.shape[0], 4, fw.draft.shape[2], 8), dev)
+        for _ in range(args.iters):
+            spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws)
+    else:
+        if name == "sweep":
+            w = workloads.sweep(B=B, dtype=dt, device=dev, temperature=T)
+        elif name == "spd":
+            w = workloads.spd(device=dev, temperature=T)
+        else:
+            w = workloads.eagle(gamma=int(name[5:] or 7), device=dev, temperature=T)
+        ws = spv.new_workspace(spv.spv_chain_workspace_bytes(w.B, w.gamma, w.V), dev)
+        for _ in range(args.iters):
+            spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature, workspace=ws)
+    torch.cuda.synchronize()
+    print("profile case done:", name, args.dtype, B, T, args.iters)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -444,7 +478,15 @@ def main(argv=None):
     ap.add_argument("--impl", default="spv", choices=["spv", "reference"])
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None, help="sweep | spd | eagle7 | eagle15 | fanout")
+    ap.add_argument("--dtype", default="float32")
+    ap.add_argument("--B", type=int, default=64)
+    ap.add_argument("--T", type=float, default=1.0)
+    ap.add_argument("--iters", type=int, default=4)
     args = ap.parse_args(argv)
+    if args.profile_case:
+        profile_case(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     rank, world = dist_init()

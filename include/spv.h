@@ -49,7 +49,8 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
 #define SPV_MAX_GAMMA 32     /* draft tokens per sequence */
 #define SPV_MAX_FANOUT 64    /* F_k per position */
 #define SPV_MAX_FANOUT_ROWS 64 /* K + 1 positions in the fan-out */
-#define SPV_SAMPLER_BLOCK 1024 /* tokens per sampler block (part of the sampling rule) */
+#define SPV_SAMPLER_BLOCK 1024 /* ids per sampler block (part of the sampling rule) */
+#define SPV_SAMPLER_SUB 32     /* ids per sampler sub-block (part of the sampling rule) */
 #define SPV_MAX_TRIALS 64    /* residual rejection trials before the direct draw */
 
 /*
@@ -68,15 +69,19 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
  *
  * Sampling rule (exact for the stated distributions; both the library and
  * any independent checker follow it): ids are grouped in blocks of
- * SPV_SAMPLER_BLOCK; a draw from a distribution P picks the block with the
- * smallest E_beta / P(block) and then the id of that block with the smallest
- * E_x / P(x) (an exponential race; E = -ln U).  The residual is drawn by up
- * to SPV_MAX_TRIALS rejection trials (draw x from p_k, accept iff
- * q_k(x) <= (1 - v) p_k(x)), then, if none is accepted, by the race over
- * max(0, p_k - q_k) directly.  Each U is ((w >> 40) + 1) * 2^-24 for one
- * 64-bit word w of Philox4x64-10 with key (sample_keys[b], 0) and counter
- * (n / 4, stream, trial, position), word n % 4; streams 1 block race,
- * 2 token race, 3 trial acceptance, 4 / 5 the direct residual race.
+ * SPV_SAMPLER_BLOCK ids and each block in sub-blocks of SPV_SAMPLER_SUB ids.
+ * A draw from a distribution P is an exponential race at three levels: the
+ * block with the smallest E / P(block) wins, then inside it the sub-block
+ * with the smallest E / P(sub-block), then the id with the smallest E / P(id)
+ * (E = -ln U, ties to the lower index).  The residual is drawn by up to
+ * SPV_MAX_TRIALS rejection trials (draw x from p_k, accept iff
+ * q_k(x) <= (1 - v) p_k(x)), then, if none is accepted, by the same race over
+ * max(0, p_k - q_k) directly.  U = ((w >> 8) + 1) * 2^-24 for one 32-bit
+ * word w of Philox4x32-10 with key (low, high half of sample_keys[b]) and
+ * counter (n / 4, stream, trial, position), word n % 4, where n is the
+ * block, global sub-block (id / 32) or id index; streams 1 / 2 / 3 block /
+ * sub-block / id race, 4 trial acceptance, 5 / 6 / 7 the direct residual
+ * race.  Trials are numbered from 0; the bonus is trial 0 at position gamma.
  *
  * Arguments (all device pointers unless noted):
  *   target_logits  [B, gamma+1, V] dtype
@@ -93,10 +98,13 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
  *                  rejected row pair per sequence; pass NULL on the hot path.
  *   row_status     [B] int32 out, optional: SPV_OK or SPV_ERR_BAD_ROW
  *   workspace      device scratch of >= spv_chain_workspace_bytes(B,gamma,V)
- *                  bytes, 256-byte aligned, ZERO-FILLED before its first use;
- *                  every call leaves it zero-filled again.  One workspace
- *                  must not be shared by calls that may overlap on the GPU.
- *   stream         cudaStream_t (void*).
+ *                  bytes, 256-byte aligned.  Its first 4 bytes are a sticky
+ *                  error word (see spv_workspace_status): zero-fill the
+ *                  workspace once before its first use.  One workspace must
+ *                  not be shared by calls that may overlap on the GPU.
+ *   stream         cudaStream_t (void*).  Two kernels are enqueued: the
+ *                  streaming pass and, as a programmatic dependent launch,
+ *                  the per-sequence finalize.
  * Bad rows do not stop the launch: their outputs are -1 and row_status is
  * SPV_ERR_BAD_ROW.  Returns SPV_OK once the work is enqueued.
  */
@@ -116,8 +124,7 @@ size_t spv_chain_workspace_bytes(int B, int gamma, int V);
  * -0.0 equal to +0.0); x_i accepted iff x_i == a_i; stop at the first
  * mismatch k and emit a_k there (a_gamma when all matched).  Draft logits are
  * not needed.  Arguments as in spv_verify_chain; workspace of
- * >= spv_greedy_workspace_bytes(B, gamma, V) bytes, zero-filled before first
- * use and left zero-filled.
+ * >= spv_greedy_workspace_bytes(B, gamma, V) bytes (zero-filled once).
  */
 spv_status spv_verify_greedy(const void *target_logits, spv_dtype dtype, const int32_t *draft_tokens,
                              int B, int gamma, int V,
@@ -138,8 +145,8 @@ size_t spv_greedy_workspace_bytes(int B, int gamma, int V);
  *   out_ids      [B, sum_k F_k] int32 out (device), k-major then rank
  *   row_status   [B, K+1] int32 out, optional: SPV_ERR_BAD_ROW for NaN rows
  *                (their ids are -1)
- *   workspace    >= spv_fanout_workspace_bytes(B, K, V, max F_k) bytes,
- *                zero-filled before first use and left zero-filled.
+ *   workspace    >= spv_fanout_workspace_bytes(B, K, V, max F_k) bytes
+ *                (zero-filled once, as for spv_verify_chain).
  */
 spv_status spv_fanout_topk(const void *draft_logits, spv_dtype dtype, const int32_t *exclude,
                            const int32_t *fanout, int B, int K, int V,

@@ -25,8 +25,10 @@ _SRC = os.path.join(_HERE, "spv_oracle.c")
 _LIB = os.path.join(_HERE, "_build", "liboracle_spv.so")
 
 BLOCK = 1024          # tokens per sampler block (must equal the C constant)
+SUB = 32              # tokens per sampler sub-block
 MAX_TRIALS = 64       # residual rejection trials before the direct fallback
-STREAM_BLOCK, STREAM_TOKEN, STREAM_ACCEPT, STREAM_FB_BLOCK, STREAM_FB_TOKEN = 1, 2, 3, 4, 5
+(STREAM_BLOCK, STREAM_SUB, STREAM_TOKEN, STREAM_ACCEPT,
+ STREAM_FB_BLOCK, STREAM_FB_SUB, STREAM_FB_TOKEN) = 1, 2, 3, 4, 5, 6, 7
 OK, BAD_ROW = 0, 4
 
 _lib = None
@@ -48,7 +50,7 @@ def _load():
     if _lib is None:
         lib = ctypes.CDLL(build())
         P = ctypes.c_void_p
-        lib.spvo_philox4x64_10.argtypes = [P, P, P]
+        lib.spvo_philox4x32_10.argtypes = [P, P, P]
         lib.spvo_uniform.argtypes = [ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
                                      ctypes.c_uint64]
         lib.spvo_uniform.restype = ctypes.c_double
@@ -80,12 +82,12 @@ def _threads(threads):
 
 
 # ---------------------------------------------------------------- primitives
-def philox4x64_10(counter, key) -> np.ndarray:
-    """One Philox4x64-10 block: 4 uint64 words for a 4-word counter, 2-word key."""
-    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint64))
-    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint64))
-    out = np.zeros(4, dtype=np.uint64)
-    _load().spvo_philox4x64_10(_ptr(c), _ptr(k), _ptr(out))
+def philox4x32_10(counter, key) -> np.ndarray:
+    """One Philox4x32-10 block: 4 uint32 words for a 4-word counter, 2-word key."""
+    c = np.ascontiguousarray(np.asarray(counter, dtype=np.uint32))
+    k = np.ascontiguousarray(np.asarray(key, dtype=np.uint32))
+    out = np.zeros(4, dtype=np.uint32)
+    _load().spvo_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
     return out
 
 

@@ -29,18 +29,20 @@
  *     division; p = 0 always rejects, q == p always accepts.
  *   - "Sample from" ([SD] step 4) is realised by an exponential race, which
  *     draws exactly from the stated distribution:
- *       * tokens are grouped in blocks of SPVO_BLOCK ids; block beta wins the
- *         block race if E_beta / W_beta is smallest (W_beta = the block's
- *         probability mass, E_beta ~ Exp(1)); then token x of the winning
- *         block wins if E_x / P(x) is smallest.  P(x) = W_beta/Z * P(x)/W_beta.
+ *       * ids are grouped in blocks of SPVO_BLOCK ids and each block in
+ *         sub-blocks of SPVO_SUB ids.  The block with the smallest
+ *         E_beta / W_beta wins (W_beta = the block's probability mass,
+ *         E_beta ~ Exp(1)); inside it the sub-block with the smallest
+ *         E_s / W_s; inside that the id with the smallest E_x / P(x).
+ *         P(x) = W_beta/Z * W_s/W_beta * P(x)/W_s.
  *       * The residual norm(max(0, p - q)) is drawn by rejection: draw x from
  *         p by the race above, accept it with probability max(0, 1 - q/p)
  *         (i.e. iff q(x) <= (1 - v) p(x)); accepted draws have density
  *         proportional to p * (1 - q/p)+ = (p - q)+.  After SPVO_MAX_TRIALS
  *         failed trials the residual is drawn directly by the same race over
  *         the residual masses, so the output stays exact.
- *     Every exponential comes from E = -ln U, U = ((w >> 40) + 1) * 2^-24,
- *     w one 64-bit word of Philox4x64-10 keyed by the sequence's key.
+ *     Every exponential comes from E = -ln U, U = ((w >> 8) + 1) * 2^-24,
+ *     w one 32-bit word of Philox4x32-10 keyed by the sequence's 64-bit key.
  *   - Ties in a race, in an argmax and in the fan-out order go to the lower
  *     index; -0.0 ranks equal to +0.0.
  *   - NaN or +inf in any row read, a row without a finite entry (in the
@@ -53,61 +55,58 @@
 #include <string.h>
 
 #define SPVO_BLOCK 1024
+#define SPVO_SUB 32
 #define SPVO_MAX_TRIALS 64
 
 /* Stream tags: the second counter word of every Philox draw. */
 #define SPVO_STREAM_BLOCK 1u
-#define SPVO_STREAM_TOKEN 2u
-#define SPVO_STREAM_ACCEPT 3u
-#define SPVO_STREAM_FB_BLOCK 4u
-#define SPVO_STREAM_FB_TOKEN 5u
+#define SPVO_STREAM_SUB 2u
+#define SPVO_STREAM_TOKEN 3u
+#define SPVO_STREAM_ACCEPT 4u
+#define SPVO_STREAM_FB_BLOCK 5u
+#define SPVO_STREAM_FB_SUB 6u
+#define SPVO_STREAM_FB_TOKEN 7u
 
 #define SPVO_OK 0
 #define SPVO_BAD_ROW 4
 
 /* ------------------------------------------------------------------------ */
-/* Philox4x64-10, from its published definition (Salmon, Moraes, Dror, Shaw,
- * "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): ten rounds of two
- * 64x64->128 multiplies, with the key bumped by two Weyl constants between
- * rounds. */
-static void mulhilo64(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo)
+/* Philox4x32-10, from its published definition (Salmon, Moraes, Dror, Shaw,
+ * "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): ten rounds; each
+ * multiplies counter words 0 and 2 by two 32-bit constants (64-bit products)
+ * and mixes the halves with the other words and the key, which is bumped by
+ * two Weyl constants between rounds. */
+void spvo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
 {
-    unsigned __int128 p = (unsigned __int128)a * (unsigned __int128)b;
-    *hi = (uint64_t)(p >> 64);
-    *lo = (uint64_t)p;
-}
-
-void spvo_philox4x64_10(const uint64_t ctr[4], const uint64_t key[2], uint64_t out[4])
-{
-    uint64_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
-    uint64_t k0 = key[0], k1 = key[1];
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
     for (int round = 0; round < 10; ++round) {
         if (round > 0) {
-            k0 += 0x9E3779B97F4A7C15ull;
-            k1 += 0xBB67AE8584CAA73Bull;
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
         }
-        uint64_t hi0, lo0, hi1, lo1;
-        mulhilo64(0xD2E7470EE14C6C93ull, c0, &hi0, &lo0);
-        mulhilo64(0xCA5A826395121157ull, c2, &hi1, &lo1);
-        uint64_t n0 = hi1 ^ c1 ^ k0;
-        uint64_t n1 = lo1;
-        uint64_t n2 = hi0 ^ c3 ^ k1;
-        uint64_t n3 = lo0;
+        uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
         c0 = n0; c1 = n1; c2 = n2; c3 = n3;
     }
     out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
 }
 
 /* Uniform in (0,1] for draw n of (stream, trial, position) of one sequence:
- * counter = (n / 4, stream, trial, position), key = (seq_key, 0), word n % 4. */
+ * counter = (n / 4, stream, trial, position), key = (low, high 32 bits of the
+ * sequence key), word n % 4, U = ((w >> 8) + 1) * 2^-24. */
 double spvo_uniform(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t pos, uint64_t n)
 {
-    uint64_t ctr[4] = { n >> 2, (uint64_t)stream, (uint64_t)trial, (uint64_t)pos };
-    uint64_t key[2] = { seq_key, 0 };
-    uint64_t out[4];
-    spvo_philox4x64_10(ctr, key, out);
-    uint64_t w = out[n & 3u];
-    return (double)((w >> 40) + 1u) * ldexp(1.0, -24);
+    uint32_t ctr[4] = { (uint32_t)(n >> 2), stream, trial, pos };
+    uint32_t key[2] = { (uint32_t)seq_key, (uint32_t)(seq_key >> 32) };
+    uint32_t out[4];
+    spvo_philox4x32_10(ctr, key, out);
+    uint32_t w = out[n & 3u];
+    return (double)((w >> 8) + 1u) * ldexp(1.0, -24);
 }
 
 /* Exp(1) variate from the same draw: E = -ln U. */
@@ -179,25 +178,38 @@ static int race_winner(const double *a, int n, double *margin)
 }
 
 /* Draw one token from the distribution with (unnormalised) masses w[0..V)
- * by the two-level exponential race described in the header.
- * bstream / tstream are the block-race and token-race stream tags. */
-static int race_sample(const double *w, int V, uint64_t key, uint32_t bstream, uint32_t tstream,
+ * by the three-level exponential race described in the header.  The three
+ * stream tags name the block, sub-block and token races. */
+static int race_sample(const double *w, int V, uint64_t key, uint32_t s_block, uint32_t s_sub, uint32_t s_tok,
                        uint32_t trial, uint32_t pos, double *margin)
 {
     int nb = (V + SPVO_BLOCK - 1) / SPVO_BLOCK;
     double *arr = (double *)malloc(sizeof(double) * (size_t)(nb > SPVO_BLOCK ? nb : SPVO_BLOCK));
+    /* level 1: blocks */
     for (int b = 0; b < nb; ++b) {
         int lo = b * SPVO_BLOCK, hi = lo + SPVO_BLOCK < V ? lo + SPVO_BLOCK : V;
         ksum W = { 0, 0 };
         for (int x = lo; x < hi; ++x) ksum_add(&W, w[x]);
         double Wb = ksum_val(&W);
-        arr[b] = Wb > 0 ? expo(key, bstream, trial, pos, (uint64_t)b) / Wb : INFINITY;
+        arr[b] = Wb > 0 ? expo(key, s_block, trial, pos, (uint64_t)b) / Wb : INFINITY;
     }
     int bw = race_winner(arr, nb, margin);
     int lo = bw * SPVO_BLOCK, hi = lo + SPVO_BLOCK < V ? lo + SPVO_BLOCK : V;
-    for (int x = lo; x < hi; ++x)
-        arr[x - lo] = w[x] > 0 ? expo(key, tstream, trial, pos, (uint64_t)x) / w[x] : INFINITY;
-    int xw = lo + race_winner(arr, hi - lo, margin);
+    /* level 2: sub-blocks of the winning block (global sub-block index s0 / SPVO_SUB) */
+    int ns = (hi - lo + SPVO_SUB - 1) / SPVO_SUB;
+    for (int j = 0; j < ns; ++j) {
+        int s0 = lo + j * SPVO_SUB, s1 = s0 + SPVO_SUB < hi ? s0 + SPVO_SUB : hi;
+        ksum W = { 0, 0 };
+        for (int x = s0; x < s1; ++x) ksum_add(&W, w[x]);
+        double Ws = ksum_val(&W);
+        arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)(s0 / SPVO_SUB)) / Ws : INFINITY;
+    }
+    int sw = race_winner(arr, ns, margin);
+    int s0 = lo + sw * SPVO_SUB, s1 = s0 + SPVO_SUB < hi ? s0 + SPVO_SUB : hi;
+    /* level 3: ids of the winning sub-block */
+    for (int x = s0; x < s1; ++x)
+        arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)x) / w[x] : INFINITY;
+    int xw = s0 + race_winner(arr, s1 - s0, margin);
     free(arr);
     return xw;
 }
@@ -297,7 +309,8 @@ int spvo_verify_chain_seq(const float *tgt, const float *drf, const int32_t *tok
     if (k == gamma) {
         const float *tb = tgt + (size_t)gamma * V;
         for (int x = 0; x < V; ++x) w[x] = prob(tb, x, T, Mt[gamma], St[gamma]);
-        emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_TOKEN, 0, (uint32_t)gamma, &margin);
+        emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,
+                              (uint32_t)gamma, &margin);
         if (Z_out) *Z_out = 1.0;
     } else {
         const float *tj = tgt + (size_t)k * V, *dj = drf + (size_t)k * V;
@@ -305,7 +318,8 @@ int spvo_verify_chain_seq(const float *tgt, const float *drf, const int32_t *tok
         emitted = -1;
         int t;
         for (t = 0; t < SPVO_MAX_TRIALS; ++t) {
-            int x = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_TOKEN, (uint32_t)t, (uint32_t)k, &margin);
+            int x = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, (uint32_t)t,
+                                (uint32_t)k, &margin);
             double v = spvo_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
             double p = w[x], q = prob(dj, x, T, Md[k], Sd[k]);
             note_margin(&margin, fabs((1.0 - v) - q / p));
@@ -318,7 +332,8 @@ int spvo_verify_chain_seq(const float *tgt, const float *drf, const int32_t *tok
             w[x] = d > 0 ? d : 0.0;
         }
         if (emitted < 0)
-            emitted = race_sample(w, V, seq_key, SPVO_STREAM_FB_BLOCK, SPVO_STREAM_FB_TOKEN, 0, (uint32_t)k, &margin);
+            emitted = race_sample(w, V, seq_key, SPVO_STREAM_FB_BLOCK, SPVO_STREAM_FB_SUB, SPVO_STREAM_FB_TOKEN, 0,
+                                  (uint32_t)k, &margin);
         if (Z_out) {
             ksum Z = { 0, 0 };
             for (int x = 0; x < V; ++x) ksum_add(&Z, w[x]);

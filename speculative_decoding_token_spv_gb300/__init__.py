@@ -24,6 +24,7 @@ SPV_MAX_GAMMA = 32
 SPV_MAX_FANOUT = 64
 SPV_MAX_FANOUT_ROWS = 64
 SPV_SAMPLER_BLOCK = 1024
+SPV_SAMPLER_SUB = 32
 SPV_MAX_TRIALS = 64
 
 _lib = None

@@ -4,8 +4,8 @@
 // Inference Latency", section "The four-phase loop", steps 2-4:
 //   one pass over the gamma+1 target rows and gamma draft rows of every
 //   sequence computes, per 1024-logit sampler block, the block max m and
-//   S = sum exp((z - m) / T).  The CTA that finishes a sequence's last work
-//   item merges the blocks into row softmax statistics, runs the accept test
+//   S = sum exp((z - m) / T).  The finalize grid (one CTA per sequence)
+//   merges the blocks into row softmax statistics, runs the accept test
 //   r_i q_i(x_i) <= p_i(x_i) for every draft token, finds the first
 //   rejection with a warp ballot, and draws the emitted token: the bonus from
 //   p_gamma, or the residual norm(max(0, p_k - q_k)) by rejection trials from
@@ -15,8 +15,8 @@
 //
 // Greedy verify, "Speculative Pipeline Decoding", streaming verification
 // ("under greedy decoding we require an exact argmax match"): the same pass
-// over the target rows keeps per-block (max, lowest argmax id); the finishing
-// CTA compares each draft token with its row argmax.
+// over the target rows keeps per-block (max, lowest argmax id); the finalize
+// CTA of a sequence compares each draft token with its row argmax.
 #include "spv_internal.h"
 #include "spv_stream.cuh"
 
@@ -30,7 +30,6 @@ namespace spv {
 struct ChainParams {
     long long total_items;
     int nc, nb, V;
-    unsigned *counter;
     unsigned *err;
     const unsigned char *target, *draft;
     const int32_t *tokens;
@@ -38,6 +37,7 @@ struct ChainParams {
     const uint64_t *keys;
     int B, gamma, R;
     float invT, c2;  // 1/T and log2(e)/T
+    int vec;         // rows 16-byte aligned: vector loads in finalize
     int32_t *accept_count, *out_tokens;
     float *out_pq, *out_Z;
     int32_t *row_status;
@@ -45,15 +45,25 @@ struct ChainParams {
     float *resid;    // [B*nb] residual block masses (direct draw / normaliser only)
 };
 
+constexpr int STAT_CACHE = 4096;  // block statistics staged in shared memory when R * nb fits
+
 struct ChainSmem {
-    float M[2 * 32 + 1];  // row max of the raw logits
-    float S[2 * 32 + 1];  // row sum exp((z - M)/T)
+    float2 st[STAT_CACHE];  // block statistics of all rows of the sequence (if they fit)
+    float M[2 * 32 + 1];    // row max of the raw logits
+    float S[2 * 32 + 1];    // row sum exp((z - M)/T)
+    int x[32];              // draft tokens
+    float rr[32];           // accept uniforms
+    float zt[32], zd[32];   // target / draft logit of each draft token
     int bad;
     int k;
+    int cached;
     int trial_x[NCW];
     int trial_acc[NCW];
+    float wbest[NCW];
+    int wbest_i[NCW];
     int result;
     float Z;
+    uint64_t key;
 };
 
 template <int DT> struct ChainOp {
@@ -72,22 +82,29 @@ template <int DT> struct ChainOp {
         const int b = static_cast<int>(row / P.R);
         return row_of(P, b, static_cast<int>(row - static_cast<long long>(b) * P.R));
     }
-    __device__ static __forceinline__ int group(const Params &P, long long row) { return static_cast<int>(row / P.R); }
-    __device__ static __forceinline__ int items_per_group(const Params &P) { return P.R * P.nc; }
 
     // Block statistics: m = max z (raw), s = sum exp((z - m) / T).
+    // The max runs as 8 independent chains and the sum as 4; each term is
+    // ex2(z * c2 - mc) with mc = m * c2 rounded, one FFMA, and the rounding
+    // of mc (delta = m * c2 - mc, exact by FMA) is removed from the sum once:
+    // sum ex2((z - m) c2) = 2^-delta * sum ex2(z c2 - mc).
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int, int lane)
     {
-        float m = -INFINITY;
+        float mx[8];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) m = fmaxf(m, v[e]);
+        for (int a = 0; a < 8; ++a) mx[a] = fmaxf(fmaxf(v[a], v[a + 8]), fmaxf(v[a + 16], v[a + 24]));
+        float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
         m = warp_max(m);
         const float mu = (m == -INFINITY) ? 0.f : m;
-        float s = 0.f;
+        const float mc = mu * P.c2;
+        const float delta = fmaf(mu, P.c2, -mc);
+        float sa[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) s += fast_exp2((v[e] - mu) * P.c2);
+        for (int e = 0; e < 32; ++e) sa[e & 3] += fast_exp2(fmaf(v[e], P.c2, -mc));
+        float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
         s = warp_sum(s);
         if (lane == 0) {
+            s = fmaf(-s * 0.6931471805599453f, delta, s);  // s * 2^-delta, |delta| < 1e-5
             // NaN anywhere, or +inf (then inf - inf), makes s NaN.
             P.stats[row * P.nb + beta] = isnan(s) ? make_float2(__int_as_float(0x7fffffff), 0.f) : make_float2(m, s);
         }
@@ -98,53 +115,110 @@ template <int DT> struct ChainOp {
         return expf((DType<DT>::load(rowp, x) - M) * P.invT) / S;
     }
 
-    // Two-level exponential race drawing one id from softmax(row / T), using
-    // the row's block statistics; one warp.  Returns the id.
-    __device__ static int race_p(const Params &P, long long row, const unsigned char *rowp, float M, uint64_t key,
-                                 uint32_t trial, uint32_t pos, int lane)
+    __device__ static __forceinline__ float2 stat(const Params &P, const Smem &sm, int b, int rho, int beta)
     {
-        float best = -INFINITY;
+        return sm.cached ? sm.st[rho * P.nb + beta]
+                         : __ldcg(&P.stats[(static_cast<long long>(b) * P.R + rho) * P.nb + beta]);
+    }
+
+    // Level 1 of a draw from softmax(row rho / T): the block with the
+    // smallest E_beta / W_beta, W_beta = 2^((m_beta - M) c2) S_beta up to the
+    // row normaliser.  Every lane gets the winner.
+    __device__ static int race_blocks_p(const Params &P, const Smem &sm, int b, int rho, float M, uint64_t key,
+                                        uint32_t trial, uint32_t pos, int lane)
+    {
+        float best = INFINITY;
         int bi = INT_MAX;
         for (int g = lane; 4 * g < P.nb; g += 32) {
-            uint64_t w[4];
-            philox_group(w, key, STREAM_BLOCK, trial, pos, static_cast<uint64_t>(g));
+            float2 st[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int beta = 4 * g + e;
-                if (beta < P.nb) {
-                    const float2 st = __ldcg(&P.stats[row * P.nb + beta]);
-                    const float sc = st.y > 0.f ? ((st.x - M) * P.invT + logf(st.y)) - log_expo(w[e]) : -INFINITY;
-                    if (sc > best) {
-                        best = sc;
-                        bi = beta;
-                    }
-                }
+                st[e] = beta < P.nb ? stat(P, sm, b, rho, beta) : make_float2(0.f, 0.f);
             }
-        }
-        warp_argmax(best, bi);
-        const float mb = __ldcg(&P.stats[row * P.nb + bi]).x;
-        const int base = bi * G;
-        const int cnt = min(G, P.V - base);
-        best = -INFINITY;
-        int bx = INT_MAX;
-        for (int g = lane; 4 * g < cnt; g += 32) {
-            uint64_t w[4];
-            philox_group(w, key, STREAM_TOKEN, trial, pos, static_cast<uint64_t>(base >> 2) + g);
+            uint32_t w[4];
+            philox_group(w, key, STREAM_BLOCK, trial, pos, static_cast<uint32_t>(g));
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int x = base + 4 * g + e;
-                if (x < P.V) {
-                    const float z = DType<DT>::load(rowp, x);
-                    const float sc = (z == -INFINITY) ? -INFINITY : (z - mb) * P.invT - log_expo(w[e]);
-                    if (sc > best) {
-                        best = sc;
-                        bx = x;
+                if (st[e].y > 0.f) {
+                    const float A = arrival(expo(w[e]), fast_exp2((M - st[e].x) * P.c2) / st[e].y);
+                    if (A < best) {
+                        best = A;
+                        bi = 4 * g + e;
                     }
                 }
             }
         }
-        warp_argmax(best, bx);
-        return bx;
+        warp_argmin(best, bi);
+        return bi;
+    }
+
+    // Block beta of a row into a warp's buffer of G floats (-inf past V):
+    // 16-byte vector loads when the rows are aligned, all in flight at once.
+    __device__ static __forceinline__ void load_block(const Params &P, const unsigned char *rowp, int beta, float *buf,
+                                                      int lane)
+    {
+        const int base = beta * G;
+        if (P.vec) {
+#pragma unroll
+            for (int j = 0; j < G / 128; ++j) {
+                const int i = 4 * (lane + 32 * j);
+                float f[4];
+                if (base + i < P.V) {
+                    if (DT == 0) {
+                        const float4 t = __ldg(reinterpret_cast<const float4 *>(rowp) + ((base + i) >> 2));
+                        f[0] = t.x; f[1] = t.y; f[2] = t.z; f[3] = t.w;
+                    } else {
+                        const uint2 t = __ldg(reinterpret_cast<const uint2 *>(rowp) + ((base + i) >> 2));
+                        f[0] = __uint_as_float(t.x << 16); f[1] = __uint_as_float(t.x & 0xffff0000u);
+                        f[2] = __uint_as_float(t.y << 16); f[3] = __uint_as_float(t.y & 0xffff0000u);
+                    }
+                } else {
+                    f[0] = f[1] = f[2] = f[3] = -INFINITY;
+                }
+                *reinterpret_cast<float4 *>(buf + i) = make_float4(f[0], f[1], f[2], f[3]);
+            }
+        } else {
+#pragma unroll 8
+            for (int j = 0; j < G / 32; ++j) {
+                const int i = lane + 32 * j;
+                buf[i] = base + i < P.V ? DType<DT>::load(rowp, base + i) : -INFINITY;
+            }
+        }
+        __syncwarp();
+    }
+
+    // Levels 2 and 3 of a draw from softmax(row / T) inside block beta whose
+    // logits are in buf: lane l owns sub-block l (ids base + 32 l + i) for the
+    // sub-block race, then id base + 32 s* + l for the id race.
+    __device__ static int race_in_block_p(const Params &P, const float *buf, int beta, uint64_t key, uint32_t s_sub,
+                                          uint32_t s_tok, uint32_t trial, uint32_t pos, int lane)
+    {
+        const int base = beta * G;
+        // sub-block max and mass relative to it (skewed reads: no bank conflicts)
+        float ms = -INFINITY;
+#pragma unroll 8
+        for (int i = 0; i < SUB; ++i) ms = fmaxf(ms, buf[SUB * lane + ((i + lane) & (SUB - 1))]);
+        float ws = 0.f;
+        if (ms != -INFINITY) {
+#pragma unroll 8
+            for (int i = 0; i < SUB; ++i) ws += fast_exp2((buf[SUB * lane + ((i + lane) & (SUB - 1))] - ms) * P.c2);
+        }
+        const float mb = warp_max(ms);
+        const uint32_t n = static_cast<uint32_t>(base / SUB + lane);  // global sub-block index
+        uint32_t w[4];
+        philox_group(w, key, s_sub, trial, pos, n >> 2);
+        float A = ws > 0.f ? arrival(expo(w[n & 3]), fast_exp2((mb - ms) * P.c2) / ws) : INFINITY;
+        int si = lane;
+        warp_argmin(A, si);
+        const float msw = __shfl_sync(0xffffffffu, ms, si);
+        const int x = base + SUB * si + lane;
+        const float z = buf[SUB * si + lane];
+        philox_group(w, key, s_tok, trial, pos, static_cast<uint32_t>(x) >> 2);
+        float Ax = (x < P.V && z != -INFINITY) ? arrival(expo(w[x & 3]), fast_exp2((msw - z) * P.c2)) : INFINITY;
+        int xi = x;
+        warp_argmin(Ax, xi);
+        return xi;
     }
 
     // Residual masses w = max(0, p - q) of one row pair, per block, into
@@ -174,92 +248,131 @@ template <int DT> struct ChainOp {
         consumer_sync();
     }
 
-    // Direct race over the residual (after the rejection trials all failed).
-    __device__ static int race_resid(const Params &P, int b, const unsigned char *tp, const unsigned char *dp,
-                                     float Mt, float St, float Md, float Sd, uint64_t key, uint32_t pos, int lane)
+    // Direct race over the residual w = max(0, p - q) (after the rejection
+    // trials all failed): block masses from residual_pass, then sub-blocks
+    // and ids of the winning block (target and draft logits in tb / db).
+    __device__ static int race_resid(const Params &P, int b, const unsigned char *tp, const unsigned char *dp, float Mt,
+                                     float St, float Md, float Sd, uint64_t key, uint32_t pos, float *tb, float *db,
+                                     int lane)
     {
-        float best = -INFINITY;
+        float best = INFINITY;
         int bi = INT_MAX;
         for (int g = lane; 4 * g < P.nb; g += 32) {
-            uint64_t w[4];
-            philox_group(w, key, STREAM_FB_BLOCK, 0, pos, static_cast<uint64_t>(g));
+            float W[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int beta = 4 * g + e;
-                if (beta < P.nb) {
-                    const float W = __ldcg(&P.resid[static_cast<size_t>(b) * P.nb + beta]);
-                    const float sc = W > 0.f ? logf(W) - log_expo(w[e]) : -INFINITY;
-                    if (sc > best) {
-                        best = sc;
-                        bi = beta;
-                    }
-                }
+                W[e] = beta < P.nb ? __ldcg(&P.resid[static_cast<size_t>(b) * P.nb + beta]) : 0.f;
             }
-        }
-        warp_argmax(best, bi);
-        const float it = 1.f / St, id = 1.f / Sd;
-        const int base = bi * G, cnt = min(G, P.V - base);
-        best = -INFINITY;
-        int bx = INT_MAX;
-        for (int g = lane; 4 * g < cnt; g += 32) {
-            uint64_t w[4];
-            philox_group(w, key, STREAM_FB_TOKEN, 0, pos, static_cast<uint64_t>(base >> 2) + g);
+            uint32_t w[4];
+            philox_group(w, key, STREAM_FB_BLOCK, 0, pos, static_cast<uint32_t>(g));
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int x = base + 4 * g + e;
-                if (x < P.V) {
-                    const float p = expf((DType<DT>::load(tp, x) - Mt) * P.invT) * it;
-                    const float q = expf((DType<DT>::load(dp, x) - Md) * P.invT) * id;
-                    const float wx = fmaxf(p - q, 0.f);
-                    const float sc = wx > 0.f ? logf(wx) - log_expo(w[e]) : -INFINITY;
-                    if (sc > best) {
-                        best = sc;
-                        bx = x;
+                if (W[e] > 0.f) {
+                    const float A = arrival(expo(w[e]), 1.f / W[e]);
+                    if (A < best) {
+                        best = A;
+                        bi = 4 * g + e;
                     }
                 }
             }
         }
-        warp_argmax(best, bx);
-        return bx;
+        warp_argmin(best, bi);
+        load_block(P, tp, bi, tb, lane);
+        load_block(P, dp, bi, db, lane);
+        const float it = 1.f / St, id = 1.f / Sd;
+        const int base = bi * G;
+        float ws = 0.f;
+        for (int i = 0; i < SUB; ++i) {
+            const int o = SUB * lane + ((i + lane) & (SUB - 1));
+            ws += fmaxf(expf((tb[o] - Mt) * P.invT) * it - expf((db[o] - Md) * P.invT) * id, 0.f);
+        }
+        const uint32_t n = static_cast<uint32_t>(base / SUB + lane);
+        uint32_t w[4];
+        philox_group(w, key, STREAM_FB_SUB, 0, pos, n >> 2);
+        float A = ws > 0.f ? arrival(expo(w[n & 3]), 1.f / ws) : INFINITY;
+        int si = lane;
+        warp_argmin(A, si);
+        const int x = base + SUB * si + lane;
+        const int o = SUB * si + lane;
+        const float wx = x < P.V ? fmaxf(expf((tb[o] - Mt) * P.invT) * it - expf((db[o] - Md) * P.invT) * id, 0.f) : 0.f;
+        philox_group(w, key, STREAM_FB_TOKEN, 0, pos, static_cast<uint32_t>(x) >> 2);
+        float Ax = wx > 0.f ? arrival(expo(w[x & 3]), 1.f / wx) : INFINITY;
+        int xi = x;
+        warp_argmin(Ax, xi);
+        return xi;
     }
 
-    __device__ static void finalize(const Params &P, int b, Smem &sm, int warp, int lane)
+    static constexpr int FIN_BUF_FLOATS = 2 * NCW * G;  // per warp: one target and one draft block
+
+    __device__ static void finalize(const Params &P, int b, Smem &sm, float *buf, int warp, int lane)
     {
-        const int R = P.R, g = P.gamma;
-        if (threadIdx.x == 0) sm.bad = 0;
-        consumer_sync();
-        // 1. Merge block statistics into row statistics (one warp per row).
-        for (int rho = warp; rho < R; rho += NCW) {
-            const float2 *st = P.stats + (static_cast<long long>(b) * R + rho) * P.nb;
-            float m = -INFINITY;
-            bool bad = false;
-            for (int beta = lane; beta < P.nb; beta += 32) {
-                const float2 v = __ldcg(&st[beta]);
-                if (isnan(v.x)) bad = true;
-                else m = fmaxf(m, v.x);
+        const int R = P.R, g = P.gamma, nb = P.nb;
+        float *tb = buf + warp * 2 * G, *db = tb + G;  // this warp's block buffers
+        // A. Inputs that do not depend on the streaming grid: tokens, r, key
+        //    and the logits of each draft token (overlaps the grid's tail).
+        if (threadIdx.x == 0) {
+            sm.bad = 0;
+            sm.key = P.keys[b];
+            sm.cached = (R * nb <= STAT_CACHE) ? 1 : 0;
+        }
+        if (warp == 0 && lane < g) {
+            const int x = P.tokens[static_cast<size_t>(b) * g + lane];
+            sm.x[lane] = x;
+            sm.rr[lane] = P.r[static_cast<size_t>(b) * g + lane];
+            if (x >= 0 && x < P.V) {
+                sm.zt[lane] = DType<DT>::load(row_of(P, b, lane), x);
+                sm.zd[lane] = DType<DT>::load(row_of(P, b, g + 1 + lane), x);
+            } else {
+                sm.zt[lane] = sm.zd[lane] = 0.f;
             }
-            m = warp_max(m);
-            bad = __any_sync(0xffffffffu, bad);
-            float s = 0.f;
-            if (!bad && m != -INFINITY) {
-                for (int beta = lane; beta < P.nb; beta += 32) {
-                    const float2 v = __ldcg(&st[beta]);
-                    if (v.y > 0.f) s += v.y * expf((v.x - m) * P.invT);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        consumer_sync();
+        if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
+        // B. Row statistics from the block statistics (one warp per row); all
+        //    loads of a row are in flight at once; rows are staged in shared
+        //    memory for the draw when they fit.
+        for (int rho = warp; rho < R; rho += NCW) {
+            const float2 *st = P.stats + (static_cast<long long>(b) * R + rho) * nb;
+            float m = -INFINITY, s = 0.f;
+            bool bad = false;
+            for (int base = 0; base < nb; base += 32 * 8) {
+                float2 v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int beta = base + 32 * u + lane;
+                    v[u] = beta < nb ? __ldcg(&st[beta]) : make_float2(-INFINITY, 0.f);
+                }
+                float cm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int beta = base + 32 * u + lane;
+                    if (isnan(v[u].x)) bad = true;
+                    else cm = fmaxf(cm, v[u].x);
+                    if (sm.cached && beta < nb) sm.st[rho * nb + beta] = v[u];
+                }
+                const float nm = fmaxf(m, cm);
+                if (nm != -INFINITY) {
+                    float acc = s > 0.f ? s * expf((m - nm) * P.invT) : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u)
+                        if (v[u].y > 0.f) acc += v[u].y * expf((v[u].x - nm) * P.invT);
+                    s = acc;
+                    m = nm;
                 }
             }
+            const float mw = warp_max(m);
+            s = (s > 0.f) ? s * expf((m - mw) * P.invT) : 0.f;
             s = warp_sum(s);
+            bad = __any_sync(0xffffffffu, bad);
             if (lane == 0) {
-                sm.M[rho] = m;
+                sm.M[rho] = mw;
                 sm.S[rho] = s;
                 if (bad || !(s > 0.f)) atomicOr(&sm.bad, 1);
             }
         }
-        if (warp == 0 && lane < g) {
-            const int x = P.tokens[static_cast<size_t>(b) * g + lane];
-            if (x < 0 || x >= P.V) atomicOr(&sm.bad, 1);
-        }
         consumer_sync();
-        const uint64_t key = P.keys[b];
         if (sm.bad) {
             for (int i = threadIdx.x; i <= g; i += NCW * 32) P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
             if (P.out_pq)
@@ -269,20 +382,16 @@ template <int DT> struct ChainOp {
                 P.accept_count[b] = -1;
                 if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
                 if (P.out_Z) P.out_Z[b] = __int_as_float(0x7fffffff);
-                P.counter[b] = 0u;
             }
-            consumer_sync();
             return;
         }
-        // 2. Accept tests for every draft position; first rejection by ballot.
+        // C. Accept tests for every draft position; first rejection by ballot.
         if (warp == 0) {
             bool acc = false;
             if (lane < g) {
-                const int x = P.tokens[static_cast<size_t>(b) * g + lane];
-                const float p = prob(P, row_of(P, b, lane), x, sm.M[lane], sm.S[lane]);
-                const float q = prob(P, row_of(P, b, g + 1 + lane), x, sm.M[g + 1 + lane], sm.S[g + 1 + lane]);
-                const float rr = P.r[static_cast<size_t>(b) * g + lane];
-                acc = (p > 0.f) && (rr * q <= p);
+                const float p = expf((sm.zt[lane] - sm.M[lane]) * P.invT) / sm.S[lane];
+                const float q = expf((sm.zd[lane] - sm.M[g + 1 + lane]) * P.invT) / sm.S[g + 1 + lane];
+                acc = (p > 0.f) && (sm.rr[lane] * q <= p);
                 if (P.out_pq) {
                     P.out_pq[(static_cast<size_t>(b) * g + lane) * 2] = p;
                     P.out_pq[(static_cast<size_t>(b) * g + lane) * 2 + 1] = q;
@@ -290,32 +399,42 @@ template <int DT> struct ChainOp {
             }
             const unsigned mask = __ballot_sync(0xffffffffu, acc);
             const unsigned all = (g == 32) ? 0xffffffffu : ((1u << g) - 1u);
-            if (lane == 0) sm.k = ((mask & all) == all) ? g : (__ffs(~mask) - 1);
+            if (lane == 0) {
+                sm.k = ((mask & all) == all) ? g : (__ffs(~mask) - 1);
+                sm.result = -1;
+            }
         }
         consumer_sync();
         const int k = sm.k;
-        // 3. The emitted token.
+        const uint64_t key = sm.key;
         const unsigned char *tp = row_of(P, b, k);
-        const long long trow = static_cast<long long>(b) * R + k;
+        const float Mt = sm.M[k], St = sm.S[k];
+        // D. The emitted token.
         if (k == g) {
+            // Bonus: one draw from p_gamma (warp 0).
             if (warp == 0) {
-                const int x = race_p(P, trow, tp, sm.M[k], key, 0u, static_cast<uint32_t>(g), lane);
+                const int beta = race_blocks_p(P, sm, b, k, Mt, key, 0u, static_cast<uint32_t>(g), lane);
+                load_block(P, tp, beta, tb, lane);
+                const int x = race_in_block_p(P, tb, beta, key, STREAM_SUB, STREAM_TOKEN, 0u, static_cast<uint32_t>(g), lane);
                 if (lane == 0) sm.result = x;
             }
             consumer_sync();
         } else {
+            // Residual: rejection trials from p_k, eight at a time (one per warp).
             const unsigned char *dp = row_of(P, b, g + 1 + k);
-            const float Mt = sm.M[k], St = sm.S[k], Md = sm.M[g + 1 + k], Sd = sm.S[g + 1 + k];
-            if (threadIdx.x == 0) sm.result = -1;
+            const float Md = sm.M[g + 1 + k], Sd = sm.S[g + 1 + k];
             for (int round = 0; round < MAX_TRIALS / NCW; ++round) {
                 const uint32_t t = static_cast<uint32_t>(round * NCW + warp);
-                const int x = race_p(P, trow, tp, Mt, key, t, static_cast<uint32_t>(k), lane);
+                const int beta = race_blocks_p(P, sm, b, k, Mt, key, t, static_cast<uint32_t>(k), lane);
+                load_block(P, tp, beta, tb, lane);
+                load_block(P, dp, beta, db, lane);
+                const int x = race_in_block_p(P, tb, beta, key, STREAM_SUB, STREAM_TOKEN, t, static_cast<uint32_t>(k), lane);
                 if (lane == 0) {
-                    uint64_t w[4];
-                    philox_group(w, key, STREAM_ACCEPT, t, static_cast<uint32_t>(k), 0);
+                    uint32_t w[4];
+                    philox_group(w, key, STREAM_ACCEPT, t, static_cast<uint32_t>(k), 0u);
                     const float v = uniform24(w[0]);
-                    const float p = prob(P, tp, x, Mt, St);
-                    const float q = prob(P, dp, x, Md, Sd);
+                    const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
+                    const float q = expf((db[x - beta * G] - Md) * P.invT) / Sd;
                     sm.trial_x[warp] = x;
                     sm.trial_acc[warp] = (q <= (1.0f - v) * p) ? 1 : 0;
                 }
@@ -335,18 +454,18 @@ template <int DT> struct ChainOp {
                 residual_pass(P, b, tp, dp, Mt, St, Md, Sd, sm, warp, lane);
                 if (fallback) {
                     if (warp == 0) {
-                        const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(k), lane);
+                        const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(k), tb, db, lane);
                         if (lane == 0) sm.result = x;
                     }
                     consumer_sync();
                 }
             }
         }
-        // 4. Outputs.
+        // E. Outputs.
         const int res = sm.result;
         for (int i = threadIdx.x; i <= g; i += NCW * 32) {
             int v = -1;
-            if (i < k) v = P.tokens[static_cast<size_t>(b) * g + i];
+            if (i < k) v = sm.x[i];
             else if (i == k) v = res;
             P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = v;
         }
@@ -354,9 +473,7 @@ template <int DT> struct ChainOp {
             P.accept_count[b] = k;
             if (P.row_status) P.row_status[b] = 0;
             if (P.out_Z) P.out_Z[b] = (k == g) ? 1.0f : sm.Z;
-            P.counter[b] = 0u;
         }
-        consumer_sync();
     }
 };
 
@@ -366,7 +483,6 @@ template <int DT> struct ChainOp {
 struct GreedyParams {
     long long total_items;
     int nc, nb, V;
-    unsigned *counter;
     unsigned *err;
     const unsigned char *target;
     const int32_t *tokens;
@@ -377,6 +493,7 @@ struct GreedyParams {
 
 struct GreedySmem {
     int a[33];
+    int x[32];
     int bad;
 };
 
@@ -389,52 +506,74 @@ template <int DT> struct GreedyOp {
     {
         return P.target + static_cast<size_t>(row) * static_cast<size_t>(P.V) * EB;
     }
-    __device__ static __forceinline__ int group(const Params &P, long long row) { return static_cast<int>(row / P.R); }
-    __device__ static __forceinline__ int items_per_group(const Params &P) { return P.R * P.nc; }
 
+    // Per-block (max, first argmax): four independent accumulators over the
+    // lane's elements e = a (mod 4), each in rising id order, then combined
+    // with ties to the lower id.
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int, int lane)
     {
-        float bv = -INFINITY;
-        int bi = INT_MAX;
+        float bv[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        int bi[4] = {INT_MAX, INT_MAX, INT_MAX, INT_MAX};
         bool nan = false;
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
             const float x = v[e];
             nan |= (x != x);
-            if (x > bv) {  // strict: the first (lowest) id keeps a tie; -0.0 == +0.0
-                bv = x;
-                bi = lane_index<DT>(lane, e);
+            if (x > bv[e & 3]) {  // strict: the first (lowest) id keeps a tie; -0.0 == +0.0
+                bv[e & 3] = x;
+                bi[e & 3] = lane_index<DT>(lane, e);
             }
         }
-        warp_argmax(bv, bi);
+        float b = bv[0];
+        int i = bi[0];
+#pragma unroll
+        for (int a = 1; a < 4; ++a)
+            if (bv[a] > b || (bv[a] == b && bi[a] < i)) {
+                b = bv[a];
+                i = bi[a];
+            }
+        warp_argmax(b, i);
         nan = __any_sync(0xffffffffu, nan);
         if (lane == 0) {
             int2 o;
-            if (nan || bv == INFINITY) o = make_int2(0x7fc00000, -2);
-            else o = make_int2(__float_as_int(bv), bi == INT_MAX ? INT_MAX : beta * G + bi);
+            if (nan || b == INFINITY) o = make_int2(0x7fc00000, -2);
+            else o = make_int2(__float_as_int(b), i == INT_MAX ? INT_MAX : beta * G + i);
             P.best[row * P.nb + beta] = o;
         }
     }
 
-    __device__ static void finalize(const Params &P, int b, Smem &sm, int warp, int lane)
+    static constexpr int FIN_BUF_FLOATS = 0;
+
+    __device__ static void finalize(const Params &P, int b, Smem &sm, float *, int warp, int lane)
     {
-        const int g = P.gamma, R = P.R;
+        const int g = P.gamma, R = P.R, nb = P.nb;
         if (threadIdx.x == 0) sm.bad = 0;
+        if (warp == 0 && lane < g) sm.x[lane] = P.tokens[static_cast<size_t>(b) * g + lane];
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         consumer_sync();
+        if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
         for (int rho = warp; rho < R; rho += NCW) {
-            const int2 *bb = P.best + (static_cast<long long>(b) * R + rho) * P.nb;
+            const int2 *bb = P.best + (static_cast<long long>(b) * R + rho) * nb;
             float bv = -INFINITY;
             int bi = INT_MAX;
             bool bad = false;
-            for (int beta = lane; beta < P.nb; beta += 32) {
-                const int2 o = __ldcg(&bb[beta]);
-                if (o.y == -2) {
-                    bad = true;
-                } else {
-                    const float v = __int_as_float(o.x);
-                    if (v > bv || (v == bv && o.y < bi)) {
-                        bv = v;
-                        bi = o.y;
+            for (int base = 0; base < nb; base += 32 * 8) {
+                int2 o[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int beta = base + 32 * u + lane;
+                    o[u] = beta < nb ? __ldcg(&bb[beta]) : make_int2(__float_as_int(-INFINITY), INT_MAX);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    if (o[u].y == -2) {
+                        bad = true;
+                    } else {
+                        const float v = __int_as_float(o[u].x);
+                        if (v > bv || (v == bv && o[u].y < bi)) {
+                            bv = v;
+                            bi = o[u].y;
+                        }
                     }
                 }
             }
@@ -445,10 +584,6 @@ template <int DT> struct GreedyOp {
                 if (bad || bv == -INFINITY || bi == INT_MAX) atomicOr(&sm.bad, 1);
             }
         }
-        if (warp == 0 && lane < g) {
-            const int x = P.tokens[static_cast<size_t>(b) * g + lane];
-            if (x < 0 || x >= P.V) atomicOr(&sm.bad, 1);
-        }
         consumer_sync();
         if (warp == 0) {
             if (sm.bad) {
@@ -458,18 +593,13 @@ template <int DT> struct GreedyOp {
                     if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
                 }
             } else {
-                int x = 0;
-                bool acc = false;
-                if (lane < g) {
-                    x = P.tokens[static_cast<size_t>(b) * g + lane];
-                    acc = (x == sm.a[lane]);
-                }
+                const bool acc = lane < g && sm.x[lane] == sm.a[lane];
                 const unsigned mask = __ballot_sync(0xffffffffu, acc);
                 const unsigned all = (g == 32) ? 0xffffffffu : ((1u << g) - 1u);
                 const int k = ((mask & all) == all) ? g : (__ffs(~mask) - 1);
                 for (int i = lane; i <= g; i += 32) {
                     int v = -1;
-                    if (i < k) v = P.tokens[static_cast<size_t>(b) * g + i];
+                    if (i < k) v = sm.x[i];
                     else if (i == k) v = sm.a[k];
                     P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = v;
                 }
@@ -478,37 +608,17 @@ template <int DT> struct GreedyOp {
                     if (P.row_status) P.row_status[b] = 0;
                 }
             }
-            if (lane == 0) P.counter[b] = 0u;
         }
-        consumer_sync();
     }
 };
 
 // =====================================================================================
 // Host launch
 // =====================================================================================
-template <class Op, int DT> static cudaError_t launch_op(const typename Op::Params &P, bool tma, cudaStream_t st)
-{
-    void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
-    const int smem = tma ? stages<DT>() * CHUNK * DType<DT>::BYTES : 0;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem)) != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const long long cap = static_cast<long long>(per_sm) * sms;
-    const int grid = static_cast<int>(P.total_items < cap ? P.total_items : cap);
-    kern<<<grid, THREADS, smem, st>>>(P);
-    return cudaGetLastError();
-}
-
 size_t chain_ws_bytes(int B, int gamma, int V)
 {
     const size_t nb = blocks_per_row(V), R = 2 * static_cast<size_t>(gamma) + 1;
     size_t n = WS_HEADER;
-    n += align256(static_cast<size_t>(B) * 4);       // counters
     n += align256(static_cast<size_t>(B) * R * nb * 8); // block statistics
     n += align256(static_cast<size_t>(B) * nb * 4);  // residual block masses
     const size_t gr = greedy_ws_bytes(B, gamma, V);
@@ -518,7 +628,7 @@ size_t chain_ws_bytes(int B, int gamma, int V)
 size_t greedy_ws_bytes(int B, int gamma, int V)
 {
     const size_t nb = blocks_per_row(V), R = static_cast<size_t>(gamma) + 1;
-    return WS_HEADER + align256(static_cast<size_t>(B) * 4) + align256(static_cast<size_t>(B) * R * nb * 8);
+    return WS_HEADER + align256(static_cast<size_t>(B) * R * nb * 8);
 }
 
 cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
@@ -534,8 +644,6 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
     unsigned char *ws = static_cast<unsigned char *>(L.ws);
     P.err = reinterpret_cast<unsigned *>(ws);
     size_t off = WS_HEADER;
-    P.counter = reinterpret_cast<unsigned *>(ws + off);
-    off += align256(static_cast<size_t>(L.B) * 4);
     P.stats = reinterpret_cast<float2 *>(ws + off);
     off += align256(static_cast<size_t>(L.B) * P.R * P.nb * 8);
     P.resid = reinterpret_cast<float *>(ws + off);
@@ -546,12 +654,14 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
     P.keys = L.keys;
     P.invT = 1.0f / L.T;
     P.c2 = 1.4426950408889634f / L.T;
+    P.vec = L.tma ? 1 : 0;
     P.accept_count = L.accept_count;
     P.out_tokens = L.out_tokens;
     P.out_pq = L.out_pq;
     P.out_Z = L.out_Z;
     P.row_status = L.row_status;
-    return L.dtype == 0 ? launch_op<ChainOp<0>, 0>(P, L.tma, st) : launch_op<ChainOp<1>, 1>(P, L.tma, st);
+    return L.dtype == 0 ? launch_stream_finalize<ChainOp<0>, 0>(P, L.tma, L.B, st)
+                        : launch_stream_finalize<ChainOp<1>, 1>(P, L.tma, L.B, st);
 }
 
 cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st)
@@ -566,16 +676,14 @@ cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st)
     P.total_items = static_cast<long long>(L.B) * P.R * P.nc;
     unsigned char *ws = static_cast<unsigned char *>(L.ws);
     P.err = reinterpret_cast<unsigned *>(ws);
-    size_t off = WS_HEADER;
-    P.counter = reinterpret_cast<unsigned *>(ws + off);
-    off += align256(static_cast<size_t>(L.B) * 4);
-    P.best = reinterpret_cast<int2 *>(ws + off);
+    P.best = reinterpret_cast<int2 *>(ws + WS_HEADER);
     P.target = static_cast<const unsigned char *>(L.target);
     P.tokens = L.tokens;
     P.accept_count = L.accept_count;
     P.out_tokens = L.out_tokens;
     P.row_status = L.row_status;
-    return L.dtype == 0 ? launch_op<GreedyOp<0>, 0>(P, L.tma, st) : launch_op<GreedyOp<1>, 1>(P, L.tma, st);
+    return L.dtype == 0 ? launch_stream_finalize<GreedyOp<0>, 0>(P, L.tma, L.B, st)
+                        : launch_stream_finalize<GreedyOp<1>, 1>(P, L.tma, L.B, st);
 }
 
 }  // namespace spv

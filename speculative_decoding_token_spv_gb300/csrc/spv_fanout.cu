@@ -6,8 +6,8 @@
 // verification.  One pass over the rows: each warp reduces a 1024-logit block
 // to its own top-F list (F rounds of a warp max over 64-bit keys
 // (order-preserving logit key, inverted id), so logit descending then id
-// ascending, every key distinct); the CTA that finishes a row's last item
-// merges the per-block lists (which are already sorted) into the row's top-F.
+// ascending, every key distinct); the finalize grid (one CTA per row) merges
+// the per-block lists (which are already sorted) into the row's top-F.
 #include "spv_internal.h"
 #include "spv_stream.cuh"
 
@@ -18,7 +18,6 @@ constexpr int FAN_MAX_LISTS_PER_LANE = 4;  // blocks per row <= 8 warps * 32 lan
 struct FanoutParams {
     long long total_items;
     int nc, nb, V;
-    unsigned *counter;
     unsigned *err;
     const unsigned char *draft;
     const int32_t *exclude;
@@ -29,7 +28,10 @@ struct FanoutParams {
     uint64_t *cand;  // [rows*nb*Fmax]; UINT64_MAX in slot 0 marks a NaN block, 0 = no candidate
 };
 
+constexpr int FAN_CACHE = 4096;  // candidates staged in shared memory when nb * F fits
+
 struct FanoutSmem {
+    uint64_t cand[FAN_CACHE];
     uint64_t list[NCW][64];
     int bad;
 };
@@ -48,8 +50,6 @@ template <int DT> struct FanoutOp {
     {
         return P.draft + static_cast<size_t>(row) * static_cast<size_t>(P.V) * EB;
     }
-    __device__ static __forceinline__ int group(const Params &, long long row) { return static_cast<int>(row); }
-    __device__ static __forceinline__ int items_per_group(const Params &P) { return P.nc; }
 
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int valid,
                                                  int lane)
@@ -89,36 +89,60 @@ template <int DT> struct FanoutOp {
         }
     }
 
-    __device__ static void finalize(const Params &P, int row, Smem &sm, int warp, int lane)
+    static constexpr int FIN_BUF_FLOATS = 0;
+
+    __device__ static void finalize(const Params &P, int row, Smem &sm, float *, int warp, int lane)
     {
         const int k = row % P.K1, b = row / P.K1;
         const int F = P.F[k];
+        const int nb = P.nb;
         if (threadIdx.x == 0) sm.bad = 0;
+        asm volatile("griddepcontrol.wait;" ::: "memory");
         consumer_sync();
-        const uint64_t *rc = P.cand + static_cast<size_t>(row) * P.nb * P.Fmax;
+        const uint64_t *rc = P.cand + static_cast<size_t>(row) * nb * P.Fmax;
+        const bool cached = nb * F <= FAN_CACHE;
         if (F > 0) {
-            for (int beta = threadIdx.x; beta < P.nb; beta += NCW * 32)
-                if (__ldcg(rc + static_cast<size_t>(beta) * P.Fmax) == ~0ull) sm.bad = 1;
+            if (cached) {
+                // stage every candidate (list beta, rank t) at cand[beta * F + t]
+                for (int i0 = 0; i0 < nb * F; i0 += NCW * 32 * 4) {
+                    uint64_t v[4];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i0 + u * NCW * 32 + threadIdx.x;
+                        v[u] = i < nb * F ? __ldcg(rc + static_cast<size_t>(i / F) * P.Fmax + (i % F)) : 0ull;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int i = i0 + u * NCW * 32 + threadIdx.x;
+                        if (i < nb * F) {
+                            sm.cand[i] = v[u];
+                            if (i % F == 0 && v[u] == ~0ull) sm.bad = 1;
+                        }
+                    }
+                }
+            } else {
+                for (int beta = threadIdx.x; beta < nb; beta += NCW * 32)
+                    if (__ldcg(rc + static_cast<size_t>(beta) * P.Fmax) == ~0ull) sm.bad = 1;
+            }
         }
         consumer_sync();
         int32_t *ids = P.out_ids + static_cast<size_t>(b) * P.sumF + P.off[k];
         if (F == 0 || sm.bad) {
             for (int t = threadIdx.x; t < F; t += NCW * 32) ids[t] = -1;
-            if (threadIdx.x == 0) {
-                if (P.row_status) P.row_status[row] = (F > 0 && sm.bad) ? STATUS_BAD_ROW : 0;
-                P.counter[row] = 0u;
-            }
-            consumer_sync();
+            if (threadIdx.x == 0 && P.row_status) P.row_status[row] = (F > 0 && sm.bad) ? STATUS_BAD_ROW : 0;
             return;
         }
         // Level 1: warp w merges the sorted lists of blocks beta = w + NCW * j.
+        auto cand_at = [&](int beta, int t) -> uint64_t {
+            return cached ? sm.cand[beta * F + t] : __ldcg(rc + static_cast<size_t>(beta) * P.Fmax + t);
+        };
         int head[FAN_MAX_LISTS_PER_LANE];
         uint64_t cur[FAN_MAX_LISTS_PER_LANE];
 #pragma unroll
         for (int q = 0; q < FAN_MAX_LISTS_PER_LANE; ++q) {
             const int beta = warp + NCW * (lane + 32 * q);
             head[q] = 0;
-            cur[q] = beta < P.nb ? __ldcg(rc + static_cast<size_t>(beta) * P.Fmax) : 0ull;
+            cur[q] = beta < nb ? cand_at(beta, 0) : 0ull;
         }
         for (int t = 0; t < F; ++t) {
             uint64_t mine = 0;
@@ -131,7 +155,7 @@ template <int DT> struct FanoutOp {
                     if (cur[q] == best) {
                         const int beta = warp + NCW * (lane + 32 * q);
                         ++head[q];
-                        cur[q] = head[q] < F ? __ldcg(rc + static_cast<size_t>(beta) * P.Fmax + head[q]) : 0ull;
+                        cur[q] = head[q] < F ? cand_at(beta, head[q]) : 0ull;
                     }
                 }
             }
@@ -150,37 +174,16 @@ template <int DT> struct FanoutOp {
                 }
                 if (lane == 0) ids[t] = best ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best)) : -1;
             }
-            if (lane == 0) {
-                if (P.row_status) P.row_status[row] = 0;
-                P.counter[row] = 0u;
-            }
+            if (lane == 0 && P.row_status) P.row_status[row] = 0;
         }
-        consumer_sync();
     }
 };
-
-template <class Op, int DT> static cudaError_t launch_fan(const typename Op::Params &P, bool tma, cudaStream_t st)
-{
-    void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
-    const int smem = tma ? stages<DT>() * CHUNK * DType<DT>::BYTES : 0;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    int dev = 0, sms = 0, per_sm = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem)) != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    const long long cap = static_cast<long long>(per_sm) * sms;
-    const int grid = static_cast<int>(P.total_items < cap ? P.total_items : cap);
-    kern<<<grid, THREADS, smem, st>>>(P);
-    return cudaGetLastError();
-}
 
 size_t fanout_ws_bytes(int B, int K1, int V, int Fmax)
 {
     const size_t rows = static_cast<size_t>(B) * K1, nb = blocks_per_row(V);
     const size_t f = Fmax > 0 ? static_cast<size_t>(Fmax) : 1;
-    return WS_HEADER + align256(rows * 4) + align256(rows * nb * f * 8);
+    return WS_HEADER + align256(rows * nb * f * 8);
 }
 
 cudaError_t launch_fanout(const FanoutLaunch &L, cudaStream_t st)
@@ -197,15 +200,14 @@ cudaError_t launch_fanout(const FanoutLaunch &L, cudaStream_t st)
     P.total_items = static_cast<long long>(L.B) * L.K1 * P.nc;
     unsigned char *ws = static_cast<unsigned char *>(L.ws);
     P.err = reinterpret_cast<unsigned *>(ws);
-    size_t off = WS_HEADER;
-    P.counter = reinterpret_cast<unsigned *>(ws + off);
-    off += align256(static_cast<size_t>(L.B) * L.K1 * 4);
-    P.cand = reinterpret_cast<uint64_t *>(ws + off);
+    P.cand = reinterpret_cast<uint64_t *>(ws + WS_HEADER);
     P.draft = static_cast<const unsigned char *>(L.draft);
     P.exclude = L.exclude;
     P.out_ids = L.out_ids;
     P.row_status = L.row_status;
-    return L.dtype == 0 ? launch_fan<FanoutOp<0>, 0>(P, L.tma, st) : launch_fan<FanoutOp<1>, 1>(P, L.tma, st);
+    const int rows = L.B * L.K1;
+    return L.dtype == 0 ? launch_stream_finalize<FanoutOp<0>, 0>(P, L.tma, rows, st)
+                        : launch_stream_finalize<FanoutOp<1>, 1>(P, L.tma, rows, st);
 }
 
 }  // namespace spv

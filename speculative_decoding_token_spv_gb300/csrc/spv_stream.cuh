@@ -1,14 +1,14 @@
 // spv_stream.cuh -- device building blocks of libspv (sm_103a).
 //
 // * A streaming pipeline that reads every logit row of a call exactly once:
-//   rows are cut into work items of SPV_CHUNK contiguous logits; a producer
-//   warp stages items in a ring of shared-memory buffers with TMA bulk copies
+//   rows are cut into work items of 8192 contiguous logits; a producer warp
+//   stages items in a ring of shared-memory buffers with TMA bulk copies
 //   (cp.async.bulk, global -> shared, completion on an mbarrier), and eight
 //   consumer warps reduce one sampler block (1024 logits) each.  Per-block
-//   partial results go to a small workspace; the CTA that completes the last
-//   item of a sequence (or row) merges them and writes the outputs
-//   (threadfence + atomic counter, no spinning on other CTAs).
-// * Philox4x64-10 and the uniform / exponential variates of the sampling rule.
+//   partial results go to a small workspace.  A second, dependent grid (one
+//   CTA per sequence or row, programmatic dependent launch) merges them and
+//   writes the outputs, so no streaming CTA ever waits on another's work.
+// * Philox4x32-10 and the uniform / exponential variates of the sampling rule.
 // * Warp reductions and order-preserving float keys.
 //
 // Every wait on an mbarrier is bounded; a wait that gives up records
@@ -32,9 +32,11 @@ constexpr int MAX_TRIALS = 64;                // residual rejection trials
 constexpr int STATUS_BAD_ROW = 4;
 constexpr int STATUS_TIMEOUT = 5;
 
+constexpr int SUB = 32;                       // sampler sub-block: ids per sub-block
+
 // Philox stream tags (second counter word).
-constexpr uint64_t STREAM_BLOCK = 1, STREAM_TOKEN = 2, STREAM_ACCEPT = 3, STREAM_FB_BLOCK = 4,
-                   STREAM_FB_TOKEN = 5;
+constexpr uint32_t STREAM_BLOCK = 1, STREAM_SUB = 2, STREAM_TOKEN = 3, STREAM_ACCEPT = 4, STREAM_FB_BLOCK = 5,
+                   STREAM_FB_SUB = 6, STREAM_FB_TOKEN = 7;
 
 template <int DT> struct DType;
 template <> struct DType<0> {  // fp32
@@ -180,24 +182,22 @@ __device__ __forceinline__ uint32_t float_key(float x)
     return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// ------------------------------------------------------------------ Philox4x64-10
+// ------------------------------------------------------------------ Philox4x32-10
 // Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
-// (SC'11): ten rounds; each multiplies counter words 0 and 2 by two fixed
-// 64-bit constants and mixes the halves with the other words and the key,
-// which is bumped by two Weyl constants between rounds.
-__device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64_t k1)
+// (SC'11): ten rounds; each multiplies counter words 0 and 2 by two 32-bit
+// constants and mixes the 64-bit products' halves with the other words and
+// the key, which is bumped by two Weyl constants between rounds.
+__device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32_t k1)
 {
-    const uint64_t M0 = 0xD2E7470EE14C6C93ull, M1 = 0xCA5A826395121157ull;
-    const uint64_t W0 = 0x9E3779B97F4A7C15ull, W1 = 0xBB67AE8584CAA73Bull;
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
         if (round) {
-            k0 += W0;
-            k1 += W1;
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
         }
-        const uint64_t lo0 = M0 * c[0], hi0 = __umul64hi(M0, c[0]);
-        const uint64_t lo1 = M1 * c[2], hi1 = __umul64hi(M1, c[2]);
-        const uint64_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
+        const uint32_t lo0 = 0xD2511F53u * c[0], hi0 = __umulhi(0xD2511F53u, c[0]);
+        const uint32_t lo1 = 0xCD9E8D57u * c[2], hi1 = __umulhi(0xCD9E8D57u, c[2]);
+        const uint32_t n0 = hi1 ^ c[1] ^ k0, n2 = hi0 ^ c[3] ^ k1;
         c[0] = n0;
         c[1] = lo1;
         c[2] = n2;
@@ -205,29 +205,49 @@ __device__ __forceinline__ void philox4x64_10(uint64_t c[4], uint64_t k0, uint64
     }
 }
 
-// The four words of draw group `grp` (draws 4*grp .. 4*grp+3) of one stream.
-__device__ __forceinline__ void philox_group(uint64_t w[4], uint64_t key, uint64_t stream, uint32_t trial,
-                                             uint32_t pos, uint64_t grp)
+// The four words of draw group `grp` (draws 4*grp .. 4*grp+3) of one
+// stream: counter (grp, stream, trial, pos), key (low, high half of `key`).
+__device__ __forceinline__ void philox_group(uint32_t w[4], uint64_t key, uint32_t stream, uint32_t trial,
+                                             uint32_t pos, uint32_t grp)
 {
     w[0] = grp;
     w[1] = stream;
     w[2] = trial;
     w[3] = pos;
-    philox4x64_10(w, key, 0);
+    philox4x32_10(w, static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32));
 }
 
-// U = ((w >> 40) + 1) * 2^-24 in (0, 1], exact in fp32.
-__device__ __forceinline__ float uniform24(uint64_t w)
+// U = ((w >> 8) + 1) * 2^-24 in (0, 1], exact in fp32.
+__device__ __forceinline__ float uniform24(uint32_t w)
 {
-    return static_cast<float>(static_cast<uint32_t>(w >> 40) + 1u) * 0x1p-24f;
+    return static_cast<float>((w >> 8) + 1u) * 0x1p-24f;
 }
 
-// ln E for E = -ln U; -inf when U == 1 (E == 0: an arrival at time zero).
-__device__ __forceinline__ float log_expo(uint64_t w)
+// E = -ln U in [0, 16.64] (0 when U == 1: an arrival at time zero).
+__device__ __forceinline__ float expo(uint32_t w)
 {
-    const float u = uniform24(w);
-    if (u == 1.0f) return -INFINITY;
-    return logf(-logf(u));
+    return -logf(uniform24(w));
+}
+
+// Arrival time E * f of a candidate whose mass is 1/f (f may be +inf for a
+// vanishing mass); E == 0 arrives at 0.
+__device__ __forceinline__ float arrival(float E, float f)
+{
+    return E == 0.f ? 0.f : E * f;
+}
+
+// argmin of (arrival, index) across the warp, ties to the lower index.
+__device__ __forceinline__ void warp_argmin(float &a, int &i)
+{
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+        const float a2 = __shfl_xor_sync(0xffffffffu, a, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        if (a2 < a || (a2 == a && i2 < i)) {
+            a = a2;
+            i = i2;
+        }
+    }
 }
 
 // ------------------------------------------------------------------ block loads
@@ -282,13 +302,14 @@ __device__ __forceinline__ void load_block_global(float v[32], const void *blk, 
 // ------------------------------------------------------------------ the pipeline
 // Op supplies:
 //   struct Params  -- with total_items, nc (items per row), nb (blocks per
-//                     row), V, counter, err fields;
-//   row_ptr(P, row)                 global address of a row;
+//                     row), V and err fields;
+//   row_ptr(P, row)                      global address of a row;
 //   block(P, row, beta, v, valid, lane)  per-warp reduction of one block;
-//   group(P, row), items_per_group(P)    counter slot and its item count;
-//   finalize(P, g, sm, warp, lane)      merge + outputs for a finished group;
-//   struct Smem                     shared scratch of finalize.
-template <class Op, int DT, bool TMA> __global__ void __launch_bounds__(THREADS, 2) stream_kernel(const typename Op::Params P)
+//   finalize(P, g, sm, warp, lane)       merge + outputs of group g (run by
+//                                        finalize_kernel, one CTA per group);
+//   struct Smem                          shared scratch of finalize.
+template <class Op, int DT, bool TMA>
+__global__ void __launch_bounds__(THREADS, 2) stream_kernel(const typename Op::Params P)
 {
     constexpr int EB = DType<DT>::BYTES;
     constexpr int S = stages<DT>();
@@ -296,9 +317,7 @@ template <class Op, int DT, bool TMA> __global__ void __launch_bounds__(THREADS,
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full_bar[S];
     __shared__ __align__(8) uint64_t empty_bar[S];
-    __shared__ int sh_group;
     __shared__ volatile int sh_abort;
-    __shared__ typename Op::Smem sm;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -310,6 +329,9 @@ template <class Op, int DT, bool TMA> __global__ void __launch_bounds__(THREADS,
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // The dependent finalize grid may be scheduled as soon as resources free
+    // up; it waits (griddepcontrol.wait) for this grid's results itself.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     const long long total = P.total_items;
     const int nc = P.nc;
@@ -377,22 +399,68 @@ template <class Op, int DT, bool TMA> __global__ void __launch_bounds__(THREADS,
         if (TMA) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[s]);
-        }
-        consumer_sync();
-        if (sh_abort) break;
-        if (threadIdx.x == 0) {
-            __threadfence();
-            const int g = Op::group(P, row);
-            const unsigned old = atomicAdd(&P.counter[g], 1u);
-            sh_group = (old == static_cast<unsigned>(Op::items_per_group(P) - 1)) ? g : -1;
-        }
-        consumer_sync();
-        const int g = sh_group;
-        if (g >= 0) {
-            __threadfence();
-            Op::finalize(P, g, sm, warp, lane);
+            // A timed-out wait anywhere stops every consumer warp together.
+            if (__any_sync(0xffffffffu, sh_abort != 0)) break;
         }
     }
+}
+
+// One CTA (NCW warps) per group: merges the group's partial results once the
+// streaming grid it depends on has finished, and writes the outputs.
+template <class Op, int DT> __global__ void __launch_bounds__(NCW * 32) finalize_kernel(const typename Op::Params P)
+{
+    __shared__ typename Op::Smem sm;
+    extern __shared__ __align__(16) float fin_buf[];  // Op::FIN_BUF_FLOATS floats
+    // Op::finalize issues griddepcontrol.wait before it reads anything the
+    // streaming grid wrote; reads of the call's inputs may come before it.
+    Op::finalize(P, static_cast<int>(blockIdx.x), sm, fin_buf, threadIdx.x >> 5, threadIdx.x & 31);
+}
+
+// Launches the streaming grid (persistent: as many CTAs as fit, capped by the
+// item count) and then the finalize grid of `groups` CTAs as a programmatic
+// dependent launch on the same stream.
+template <class Op, int DT>
+static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma, int groups, cudaStream_t st)
+{
+    void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
+    const int smem = tma ? stages<DT>() * CHUNK * DType<DT>::BYTES : 0;
+    // Per device and kernel: the shared-memory attribute and the resident
+    // CTA count are set / queried once (a kernel is a function of the
+    // template arguments, so a function-local static is per kernel).
+    constexpr int MAX_DEV = 64;
+    static int cap_cache[MAX_DEV];  // resident CTAs of the whole GPU, 0 = not yet known
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    int cap = (dev >= 0 && dev < MAX_DEV) ? cap_cache[dev] : 0;
+    if (cap == 0) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+            return e;
+        int sms = 0, per_sm = 0;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem)) != cudaSuccess)
+            return e;
+        cap = (per_sm < 1 ? 1 : per_sm) * sms;
+        if ((e = cudaFuncSetAttribute(finalize_kernel<Op, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Op::FIN_BUF_FLOATS * 4)) != cudaSuccess)
+            return e;
+        if (dev >= 0 && dev < MAX_DEV) cap_cache[dev] = cap;
+    }
+    const int grid = static_cast<int>(P.total_items < cap ? P.total_items : cap);
+    kern<<<grid, THREADS, smem, st>>>(P);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(groups));
+    cfg.blockDim = dim3(NCW * 32);
+    cfg.dynamicSmemBytes = Op::FIN_BUF_FLOATS * 4;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, finalize_kernel<Op, DT>, P);
 }
 
 }  // namespace spv

@@ -1,0 +1,84 @@
+"""The pins are sharp: each plausible mistake planted in a copy of the
+oracle's C source (a transposed operand, a wrong sign, a wrong row, a dropped
+stop, a dropped temperature, a broken constant, a reversed tie order) makes at
+least one pin of test_oracle_pins fail.  Mutants are compiled to a temporary
+library; the committed oracle is untouched."""
+import ctypes
+import os
+import subprocess
+
+import pytest
+
+import oracle
+import test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "spv_oracle.c")
+
+MUTANTS = {
+    "accept_transposed": ("int acc = (p > 0) && ((double)r[i] * q <= p);",
+                          "int acc = (p > 0) && ((double)r[i] * p <= q);",
+                          ["test_acceptance_rate_is_one_minus_tvd", "test_target_above_draft_always_accepts"]),
+    "residual_sign": ("double d = w[x] - prob(dj, x, T, Md[k], Sd[k]);",
+                      "double d = prob(dj, x, T, Md[k], Sd[k]) - w[x];",
+                      ["test_residual_fallback_is_exact"]),
+    "bonus_wrong_row": ("const float *tb = tgt + (size_t)gamma * V;",
+                        "const float *tb = tgt + (size_t)(gamma - 1) * V;",
+                        ["test_bonus_is_distributed_as_last_target_row"]),
+    "no_first_rejection_stop": ("if (i < k) { /* decisions", "if (1) { /* decisions",
+                                ["test_expected_tokens_per_iteration", "test_output_length_and_padding"]),
+    "temperature_dropped": ("return exp((double)z[x] / T - M) / S;", "return exp((double)z[x] - M) / S;",
+                            ["test_acceptance_rate_is_one_minus_tvd"]),
+    "trial_accept_inverted": ("if (q <= (1.0 - v) * p) { emitted = x; break; }",
+                              "if (p <= (1.0 - v) * q) { emitted = x; break; }",
+                              ["test_residual_distribution_on_forced_rejection"]),
+    "block_race_weight": ("arr[b] = Wb > 0 ? expo(key, s_block, trial, pos, (uint64_t)b) / Wb : INFINITY;",
+                          "arr[b] = Wb > 0 ? expo(key, s_block, trial, pos, (uint64_t)b) * Wb : INFINITY;",
+                          ["test_first_token_is_distributed_as_target", "test_bonus_is_distributed_as_last_target_row"]),
+    "sub_block_race_weight": ("arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)(s0 / SPVO_SUB)) / Ws : INFINITY;",
+                              "arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)(s0 / SPVO_SUB)) : INFINITY;",
+                              ["test_first_token_is_distributed_as_target",
+                               "test_bonus_is_distributed_as_last_target_row"]),
+    "token_race_weight": ("arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)x) / w[x] : INFINITY;",
+                          "arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)x) : INFINITY;",
+                          ["test_first_token_is_distributed_as_target", "test_bonus_is_distributed_as_last_target_row"]),
+    "philox_constant": ("uint64_t p0 = (uint64_t)0xD2511F53u * c0;", "uint64_t p0 = (uint64_t)0xD2511F55u * c0;",
+                        ["test_philox_known_answer_vectors"]),
+    "fanout_tie_order": ("return (x->id > y->id) - (x->id < y->id);", "return (x->id < y->id) - (x->id > y->id);",
+                         ["test_fanout_vs_numpy_lexsort"]),
+    "greedy_last_tie": ("if (best < 0 || v > bv) { best = x; bv = v; }", "if (best < 0 || v >= bv) { best = x; bv = v; }",
+                        ["test_greedy_matches_numpy_argmax"]),
+    "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
+                       ["test_fanout_sizes_golden"]),
+}
+
+
+def _calls(name):
+    fn = getattr(pins, name)
+    if name == "test_acceptance_rate_is_one_minus_tvd":
+        return [lambda: fn(1.0), lambda: fn(0.6)]
+    if name == "test_fanout_vs_numpy_lexsort":
+        return [lambda: fn(None), lambda: fn(8)]
+    return [fn]
+
+
+@pytest.mark.parametrize("mutant", sorted(MUTANTS))
+def test_mutant_is_caught(mutant, tmp_path, monkeypatch):
+    old, new, tests = MUTANTS[mutant]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation site not found for {mutant}"
+    msrc = tmp_path / "mutant.c"
+    msrc.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.check_call(["gcc", "-O2", "-std=gnu11", "-fPIC", "-shared", "-o", str(lib), str(msrc), "-lm"])
+    monkeypatch.setattr(oracle, "_lib", None)
+    monkeypatch.setattr(oracle, "build", lambda force=False: str(lib))
+    caught = []
+    for name in tests:
+        for call in _calls(name):
+            try:
+                call()
+            except AssertionError:
+                caught.append(name)
+                break
+    monkeypatch.setattr(oracle, "_lib", None)
+    assert caught, f"mutant {mutant} survived {tests}"

@@ -49,32 +49,29 @@ def _chi2_ok(counts, probs, min_p=1e-6):
 
 
 # ----------------------------------------------------------------- Philox
-def test_philox_matches_numpy_bitgenerator():
-    """Philox4x64-10 against numpy.random.Philox (numpy steps the counter
-    before each block, so numpy(counter=c-1) yields the block for c)."""
-    rng = np.random.default_rng(RNG_SEED)
-    for _ in range(20):
-        ctr = [int(x) for x in rng.integers(1, 2 ** 63, 4, dtype=np.int64)]
-        key = [int(x) for x in rng.integers(0, 2 ** 63, 2, dtype=np.int64)]
-        bg = np.random.Philox(key=key, counter=[ctr[0] - 1] + ctr[1:])
-        ref = bg.random_raw(4)
-        got = oracle.philox4x64_10(ctr, key)
-        assert np.array_equal(ref.astype(np.uint64), got)
+def test_philox_known_answer_vectors():
+    """Philox4x32-10 against the known-answer vectors published with its
+    reference implementation."""
+    rows = _read_golden("philox4x32_10_kat.txt")
+    assert len(rows) == 3
+    for r in rows:
+        words = [int(x, 16) for x in r]
+        ctr, key, ref = words[:4], words[4:6], words[6:10]
+        assert list(oracle.philox4x32_10(ctr, key)) == ref
 
 
 def test_uniform_word_mapping():
-    """uniform(n) takes word n % 4 of the block at counter (n/4, stream, trial, pos)."""
+    """uniform(n) = ((w >> 8) + 1) * 2^-24 for word n % 4 of the block at
+    counter (n / 4, stream, trial, pos) and key (low, high half of the key)."""
     key = 0x1234_5678_9ABC_DEF0
-    for n in range(9):
-        # numpy steps the 256-bit counter before each block, with carry:
-        # (2^64-1, s-1, t, p) steps to (0, s, t, p).
-        c0 = n >> 2
-        ctr = [c0 - 1, 3, 7, 2] if c0 > 0 else [2 ** 64 - 1, 2, 7, 2]
-        bg = np.random.Philox(key=np.array([key, 0], np.uint64), counter=np.array(ctr, np.uint64))
-        w = bg.random_raw(4)[n & 3]
+    seen = set()
+    for n in range(12):
+        w = oracle.philox4x32_10([n >> 2, 3, 7, 2], [key & 0xFFFFFFFF, key >> 32])[n & 3]
         u = oracle.uniform(key, 3, 7, 2, n)
-        assert u == ((int(w) >> 40) + 1) * 2.0 ** -24
+        assert u == ((int(w) >> 8) + 1) * 2.0 ** -24
         assert 0 < u <= 1
+        seen.add(u)
+    assert len(seen) == 12
 
 
 # ----------------------------------------------------------------- softmax
@@ -358,6 +355,29 @@ def test_bonus_is_distributed_as_last_target_row():
     pb = _probs(zb)
     counts = np.bincount(out["out_tokens"][:, 1], minlength=V)[ids]
     ok, pv = _chi2_ok(counts, pb[ids])
+    assert ok, pv
+
+
+def test_dense_support_draw_over_sub_blocks():
+    """Every id of a 1500-id vocabulary (two blocks, 47 sub-blocks) carries
+    mass: the bonus draw matches p over all ids."""
+    rng = np.random.default_rng(16)
+    V, B = 1500, 60000
+    zb = rng.normal(0, 0.7, V).astype(np.float32)
+    zl = rng.normal(0, 1, V).astype(np.float32)
+    z = np.broadcast_to(np.stack([zl, zb]), (B, 2, V)).astype(np.float32)
+    d = np.broadcast_to(zl, (B, 1, V)).astype(np.float32)
+    tok = np.zeros((B, 1), np.int32)
+    out = _chain(z, d, tok, np.ones((B, 1), np.float32), _keys(B, 17))
+    assert (out["accept_count"] == 1).all()
+    counts = np.bincount(out["out_tokens"][:, 1], minlength=V)
+    pb = _probs(zb)
+    ok, pv = _chi2_ok(counts, pb)
+    assert ok, pv
+    # coarser check per sub-block of 32 ids
+    sub = np.add.reduceat(counts, np.arange(0, V, 32))
+    psub = np.add.reduceat(pb, np.arange(0, V, 32))
+    ok, pv = _chi2_ok(sub, psub)
     assert ok, pv
 
 

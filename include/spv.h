@@ -118,6 +118,43 @@ spv_status spv_verify_chain(const void *target_logits, const void *draft_logits,
 /* Workspace bytes spv_verify_chain needs (also valid for T == 0). */
 size_t spv_chain_workspace_bytes(int B, int gamma, int V);
 
+/* Bytes of device memory behind spv_verify_chain_noalloc (per GPU, held from
+ * library load until process exit). */
+#define SPV_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
+
+/*
+ * spv_verify_chain_noalloc -- spv_verify_chain for callers that cannot
+ * allocate device memory.  The pages have no counterpart: this is an
+ * interface addition, not part of the method.
+ *
+ * Who needs it: a caller that cannot hand the library a workspace -- a
+ * serving loop whose device memory is entirely pre-reserved by its own pool,
+ * a host program that links this library but manages no device memory, or
+ * code running where cudaMalloc is not allowed or would stall the device
+ * (cudaMalloc / cudaFree may synchronise).  Same arguments, semantics and
+ * kernels as spv_verify_chain, without workspace / workspace_bytes: the
+ * scratch space is a fixed array of SPV_NOALLOC_SCRATCH_BYTES in the
+ * library's own device memory.  The call allocates and frees nothing.
+ *
+ *   - Returns SPV_ERR_UNSUPPORTED when the call needs more scratch than the
+ *     array holds (spv_chain_workspace_bytes(B, gamma, V) >
+ *     SPV_NOALLOC_SCRATCH_BYTES; e.g. B = 64, gamma = 4, V = 151,936 needs
+ *     about 0.7 MB, B = 256 about 2.9 MB).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current) and keeps it; make
+ *     that first call before any stream capture.
+ *   - Every call on a device uses the same array, and the array keeps the
+ *     last call's contents.  Calls whose kernels may overlap on the GPU (on
+ *     different streams, or from different host threads) race on it and
+ *     must be serialised by the caller.  Each call clears the array's error
+ *     word first (an asynchronous 4-byte memset on `stream`).
+ */
+spv_status spv_verify_chain_noalloc(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                                    const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
+                                    int B, int gamma, int V, float temperature,
+                                    int32_t *accept_count, int32_t *out_tokens, float *out_pq,
+                                    float *out_resid_norm, int32_t *row_status, void *stream);
+
 /*
  * spv_verify_greedy -- T = 0 ([SPD] "under greedy decoding we require an
  * exact argmax match").  a_i = argmax_x target[b,i,x] (lowest id on ties,

@@ -83,6 +83,65 @@ template <int DT> struct ChainOp {
         return row_of(P, b, static_cast<int>(row - static_cast<long long>(b) * P.R));
     }
 
+    static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 3;
+
+    // From the staged block.  bf16 stays packed for the max (bf16x2 max,
+    // NaN ignored like fmaxf) and is widened only for the exponentials.
+    __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta,
+                                                      const unsigned char *blk, int valid, int lane)
+    {
+        if (DT == 0) {
+            float v[32];
+            load_block_smem<DT>(v, blk, lane);
+            mask_tail<DT>(v, valid, lane);
+            block(P, row, beta, v, valid, lane);
+            return;
+        }
+        uint32_t w[16];
+        const uint4 *p = reinterpret_cast<const uint4 *>(blk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 t = p[j * 32 + lane];
+            w[4 * j] = t.x;
+            w[4 * j + 1] = t.y;
+            w[4 * j + 2] = t.z;
+            w[4 * j + 3] = t.w;
+        }
+        if (valid < G) {  // element 2h / 2h+1 of word h of vector j: j*256 + lane*8 + 2h (+1)
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int e0 = (q >> 2) * 256 + lane * 8 + 2 * (q & 3);
+                if (e0 >= valid) w[q] = (w[q] & 0xffff0000u) | 0xff80u;       // -inf in the low half
+                if (e0 + 1 >= valid) w[q] = (w[q] & 0x0000ffffu) | 0xff800000u; // and the high half
+            }
+        }
+        __nv_bfloat162 mx[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a)
+            mx[a] = __hmax2(*reinterpret_cast<const __nv_bfloat162 *>(&w[a]),
+                            *reinterpret_cast<const __nv_bfloat162 *>(&w[a + 8]));
+#pragma unroll
+        for (int a = 0; a < 4; ++a) mx[a] = __hmax2(mx[a], mx[a + 4]);
+        mx[0] = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
+        float m = fmaxf(__low2float(mx[0]), __high2float(mx[0]));
+        m = warp_max(m);
+        const float mu = (m == -INFINITY) ? 0.f : m;
+        const float mc = mu * P.c2;
+        const float delta = fmaf(mu, P.c2, -mc);
+        float sa[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            sa[(2 * q) & 3] += fast_exp2(fmaf(__uint_as_float(w[q] << 16), P.c2, -mc));
+            sa[(2 * q + 1) & 3] += fast_exp2(fmaf(__uint_as_float(w[q] & 0xffff0000u), P.c2, -mc));
+        }
+        float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
+        s = warp_sum(s);
+        if (lane == 0) {
+            s = fmaf(-s * 0.6931471805599453f, delta, s);
+            P.stats[row * P.nb + beta] = isnan(s) ? make_float2(__int_as_float(0x7fffffff), 0.f) : make_float2(m, s);
+        }
+    }
+
     // Block statistics: m = max z (raw), s = sum exp((z - m) / T).
     // The max runs as 8 independent chains and the sum as 4; each term is
     // ex2(z * c2 - mc) with mc = m * c2 rounded, one FFMA, and the rounding
@@ -505,6 +564,17 @@ template <int DT> struct GreedyOp {
     __device__ static __forceinline__ const void *row_ptr(const Params &P, long long row)
     {
         return P.target + static_cast<size_t>(row) * static_cast<size_t>(P.V) * EB;
+    }
+
+    static constexpr int CTAS_PER_SM = 2;
+
+    __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta,
+                                                      const unsigned char *blk, int valid, int lane)
+    {
+        float v[32];
+        load_block_smem<DT>(v, blk, lane);
+        mask_tail<DT>(v, valid, lane);
+        block(P, row, beta, v, valid, lane);
     }
 
     // Per-block (max, first argmax): four independent accumulators over the

@@ -51,6 +51,17 @@ template <int DT> struct FanoutOp {
         return P.draft + static_cast<size_t>(row) * static_cast<size_t>(P.V) * EB;
     }
 
+    static constexpr int CTAS_PER_SM = 2;
+
+    __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta,
+                                                      const unsigned char *blk, int valid, int lane)
+    {
+        float v[32];
+        load_block_smem<DT>(v, blk, lane);
+        mask_tail<DT>(v, valid, lane);
+        block(P, row, beta, v, valid, lane);
+    }
+
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int valid,
                                                  int lane)
     {

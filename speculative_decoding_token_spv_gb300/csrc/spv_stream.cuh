@@ -26,7 +26,7 @@ constexpr int CHUNK_BLOCKS = 8;               // sampler blocks per work item
 constexpr int CHUNK = G * CHUNK_BLOCKS;       // logits per work item
 constexpr int NCW = 8;                        // consumer warps (one block each)
 constexpr int THREADS = (NCW + 1) * 32;       // + one producer warp
-constexpr int STAGE_BYTES_BUDGET = 96 * 1024; // ring size: two CTAs fit on an SM
+constexpr int RING_BYTES_PER_SM = 192 * 1024; // shared-memory ring of all resident CTAs of an SM
 constexpr uint32_t WAIT_LIMIT = 1u << 22;     // try_wait polls before giving up
 constexpr int MAX_TRIALS = 64;                // residual rejection trials
 constexpr int STATUS_BAD_ROW = 4;
@@ -55,9 +55,12 @@ template <> struct DType<1> {  // bf16
     }
 };
 
-template <int DT> constexpr int stages()
+// Ring stages of one CTA when `ctas` CTAs share an SM (at least 2).
+template <int DT> constexpr int stages(int ctas)
 {
-    return STAGE_BYTES_BUDGET / (CHUNK * DType<DT>::BYTES);
+    return RING_BYTES_PER_SM / ctas / (CHUNK * DType<DT>::BYTES) < 2
+               ? 2
+               : RING_BYTES_PER_SM / ctas / (CHUNK * DType<DT>::BYTES);
 }
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -288,6 +291,16 @@ template <int DT> __device__ __forceinline__ void load_block_smem(float v[32], c
     }
 }
 
+// Elements of a partial block (index >= valid) become -inf.
+template <int DT> __device__ __forceinline__ void mask_tail(float v[32], int valid, int lane)
+{
+    if (valid < G) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e)
+            if (lane_index<DT>(lane, e) >= valid) v[e] = -INFINITY;
+    }
+}
+
 // From global memory, scalar loads (any alignment); elements >= valid are -inf.
 template <int DT>
 __device__ __forceinline__ void load_block_global(float v[32], const void *blk, int lane, int valid)
@@ -303,16 +316,20 @@ __device__ __forceinline__ void load_block_global(float v[32], const void *blk, 
 // Op supplies:
 //   struct Params  -- with total_items, nc (items per row), nb (blocks per
 //                     row), V and err fields;
+//   CTAS_PER_SM                          resident CTAs the kernel is built for;
 //   row_ptr(P, row)                      global address of a row;
-//   block(P, row, beta, v, valid, lane)  per-warp reduction of one block;
+//   block(P, row, beta, v, valid, lane)  per-warp reduction of one block
+//                                        (32 logits per lane as floats);
+//   block_smem(P, row, beta, blk, valid, lane)  the same from the staged
+//                                        block in shared memory;
 //   finalize(P, g, sm, warp, lane)       merge + outputs of group g (run by
 //                                        finalize_kernel, one CTA per group);
 //   struct Smem                          shared scratch of finalize.
 template <class Op, int DT, bool TMA>
-__global__ void __launch_bounds__(THREADS, 2) stream_kernel(const typename Op::Params P)
+__global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const typename Op::Params P)
 {
     constexpr int EB = DType<DT>::BYTES;
-    constexpr int S = stages<DT>();
+    constexpr int S = stages<DT>(Op::CTAS_PER_SM);
     constexpr int CHUNK_BYTES = CHUNK * EB;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full_bar[S];
@@ -381,20 +398,15 @@ __global__ void __launch_bounds__(THREADS, 2) stream_kernel(const typename Op::P
         const int beta = c * CHUNK_BLOCKS + warp;
         if (ok && beta < P.nb) {
             const int valid = min(G, P.V - beta * G);
-            float v[32];
             if (TMA) {
-                load_block_smem<DT>(v, ring + s * CHUNK_BYTES + warp * G * EB, lane);
-                if (valid < G) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        if (lane_index<DT>(lane, e) >= valid) v[e] = -INFINITY;
-                }
+                Op::block_smem(P, row, beta, ring + s * CHUNK_BYTES + warp * G * EB, valid, lane);
             } else {
+                float v[32];
                 const unsigned char *blk = reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) +
                                            static_cast<size_t>(beta) * G * EB;
                 load_block_global<DT>(v, blk, lane, valid);
+                Op::block(P, row, beta, v, valid, lane);
             }
-            Op::block(P, row, beta, v, valid, lane);
         }
         if (TMA) {
             __syncwarp();
@@ -423,7 +435,7 @@ template <class Op, int DT>
 static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma, int groups, cudaStream_t st)
 {
     void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
-    const int smem = tma ? stages<DT>() * CHUNK * DType<DT>::BYTES : 0;
+    const int smem = tma ? stages<DT>(Op::CTAS_PER_SM) * CHUNK * DType<DT>::BYTES : 0;
     // Per device and kernel: the shared-memory attribute and the resident
     // CTA count are set / queried once (a kernel is a function of the
     // template arguments, so a function-local static is per kernel).

@@ -45,10 +45,11 @@ struct ChainParams {
     float *resid;    // [B*nb] residual block masses (direct draw / normaliser only)
 };
 
-constexpr int STAT_CACHE = 4096;  // block statistics staged in shared memory when R * nb fits
+constexpr int FW = 16;            // widest chain finalize CTA (warps; one residual trial each per round)
+constexpr int STAT_CACHE = 4096;  // target-row block statistics staged in shared memory when they fit
 
 struct ChainSmem {
-    float2 st[STAT_CACHE];  // block statistics of all rows of the sequence (if they fit)
+    float2 st[STAT_CACHE];  // target rows: (block max, race factor 2^((M - m) c2) / S or -1 if empty)
     float M[2 * 32 + 1];    // row max of the raw logits
     float S[2 * 32 + 1];    // row sum exp((z - M)/T)
     int x[32];              // draft tokens
@@ -57,14 +58,18 @@ struct ChainSmem {
     int bad;
     int k;
     int cached;
-    int trial_x[NCW];
-    int trial_acc[NCW];
-    float wbest[NCW];
-    int wbest_i[NCW];
+    int trial_x[FW];
+    int trial_acc[FW];
     int result;
     float Z;
     uint64_t key;
 };
+
+// Barrier of the FWV warps of a chain finalize CTA.
+template <int FWV> __device__ __forceinline__ void fin_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(FWV * 32) : "memory");
+}
 
 template <int DT> struct ChainOp {
     using Params = ChainParams;
@@ -174,33 +179,36 @@ template <int DT> struct ChainOp {
         return expf((DType<DT>::load(rowp, x) - M) * P.invT) / S;
     }
 
-    __device__ static __forceinline__ float2 stat(const Params &P, const Smem &sm, int b, int rho, int beta)
-    {
-        return sm.cached ? sm.st[rho * P.nb + beta]
-                         : __ldcg(&P.stats[(static_cast<long long>(b) * P.R + rho) * P.nb + beta]);
-    }
-
     // Level 1 of a draw from softmax(row rho / T): the block with the
     // smallest E_beta / W_beta, W_beta = 2^((m_beta - M) c2) S_beta up to the
-    // row normaliser.  Every lane gets the winner.
+    // row normaliser, i.e. arrival E_beta * f_beta with the factor
+    // f_beta = 2^((M - m_beta) c2) / S_beta staged by the merge (computed here
+    // when the statistics were not staged).  Every lane gets the winner.
     __device__ static int race_blocks_p(const Params &P, const Smem &sm, int b, int rho, float M, uint64_t key,
                                         uint32_t trial, uint32_t pos, int lane)
     {
         float best = INFINITY;
         int bi = INT_MAX;
         for (int g = lane; 4 * g < P.nb; g += 32) {
-            float2 st[4];
+            float f[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int beta = 4 * g + e;
-                st[e] = beta < P.nb ? stat(P, sm, b, rho, beta) : make_float2(0.f, 0.f);
+                if (beta >= P.nb) {
+                    f[e] = -1.f;
+                } else if (sm.cached) {
+                    f[e] = sm.st[rho * P.nb + beta].y;
+                } else {
+                    const float2 st = __ldcg(&P.stats[(static_cast<long long>(b) * P.R + rho) * P.nb + beta]);
+                    f[e] = st.y > 0.f ? fast_exp2((M - st.x) * P.c2) / st.y : -1.f;
+                }
             }
             uint32_t w[4];
             philox_group(w, key, STREAM_BLOCK, trial, pos, static_cast<uint32_t>(g));
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                if (st[e].y > 0.f) {
-                    const float A = arrival(expo(w[e]), fast_exp2((M - st[e].x) * P.c2) / st[e].y);
+                if (f[e] >= 0.f) {
+                    const float A = arrival(expo(w[e]), f[e]);
                     if (A < best) {
                         best = A;
                         bi = 4 * g + e;
@@ -280,33 +288,6 @@ template <int DT> struct ChainOp {
         return xi;
     }
 
-    // Residual masses w = max(0, p - q) of one row pair, per block, into
-    // P.resid; returns Z = sum w in sm.Z.  All consumer warps.
-    __device__ static void residual_pass(const Params &P, int b, const unsigned char *tp, const unsigned char *dp,
-                                         float Mt, float St, float Md, float Sd, Smem &sm, int warp, int lane)
-    {
-        const float it = 1.f / St, id = 1.f / Sd;
-        for (int beta = warp; beta < P.nb; beta += NCW) {
-            float part = 0.f;
-            const int hi = min(P.V, (beta + 1) * G);
-            for (int x = beta * G + lane; x < hi; x += 32) {
-                const float p = expf((DType<DT>::load(tp, x) - Mt) * P.invT) * it;
-                const float q = expf((DType<DT>::load(dp, x) - Md) * P.invT) * id;
-                part += fmaxf(p - q, 0.f);
-            }
-            part = warp_sum(part);
-            if (lane == 0) P.resid[static_cast<size_t>(b) * P.nb + beta] = part;
-        }
-        consumer_sync();
-        if (warp == 0) {
-            float z = 0.f;
-            for (int beta = lane; beta < P.nb; beta += 32) z += __ldcg(&P.resid[static_cast<size_t>(b) * P.nb + beta]);
-            z = warp_sum(z);
-            if (lane == 0) sm.Z = z;
-        }
-        consumer_sync();
-    }
-
     // Direct race over the residual w = max(0, p - q) (after the rejection
     // trials all failed): block masses from residual_pass, then sub-blocks
     // and ids of the winning block (target and draft logits in tb / db).
@@ -362,18 +343,61 @@ template <int DT> struct ChainOp {
         return xi;
     }
 
-    static constexpr int FIN_BUF_FLOATS = 2 * NCW * G;  // per warp: one target and one draft block
+};
+
+// The chain finalize at a given width: FWV warps, FWV residual trials per
+// round.  Wider CTAs draw in fewer rounds; narrower ones fit two per SM.
+template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
+    using Base = ChainOp<DT>;
+    using Params = ChainParams;
+    using Smem = ChainSmem;
+    using Base::row_of;
+    using Base::race_blocks_p;
+    using Base::load_block;
+    using Base::race_in_block_p;
+    using Base::race_resid;
+
+    // Residual masses w = max(0, p - q) of one row pair, per block, into
+    // P.resid; returns Z = sum w in sm.Z.  All consumer warps.
+    __device__ static void residual_pass(const Params &P, int b, const unsigned char *tp, const unsigned char *dp,
+                                         float Mt, float St, float Md, float Sd, Smem &sm, int warp, int lane)
+    {
+        const float it = 1.f / St, id = 1.f / Sd;
+        for (int beta = warp; beta < P.nb; beta += FWV) {
+            float part = 0.f;
+            const int hi = min(P.V, (beta + 1) * G);
+            for (int x = beta * G + lane; x < hi; x += 32) {
+                const float p = expf((DType<DT>::load(tp, x) - Mt) * P.invT) * it;
+                const float q = expf((DType<DT>::load(dp, x) - Md) * P.invT) * id;
+                part += fmaxf(p - q, 0.f);
+            }
+            part = warp_sum(part);
+            if (lane == 0) P.resid[static_cast<size_t>(b) * P.nb + beta] = part;
+        }
+        fin_sync<FWV>();
+        if (warp == 0) {
+            float z = 0.f;
+            for (int beta = lane; beta < P.nb; beta += 32) z += __ldcg(&P.resid[static_cast<size_t>(b) * P.nb + beta]);
+            z = warp_sum(z);
+            if (lane == 0) sm.Z = z;
+        }
+        fin_sync<FWV>();
+    }
+
+    static constexpr int FIN_WARPS = FWV;
+    static constexpr int FIN_BUF_FLOATS = 2 * FWV * G;  // per warp: one target and one draft block
 
     __device__ static void finalize(const Params &P, int b, Smem &sm, float *buf, int warp, int lane)
     {
         const int R = P.R, g = P.gamma, nb = P.nb;
+        constexpr int NT = FWV * 32;
         float *tb = buf + warp * 2 * G, *db = tb + G;  // this warp's block buffers
         // A. Inputs that do not depend on the streaming grid: tokens, r, key
         //    and the logits of each draft token (overlaps the grid's tail).
         if (threadIdx.x == 0) {
             sm.bad = 0;
             sm.key = P.keys[b];
-            sm.cached = (R * nb <= STAT_CACHE) ? 1 : 0;
+            sm.cached = ((g + 1) * nb <= STAT_CACHE) ? 1 : 0;
         }
         if (warp == 0 && lane < g) {
             const int x = P.tokens[static_cast<size_t>(b) * g + lane];
@@ -387,29 +411,33 @@ template <int DT> struct ChainOp {
             }
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
-        consumer_sync();
+        fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
-        // B. Row statistics from the block statistics (one warp per row); all
-        //    loads of a row are in flight at once; rows are staged in shared
-        //    memory for the draw when they fit.
-        for (int rho = warp; rho < R; rho += NCW) {
-            const float2 *st = P.stats + (static_cast<long long>(b) * R + rho) * nb;
+        // B. Row statistics from the block statistics: one half-warp per row,
+        //    all rows at once, all loads of a row in flight together.  Target
+        //    rows keep (m_beta, race factor) in shared memory for the draw.
+        const int half = lane >> 4, hl = lane & 15;
+        for (int rho0 = 0; rho0 < R; rho0 += 2 * FWV) {
+            const int rho = rho0 + 2 * warp + half;
+            const bool active = rho < R;
+            const float2 *st = P.stats + (static_cast<long long>(b) * R + (active ? rho : 0)) * nb;
+            const bool keep = active && rho <= g && sm.cached;
             float m = -INFINITY, s = 0.f;
             bool bad = false;
-            for (int base = 0; base < nb; base += 32 * 8) {
+            for (int base = 0; base < nb; base += 16 * 8) {
                 float2 v[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const int beta = base + 32 * u + lane;
-                    v[u] = beta < nb ? __ldcg(&st[beta]) : make_float2(-INFINITY, 0.f);
+                    const int beta = base + 16 * u + hl;
+                    v[u] = (active && beta < nb) ? __ldcg(&st[beta]) : make_float2(-INFINITY, 0.f);
                 }
                 float cm = -INFINITY;
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                    const int beta = base + 32 * u + lane;
+                    const int beta = base + 16 * u + hl;
                     if (isnan(v[u].x)) bad = true;
                     else cm = fmaxf(cm, v[u].x);
-                    if (sm.cached && beta < nb) sm.st[rho * nb + beta] = v[u];
+                    if (keep && beta < nb) sm.st[rho * nb + beta] = v[u];
                 }
                 const float nm = fmaxf(m, cm);
                 if (nm != -INFINITY) {
@@ -421,21 +449,32 @@ template <int DT> struct ChainOp {
                     m = nm;
                 }
             }
-            const float mw = warp_max(m);
+            float mw = m;
+#pragma unroll
+            for (int o = 8; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
             s = (s > 0.f) ? s * expf((m - mw) * P.invT) : 0.f;
-            s = warp_sum(s);
-            bad = __any_sync(0xffffffffu, bad);
-            if (lane == 0) {
+#pragma unroll
+            for (int o = 8; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            const unsigned badm = __ballot_sync(0xffffffffu, bad);
+            const bool rowbad = ((badm >> (16 * half)) & 0xffffu) != 0;
+            if (active && hl == 0) {
                 sm.M[rho] = mw;
                 sm.S[rho] = s;
-                if (bad || !(s > 0.f)) atomicOr(&sm.bad, 1);
+                if (rowbad || !(s > 0.f)) atomicOr(&sm.bad, 1);
+            }
+            if (keep && !rowbad && mw != -INFINITY) {
+                // entry beta was staged by this lane (beta = hl mod 16): no warp barrier needed
+                for (int beta = hl; beta < nb; beta += 16) {
+                    const float2 v = sm.st[rho * nb + beta];
+                    sm.st[rho * nb + beta].y = v.y > 0.f ? fast_exp2((mw - v.x) * P.c2) / v.y : -1.f;
+                }
             }
         }
-        consumer_sync();
+        fin_sync<FWV>();
         if (sm.bad) {
-            for (int i = threadIdx.x; i <= g; i += NCW * 32) P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
+            for (int i = threadIdx.x; i <= g; i += NT) P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
             if (P.out_pq)
-                for (int i = threadIdx.x; i < 2 * g; i += NCW * 32)
+                for (int i = threadIdx.x; i < 2 * g; i += NT)
                     P.out_pq[static_cast<size_t>(b) * 2 * g + i] = __int_as_float(0x7fffffff);
             if (threadIdx.x == 0) {
                 P.accept_count[b] = -1;
@@ -463,7 +502,7 @@ template <int DT> struct ChainOp {
                 sm.result = -1;
             }
         }
-        consumer_sync();
+        fin_sync<FWV>();
         const int k = sm.k;
         const uint64_t key = sm.key;
         const unsigned char *tp = row_of(P, b, k);
@@ -477,13 +516,13 @@ template <int DT> struct ChainOp {
                 const int x = race_in_block_p(P, tb, beta, key, STREAM_SUB, STREAM_TOKEN, 0u, static_cast<uint32_t>(g), lane);
                 if (lane == 0) sm.result = x;
             }
-            consumer_sync();
+            fin_sync<FWV>();
         } else {
-            // Residual: rejection trials from p_k, eight at a time (one per warp).
+            // Residual: rejection trials from p_k, FWV at a time (one per warp).
             const unsigned char *dp = row_of(P, b, g + 1 + k);
             const float Md = sm.M[g + 1 + k], Sd = sm.S[g + 1 + k];
-            for (int round = 0; round < MAX_TRIALS / NCW; ++round) {
-                const uint32_t t = static_cast<uint32_t>(round * NCW + warp);
+            for (int round = 0; round < MAX_TRIALS / FWV; ++round) {
+                const uint32_t t = static_cast<uint32_t>(round * FWV + warp);
                 const int beta = race_blocks_p(P, sm, b, k, Mt, key, t, static_cast<uint32_t>(k), lane);
                 load_block(P, tp, beta, tb, lane);
                 load_block(P, dp, beta, db, lane);
@@ -497,15 +536,15 @@ template <int DT> struct ChainOp {
                     sm.trial_x[warp] = x;
                     sm.trial_acc[warp] = (q <= (1.0f - v) * p) ? 1 : 0;
                 }
-                consumer_sync();
+                fin_sync<FWV>();
                 if (threadIdx.x == 0) {
-                    for (int w = 0; w < NCW; ++w)
+                    for (int w = 0; w < FWV; ++w)
                         if (sm.trial_acc[w]) {
                             sm.result = sm.trial_x[w];
                             break;
                         }
                 }
-                consumer_sync();
+                fin_sync<FWV>();
                 if (sm.result >= 0) break;
             }
             const bool fallback = sm.result < 0;
@@ -516,13 +555,13 @@ template <int DT> struct ChainOp {
                         const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(k), tb, db, lane);
                         if (lane == 0) sm.result = x;
                     }
-                    consumer_sync();
+                    fin_sync<FWV>();
                 }
             }
         }
         // E. Outputs.
         const int res = sm.result;
-        for (int i = threadIdx.x; i <= g; i += NCW * 32) {
+        for (int i = threadIdx.x; i <= g; i += NT) {
             int v = -1;
             if (i < k) v = sm.x[i];
             else if (i == k) v = res;
@@ -612,6 +651,7 @@ template <int DT> struct GreedyOp {
         }
     }
 
+    static constexpr int FIN_WARPS = NCW;
     static constexpr int FIN_BUF_FLOATS = 0;
 
     __device__ static void finalize(const Params &P, int b, Smem &sm, float *, int warp, int lane)
@@ -730,8 +770,17 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
     P.out_pq = L.out_pq;
     P.out_Z = L.out_Z;
     P.row_status = L.row_status;
-    return L.dtype == 0 ? launch_stream_finalize<ChainOp<0>, 0>(P, L.tma, L.B, st)
-                        : launch_stream_finalize<ChainOp<1>, 1>(P, L.tma, L.B, st);
+    // One finalize CTA per sequence: the 16-warp CTA (one per SM) while the
+    // sequences fit on the SMs at once, else the 8-warp CTA (two per SM).
+    int sms = 0;
+    cudaError_t e = device_sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    const bool wide = L.B <= sms;
+    if (L.dtype == 0)
+        return wide ? launch_stream_finalize<ChainOp<0>, ChainFin<0, FW>, 0>(P, L.tma, L.B, st)
+                    : launch_stream_finalize<ChainOp<0>, ChainFin<0, NCW>, 0>(P, L.tma, L.B, st);
+    return wide ? launch_stream_finalize<ChainOp<1>, ChainFin<1, FW>, 1>(P, L.tma, L.B, st)
+                : launch_stream_finalize<ChainOp<1>, ChainFin<1, NCW>, 1>(P, L.tma, L.B, st);
 }
 
 cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st)
@@ -752,8 +801,8 @@ cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st)
     P.accept_count = L.accept_count;
     P.out_tokens = L.out_tokens;
     P.row_status = L.row_status;
-    return L.dtype == 0 ? launch_stream_finalize<GreedyOp<0>, 0>(P, L.tma, L.B, st)
-                        : launch_stream_finalize<GreedyOp<1>, 1>(P, L.tma, L.B, st);
+    return L.dtype == 0 ? launch_stream_finalize<GreedyOp<0>, GreedyOp<0>, 0>(P, L.tma, L.B, st)
+                        : launch_stream_finalize<GreedyOp<1>, GreedyOp<1>, 1>(P, L.tma, L.B, st);
 }
 
 }  // namespace spv

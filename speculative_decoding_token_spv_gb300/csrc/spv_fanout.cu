@@ -100,6 +100,7 @@ template <int DT> struct FanoutOp {
         }
     }
 
+    static constexpr int FIN_WARPS = NCW;
     static constexpr int FIN_BUF_FLOATS = 0;
 
     __device__ static void finalize(const Params &P, int row, Smem &sm, float *, int warp, int lane)
@@ -217,8 +218,8 @@ cudaError_t launch_fanout(const FanoutLaunch &L, cudaStream_t st)
     P.out_ids = L.out_ids;
     P.row_status = L.row_status;
     const int rows = L.B * L.K1;
-    return L.dtype == 0 ? launch_stream_finalize<FanoutOp<0>, 0>(P, L.tma, rows, st)
-                        : launch_stream_finalize<FanoutOp<1>, 1>(P, L.tma, rows, st);
+    return L.dtype == 0 ? launch_stream_finalize<FanoutOp<0>, FanoutOp<0>, 0>(P, L.tma, rows, st)
+                        : launch_stream_finalize<FanoutOp<1>, FanoutOp<1>, 1>(P, L.tma, rows, st);
 }
 
 }  // namespace spv

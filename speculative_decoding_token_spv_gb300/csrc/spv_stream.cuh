@@ -417,9 +417,10 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
     }
 }
 
-// One CTA (NCW warps) per group: merges the group's partial results once the
+// One CTA (Op::FIN_WARPS warps) per group: merges the group's partial results once the
 // streaming grid it depends on has finished, and writes the outputs.
-template <class Op, int DT> __global__ void __launch_bounds__(NCW * 32) finalize_kernel(const typename Op::Params P)
+template <class Op, int DT>
+__global__ void __launch_bounds__(Op::FIN_WARPS * 32) finalize_kernel(const typename Op::Params P)
 {
     __shared__ typename Op::Smem sm;
     extern __shared__ __align__(16) float fin_buf[];  // Op::FIN_BUF_FLOATS floats
@@ -428,10 +429,29 @@ template <class Op, int DT> __global__ void __launch_bounds__(NCW * 32) finalize
     Op::finalize(P, static_cast<int>(blockIdx.x), sm, fin_buf, threadIdx.x >> 5, threadIdx.x & 31);
 }
 
-// Launches the streaming grid (persistent: as many CTAs as fit, capped by the
-// item count) and then the finalize grid of `groups` CTAs as a programmatic
-// dependent launch on the same stream.
-template <class Op, int DT>
+// SM count of the current device (queried once per device).
+static inline cudaError_t device_sm_count(int *out)
+{
+    constexpr int MAX_DEV = 64;
+    static int cache[MAX_DEV];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < MAX_DEV && cache[dev] > 0) {
+        *out = cache[dev];
+        return cudaSuccess;
+    }
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if (dev >= 0 && dev < MAX_DEV) cache[dev] = sms;
+    *out = sms;
+    return cudaSuccess;
+}
+
+// Launches the streaming grid of Op (persistent: as many CTAs as fit, capped
+// by the item count) and then the finalize grid of Fin, `groups` CTAs, as a
+// programmatic dependent launch on the same stream.
+template <class Op, class Fin, int DT>
 static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma, int groups, cudaStream_t st)
 {
     void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
@@ -453,8 +473,8 @@ static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma
         if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, THREADS, smem)) != cudaSuccess)
             return e;
         cap = (per_sm < 1 ? 1 : per_sm) * sms;
-        if ((e = cudaFuncSetAttribute(finalize_kernel<Op, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                      Op::FIN_BUF_FLOATS * 4)) != cudaSuccess)
+        if ((e = cudaFuncSetAttribute(finalize_kernel<Fin, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      Fin::FIN_BUF_FLOATS * 4)) != cudaSuccess)
             return e;
         if (dev >= 0 && dev < MAX_DEV) cap_cache[dev] = cap;
     }
@@ -464,15 +484,15 @@ static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(groups));
-    cfg.blockDim = dim3(NCW * 32);
-    cfg.dynamicSmemBytes = Op::FIN_BUF_FLOATS * 4;
+    cfg.blockDim = dim3(Fin::FIN_WARPS * 32);
+    cfg.dynamicSmemBytes = Fin::FIN_BUF_FLOATS * 4;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, finalize_kernel<Op, DT>, P);
+    return cudaLaunchKernelEx(&cfg, finalize_kernel<Fin, DT>, P);
 }
 
 }  // namespace spv

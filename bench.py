@@ -331,45 +331,76 @@ def run_spv(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
+def time_graph(fn, n_inner=20, n_outer=10):
+    """Average device ms per call of `fn` replayed from a CUDA graph that holds
+    `n_inner` calls (launch overhead of the host removed)."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(n_inner):
+                fn()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(st)
+    for _ in range(n_outer):
+        g.replay()
+    b.record(st)
+    b.synchronize()
+    return a.elapsed_time(b) / (n_outer * n_inner)
+
+
 def run_variants(spv, dev, stream, args):
-    """Every hot-path row on its own workload: rows/s and GB/s per call."""
+    """Every hot-path row on its own workload: device time per call, replayed
+    from a CUDA graph (small calls are otherwise bound by host launch cost)."""
     import torch
 
     from speculative_decoding_token_spv_gb300 import workloads
     peak, _ = measured_peaks()
     res = []
-    n, wu = 30, 5
 
     def add(name, ms, algo, rows):
         gbs = algo / (ms * 1e-3) / 1e9
         res.append({"workload": name, "ms": round(ms, 5), "rows_per_s": rows / (ms * 1e-3), "gb_per_s": round(gbs, 1),
                     "frac_measured": round(gbs / peak, 4), "frac_8000": round(gbs / 8000.0, 4),
-                    "algorithmic_bytes": algo})
+                    "algorithmic_bytes": algo, "timing": "cuda graph replay"})
 
     cases = [("sweep B=64 fp32 T=0", lambda: workloads.sweep(B=64, dtype=torch.float32, device=dev, temperature=0.0)),
              ("sweep B=64 bf16 T=1", lambda: workloads.sweep(B=64, dtype=torch.bfloat16, device=dev)),
+             ("sweep B=128 fp32 T=1", lambda: workloads.sweep(B=128, dtype=torch.float32, device=dev)),
              ("sweep B=256 fp32 T=1", lambda: workloads.sweep(B=256, dtype=torch.float32, device=dev)),
              ("sweep B=256 bf16 T=1", lambda: workloads.sweep(B=256, dtype=torch.bfloat16, device=dev)),
+             ("sweep B=256 fp32 T=0", lambda: workloads.sweep(B=256, dtype=torch.float32, device=dev, temperature=0.0)),
              ("sweep B=8 fp32 T=1", lambda: workloads.sweep(B=8, dtype=torch.float32, device=dev)),
              ("sweep B=1 fp32 T=1", lambda: workloads.sweep(B=1, dtype=torch.float32, device=dev)),
+             ("tiny B=1 g=4 V=1000 fp32 T=1", lambda: workloads.tiny(device=dev)),
              ("spd B=64 g=1 bf16 T=1", lambda: workloads.spd(device=dev)),
              ("spd B=64 g=1 bf16 T=0", lambda: workloads.spd(device=dev, temperature=0.0)),
              ("eagle B=32 g=7 bf16 T=1", lambda: workloads.eagle(gamma=7, device=dev)),
-             ("eagle B=32 g=15 bf16 T=1", lambda: workloads.eagle(gamma=15, device=dev))]
+             ("eagle B=32 g=15 bf16 T=1", lambda: workloads.eagle(gamma=15, device=dev)),
+             ("eagle B=32 g=15 bf16 T=0", lambda: workloads.eagle(gamma=15, device=dev, temperature=0.0))]
     for name, mk in cases:
         w = mk()
         eb = w.target.element_size()
         ws = spv.new_workspace(spv.spv_chain_workspace_bytes(w.B, w.gamma, w.V), dev)
         o = spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature, workspace=ws)
-        ms = time_device(lambda i: spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature,
-                                                       workspace=ws, out=o), n, wu, stream)
+        ms = time_graph(lambda: spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature,
+                                                     workspace=ws, out=o))
         add(name, ms, chain_bytes(w.B, w.gamma, w.V, eb, w.temperature), w.B * (w.gamma + 1))
         del w, o, ws
     fw = workloads.fanout(device=dev)
     ws = spv.new_workspace(spv.spv_fanout_workspace_bytes(8, 4, fw.draft.shape[2], max(fw.fanout)), dev)
     o = spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws)
-    ms = time_device(lambda i: spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws, out=o), n, wu,
-                     stream)
+    ms = time_graph(lambda: spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws, out=o))
     add("fanout B=8 K=4 fp32 F=[8,7,6,5,4]", ms, fanout_bytes(8, 5, fw.draft.shape[2], 4, sum(fw.fanout)), 8 * 5)
     torch.cuda.synchronize()
     return res

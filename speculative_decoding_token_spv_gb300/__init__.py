@@ -73,7 +73,7 @@ def spv_status_string(status: int) -> str:
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()
 
 
 def _dtype_code(t: torch.Tensor) -> int:
@@ -97,7 +97,7 @@ def _cuda(t: torch.Tensor, name: str, dtype=None) -> torch.Tensor:
 def _stream(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
 
 
 def _check(status: int, what: str):
@@ -163,15 +163,17 @@ def spv_verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, 
     need = lib.spv_chain_workspace_bytes(B, g, V)
     if workspace is None:
         workspace = new_workspace(need, dev)
-    out = dict(out or {})
-    out.setdefault("accept_count", torch.empty(B, dtype=torch.int32, device=dev))
-    out.setdefault("out_tokens", torch.empty(B, g + 1, dtype=torch.int32, device=dev))
-    if want_pq and not greedy:
-        out.setdefault("pq", torch.empty(B, g, 2, dtype=torch.float32, device=dev))
-    if want_resid_norm and not greedy:
-        out.setdefault("resid_norm", torch.empty(B, dtype=torch.float32, device=dev))
-    if want_status:
-        out.setdefault("row_status", torch.empty(B, dtype=torch.int32, device=dev))
+    out = dict(out) if out else {}
+    if "accept_count" not in out:
+        out["accept_count"] = torch.empty(B, dtype=torch.int32, device=dev)
+    if "out_tokens" not in out:
+        out["out_tokens"] = torch.empty(B, g + 1, dtype=torch.int32, device=dev)
+    if want_pq and not greedy and "pq" not in out:
+        out["pq"] = torch.empty(B, g, 2, dtype=torch.float32, device=dev)
+    if want_resid_norm and not greedy and "resid_norm" not in out:
+        out["resid_norm"] = torch.empty(B, dtype=torch.float32, device=dev)
+    if want_status and "row_status" not in out:
+        out["row_status"] = torch.empty(B, dtype=torch.int32, device=dev)
     st = lib.spv_verify_chain(_ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(r),
                               _ptr(sample_keys), B, g, V, float(temperature), _ptr(out["accept_count"]),
                               _ptr(out["out_tokens"]), _ptr(out.get("pq")), _ptr(out.get("resid_norm")),
@@ -194,11 +196,13 @@ def spv_verify_greedy(target_logits, draft_tokens, *, workspace=None, out=None, 
     lib = load_library()
     if workspace is None:
         workspace = new_workspace(lib.spv_greedy_workspace_bytes(B, g, V), dev)
-    out = dict(out or {})
-    out.setdefault("accept_count", torch.empty(B, dtype=torch.int32, device=dev))
-    out.setdefault("out_tokens", torch.empty(B, g + 1, dtype=torch.int32, device=dev))
-    if want_status:
-        out.setdefault("row_status", torch.empty(B, dtype=torch.int32, device=dev))
+    out = dict(out) if out else {}
+    if "accept_count" not in out:
+        out["accept_count"] = torch.empty(B, dtype=torch.int32, device=dev)
+    if "out_tokens" not in out:
+        out["out_tokens"] = torch.empty(B, g + 1, dtype=torch.int32, device=dev)
+    if want_status and "row_status" not in out:
+        out["row_status"] = torch.empty(B, dtype=torch.int32, device=dev)
     st = lib.spv_verify_greedy(_ptr(target_logits), _dtype_code(target_logits), _ptr(draft_tokens), B, g, V,
                                _ptr(out["accept_count"]), _ptr(out["out_tokens"]), _ptr(out.get("row_status")),
                                _ptr(workspace), workspace.numel(), _stream(stream, dev))
@@ -220,13 +224,14 @@ def spv_fanout_topk(draft_logits, exclude, fanout, *, workspace=None, out=None, 
     Fmax = max(F) if F else 0
     if workspace is None:
         workspace = new_workspace(lib.spv_fanout_workspace_bytes(B, K1 - 1, V, Fmax), dev)
-    out = dict(out or {})
-    out.setdefault("ids", torch.empty(B, sum(F), dtype=torch.int32, device=dev))
-    if want_status:
-        out.setdefault("row_status", torch.empty(B, K1, dtype=torch.int32, device=dev))
+    out = dict(out) if out else {}
+    if "ids" not in out:
+        out["ids"] = torch.empty(B, sum(F), dtype=torch.int32, device=dev)
+    if want_status and "row_status" not in out:
+        out["row_status"] = torch.empty(B, K1, dtype=torch.int32, device=dev)
     f_host = (ctypes.c_int32 * max(K1, 1))(*F)
     st = lib.spv_fanout_topk(_ptr(draft_logits), _dtype_code(draft_logits), _ptr(exclude),
-                             ctypes.cast(f_host, ctypes.c_void_p), B, K1 - 1, V, _ptr(out["ids"]),
+                             ctypes.addressof(f_host), B, K1 - 1, V, _ptr(out["ids"]),
                              _ptr(out.get("row_status")), _ptr(workspace), workspace.numel(), _stream(stream, dev))
     _check(st, "spv_fanout_topk")
     return out

@@ -53,13 +53,81 @@ template <int DT> struct FanoutOp {
 
     static constexpr int CTAS_PER_SM = 2;
 
+    // Key of element e of the lane from the staged block (the same element
+    // lane_index(lane, e) as in the register copy); 0 = not a candidate.
+    __device__ static __forceinline__ uint32_t smem_key(const unsigned char *blk, int lane, int e, int valid, int base,
+                                                        int ex)
+    {
+        const int i = lane_index<DT>(lane, e);
+        float x;
+        if (DT == 0) x = reinterpret_cast<const float *>(blk)[i];
+        else x = __uint_as_float(static_cast<uint32_t>(reinterpret_cast<const unsigned short *>(blk)[i]) << 16);
+        return (i < valid && base + i != ex && x == x) ? float_key(x) : 0u;
+    }
+
+    // Top-F of a block staged in shared memory.  The F-th largest of the 32
+    // lane maxima bounds the block's F-th largest key from below (F distinct
+    // elements reach it), so only elements at or above it can be in the
+    // top F; the F rounds then visit only those (keys re-read from the
+    // staged block).  F > 32 visits every element.
     __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta,
                                                       const unsigned char *blk, int valid, int lane)
     {
+        const int k = static_cast<int>(row % P.K1);
+        const int F = P.F[k];
+        if (F == 0) return;
+        const int ex = P.exclude[row];
+        const int base = beta * G;
         float v[32];
         load_block_smem<DT>(v, blk, lane);
-        mask_tail<DT>(v, valid, lane);
-        block(P, row, beta, v, valid, lane);
+        uint32_t key[32];
+        bool nan = false;
+        uint32_t lmax = 0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int i = lane_index<DT>(lane, e);
+            const float x = v[e];
+            nan |= (x != x) && i < valid;
+            key[e] = (i < valid && base + i != ex && x == x) ? float_key(x) : 0u;
+            lmax = key[e] > lmax ? key[e] : lmax;
+        }
+        nan = __any_sync(0xffffffffu, nan);
+        uint64_t *out = P.cand + (static_cast<size_t>(row) * P.nb + beta) * P.Fmax;
+        if (nan) {
+            if (lane == 0) out[0] = ~0ull;
+            return;
+        }
+        uint32_t thr = 1u;  // keys of candidates are >= 1
+        if (F <= 32) {
+            // descending bitonic sort of the lane maxima across the warp
+            uint32_t sv = lmax;
+#pragma unroll
+            for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    const uint32_t o = __shfl_xor_sync(0xffffffffu, sv, j);
+                    const bool desc = (lane & kk) == 0, lower = (lane & j) == 0;
+                    sv = (lower == desc) ? (sv > o ? sv : o) : (sv < o ? sv : o);
+                }
+            }
+            const uint32_t t = __shfl_sync(0xffffffffu, sv, F - 1);
+            thr = t > 1u ? t : 1u;
+        }
+        uint32_t mask = 0;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) mask |= (key[e] >= thr ? 1u : 0u) << e;
+        uint64_t prev = ~0ull;
+        for (int t = 0; t < F; ++t) {
+            uint64_t best = 0;
+            for (uint32_t m = mask; m; m &= m - 1) {
+                const int e = __ffs(m) - 1;
+                const uint64_t K = cand_key(smem_key(blk, lane, e, valid, base, ex), base + lane_index<DT>(lane, e));
+                if (K < prev && K > best) best = K;
+            }
+            best = warp_max_u64(best);
+            if (lane == 0) out[t] = best;
+            prev = best;
+        }
     }
 
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int valid,

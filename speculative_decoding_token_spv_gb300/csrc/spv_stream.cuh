@@ -456,15 +456,17 @@ static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma
 {
     void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
     const int smem = tma ? stages<DT>(Op::CTAS_PER_SM) * CHUNK * DType<DT>::BYTES : 0;
-    // Per device and kernel: the shared-memory attribute and the resident
-    // CTA count are set / queried once (a kernel is a function of the
-    // template arguments, so a function-local static is per kernel).
+    // Per device and kernel variant: the shared-memory attributes and the
+    // resident CTA count are set / queried once (the function-local static
+    // is per template instantiation; the TMA / plain-load variant is chosen
+    // at run time, so it indexes the cache).
     constexpr int MAX_DEV = 64;
-    static int cap_cache[MAX_DEV];  // resident CTAs of the whole GPU, 0 = not yet known
+    static int cap_cache[2][MAX_DEV];  // [TMA variant][device]: resident CTAs of the GPU, 0 = not yet known
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    int cap = (dev >= 0 && dev < MAX_DEV) ? cap_cache[dev] : 0;
+    int *slot = (dev >= 0 && dev < MAX_DEV) ? &cap_cache[tma ? 1 : 0][dev] : nullptr;
+    int cap = slot ? *slot : 0;
     if (cap == 0) {
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
             return e;
@@ -476,7 +478,7 @@ static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma
         if ((e = cudaFuncSetAttribute(finalize_kernel<Fin, DT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                       Fin::FIN_BUF_FLOATS * 4)) != cudaSuccess)
             return e;
-        if (dev >= 0 && dev < MAX_DEV) cap_cache[dev] = cap;
+        if (slot) *slot = cap;
     }
     const int grid = static_cast<int>(P.total_items < cap ? P.total_items : cap);
     kern<<<grid, THREADS, smem, st>>>(P);

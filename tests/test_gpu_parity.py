@@ -118,6 +118,37 @@ def test_fanout_config(spv):
         assert not (ids[:, offs[k]:offs[k + 1]] == ex[:, k:k + 1]).any()
 
 
+@pytest.mark.parametrize("V", [7, 1000, 1025, 8193, 50000])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("levels", [None, 6])
+def test_fanout_ties_ragged_and_wide(spv, V, dtype, levels):
+    """Top-F over ragged vocabularies, F up to 64 (the unpruned path), heavy
+    ties from quantised logits (lowest id first, -0.0 equal to +0.0),
+    exclusions and a NaN row."""
+    gen = torch.Generator(device="cuda").manual_seed(V + (levels or 0))
+    B, K1 = 3, 6
+    d = torch.randn(B, K1, V, generator=gen, device="cuda") * 2.0
+    if levels:
+        d = torch.round(d * levels / 4)
+        d[d == 0] = -0.0
+    d = d.to(dtype)
+    F = [min(f, V - 1) for f in (8, 1, 0, 33, 64, 5)]
+    ex = torch.randint(-1, V, (B, K1), generator=gen, device="cuda", dtype=torch.int32)
+    got = spv.spv_fanout_topk(d, ex, F)
+    torch.cuda.synchronize()
+    ref = oracle.fanout_topk(_np(d), _np(ex), F)
+    assert np.array_equal(_np(got["ids"]), ref["ids"])
+    assert np.array_equal(_np(got["row_status"]), ref["status"])
+    d2 = d.clone()
+    d2[1, 3, V // 2] = float("nan")
+    got = spv.spv_fanout_topk(d2, ex, F)
+    torch.cuda.synchronize()
+    ref = oracle.fanout_topk(_np(d2), _np(ex), F)
+    assert np.array_equal(_np(got["ids"]), ref["ids"])
+    assert np.array_equal(_np(got["row_status"]), ref["status"])
+    assert ref["status"][1, 3] == 4
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("B", [1, 8, 64, 128, 256])
 @pytest.mark.parametrize("T", [1.0, 0.0])

@@ -220,6 +220,13 @@ template <int DT> struct ChainOp {
         return bi;
     }
 
+    // Max of the raw logits of block beta of target row rho.
+    __device__ static __forceinline__ float block_max(const Params &P, const Smem &sm, int b, int rho, int beta)
+    {
+        return sm.cached ? sm.st[rho * P.nb + beta].x
+                         : __ldcg(&P.stats[(static_cast<long long>(b) * P.R + rho) * P.nb + beta]).x;
+    }
+
     // Block beta of a row into a warp's buffer of G floats (-inf past V):
     // 16-byte vector loads when the rows are aligned, all in flight at once.
     __device__ static __forceinline__ void load_block(const Params &P, const unsigned char *rowp, int beta, float *buf,
@@ -255,34 +262,49 @@ template <int DT> struct ChainOp {
         __syncwarp();
     }
 
-    // Levels 2 and 3 of a draw from softmax(row / T) inside block beta whose
-    // logits are in buf: lane l owns sub-block l (ids base + 32 l + i) for the
-    // sub-block race, then id base + 32 s* + l for the id race.
-    __device__ static int race_in_block_p(const Params &P, const float *buf, int beta, uint64_t key, uint32_t s_sub,
-                                          uint32_t s_tok, uint32_t trial, uint32_t pos, int lane)
+    // One Philox call per lane: lane l computes draw group g0 + (l & 7) of
+    // `stream` (8 distinct groups, 32 draws), lane 8 instead computes group 0
+    // of `extra` when extra != 0.  spread_word fetches word j of lane src.
+    __device__ static __forceinline__ void philox_spread(uint32_t w[4], uint64_t key, uint32_t stream, uint32_t extra,
+                                                         uint32_t trial, uint32_t pos, uint32_t g0, int lane)
+    {
+        const bool ex = (lane == 8) && extra != 0u;
+        philox_group(w, key, ex ? extra : stream, trial, pos, ex ? 0u : g0 + static_cast<uint32_t>(lane & 7));
+    }
+    __device__ static __forceinline__ uint32_t spread_word(const uint32_t w[4], int src, int j)
+    {
+        const uint32_t a = __shfl_sync(0xffffffffu, w[0], src), b = __shfl_sync(0xffffffffu, w[1], src);
+        const uint32_t c = __shfl_sync(0xffffffffu, w[2], src), d = __shfl_sync(0xffffffffu, w[3], src);
+        return j == 0 ? a : (j == 1 ? b : (j == 2 ? c : d));
+    }
+
+    // Levels 2 and 3 of a draw from softmax(row / T) inside block beta (block
+    // max mb) whose logits are in buf: lane l owns sub-block l (ids
+    // base + 32 l + i) for the sub-block race, then id base + 32 s* + l for
+    // the id race.  If accept != 0 the acceptance word of the trial (group 0
+    // of stream `accept`) is returned in *accept_word.
+    __device__ static int race_in_block_p(const Params &P, const float *buf, int beta, float mb, uint64_t key,
+                                          uint32_t s_sub, uint32_t s_tok, uint32_t trial, uint32_t pos, int lane,
+                                          uint32_t accept = 0u, uint32_t *accept_word = nullptr)
     {
         const int base = beta * G;
-        // sub-block max and mass relative to it (skewed reads: no bank conflicts)
-        float ms = -INFINITY;
-#pragma unroll 8
-        for (int i = 0; i < SUB; ++i) ms = fmaxf(ms, buf[SUB * lane + ((i + lane) & (SUB - 1))]);
+        // sub-block mass relative to the block max (skewed reads: no bank conflicts)
         float ws = 0.f;
-        if (ms != -INFINITY) {
 #pragma unroll 8
-            for (int i = 0; i < SUB; ++i) ws += fast_exp2((buf[SUB * lane + ((i + lane) & (SUB - 1))] - ms) * P.c2);
-        }
-        const float mb = warp_max(ms);
-        const uint32_t n = static_cast<uint32_t>(base / SUB + lane);  // global sub-block index
+        for (int i = 0; i < SUB; ++i) ws += fast_exp2((buf[SUB * lane + ((i + lane) & (SUB - 1))] - mb) * P.c2);
         uint32_t w[4];
-        philox_group(w, key, s_sub, trial, pos, n >> 2);
-        float A = ws > 0.f ? arrival(expo(w[n & 3]), fast_exp2((mb - ms) * P.c2) / ws) : INFINITY;
+        philox_spread(w, key, s_sub, accept, trial, pos, static_cast<uint32_t>(base / (4 * SUB)), lane);
+        if (accept_word) *accept_word = __shfl_sync(0xffffffffu, w[0], 8);
+        const uint32_t us = spread_word(w, lane >> 2, lane & 3);  // sub-block n = base/32 + lane: word n & 3
+        float A = ws > 0.f ? arrival(expo(us), 1.f / ws) : INFINITY;
         int si = lane;
         warp_argmin(A, si);
-        const float msw = __shfl_sync(0xffffffffu, ms, si);
         const int x = base + SUB * si + lane;
         const float z = buf[SUB * si + lane];
-        philox_group(w, key, s_tok, trial, pos, static_cast<uint32_t>(x) >> 2);
-        float Ax = (x < P.V && z != -INFINITY) ? arrival(expo(w[x & 3]), fast_exp2((msw - z) * P.c2)) : INFINITY;
+        const float msw = warp_max(z);  // max of the winning sub-block
+        philox_spread(w, key, s_tok, 0u, trial, pos, static_cast<uint32_t>(base + SUB * si) >> 2, lane);
+        const uint32_t ut = spread_word(w, lane >> 2, lane & 3);  // id x: group x >> 2, word x & 3
+        float Ax = (x < P.V && z != -INFINITY) ? arrival(expo(ut), fast_exp2((msw - z) * P.c2)) : INFINITY;
         int xi = x;
         warp_argmin(Ax, xi);
         return xi;
@@ -356,6 +378,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
     using Base::load_block;
     using Base::race_in_block_p;
     using Base::race_resid;
+    using Base::block_max;
 
     // Residual masses w = max(0, p - q) of one row pair, per block, into
     // P.resid; returns Z = sum w in sm.Z.  All consumer warps.
@@ -414,7 +437,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
         // B. Row statistics from the block statistics: one half-warp per row,
-        //    all rows at once, all loads of a row in flight together.  Target
+        //    all rows at once, up to 16 loads per lane in flight together.  Target
         //    rows keep (m_beta, race factor) in shared memory for the draw.
         const int half = lane >> 4, hl = lane & 15;
         for (int rho0 = 0; rho0 < R; rho0 += 2 * FWV) {
@@ -424,16 +447,16 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             const bool keep = active && rho <= g && sm.cached;
             float m = -INFINITY, s = 0.f;
             bool bad = false;
-            for (int base = 0; base < nb; base += 16 * 8) {
-                float2 v[8];
+            for (int base = 0; base < nb; base += 16 * 16) {
+                float2 v[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 16; ++u) {
                     const int beta = base + 16 * u + hl;
                     v[u] = (active && beta < nb) ? __ldcg(&st[beta]) : make_float2(-INFINITY, 0.f);
                 }
                 float cm = -INFINITY;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < 16; ++u) {
                     const int beta = base + 16 * u + hl;
                     if (isnan(v[u].x)) bad = true;
                     else cm = fmaxf(cm, v[u].x);
@@ -443,7 +466,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 if (nm != -INFINITY) {
                     float acc = s > 0.f ? s * expf((m - nm) * P.invT) : 0.f;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u)
+                    for (int u = 0; u < 16; ++u)
                         if (v[u].y > 0.f) acc += v[u].y * expf((v[u].x - nm) * P.invT);
                     s = acc;
                     m = nm;
@@ -513,7 +536,8 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             if (warp == 0) {
                 const int beta = race_blocks_p(P, sm, b, k, Mt, key, 0u, static_cast<uint32_t>(g), lane);
                 load_block(P, tp, beta, tb, lane);
-                const int x = race_in_block_p(P, tb, beta, key, STREAM_SUB, STREAM_TOKEN, 0u, static_cast<uint32_t>(g), lane);
+                const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), key, STREAM_SUB, STREAM_TOKEN,
+                                              0u, static_cast<uint32_t>(g), lane);
                 if (lane == 0) sm.result = x;
             }
             fin_sync<FWV>();
@@ -526,11 +550,11 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 const int beta = race_blocks_p(P, sm, b, k, Mt, key, t, static_cast<uint32_t>(k), lane);
                 load_block(P, tp, beta, tb, lane);
                 load_block(P, dp, beta, db, lane);
-                const int x = race_in_block_p(P, tb, beta, key, STREAM_SUB, STREAM_TOKEN, t, static_cast<uint32_t>(k), lane);
+                uint32_t aw = 0;
+                const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), key, STREAM_SUB, STREAM_TOKEN, t,
+                                              static_cast<uint32_t>(k), lane, STREAM_ACCEPT, &aw);
                 if (lane == 0) {
-                    uint32_t w[4];
-                    philox_group(w, key, STREAM_ACCEPT, t, static_cast<uint32_t>(k), 0u);
-                    const float v = uniform24(w[0]);
+                    const float v = uniform24(aw);
                     const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
                     const float q = expf((db[x - beta * G] - Md) * P.invT) / Sd;
                     sm.trial_x[warp] = x;

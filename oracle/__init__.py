@@ -61,6 +61,8 @@ def _load():
         lib.spvo_fanout_row.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, P]
         lib.spvo_fanout_size.argtypes = [ctypes.c_int, ctypes.c_double, ctypes.c_double, ctypes.c_int]
         lib.spvo_fanout_size.restype = ctypes.c_double
+        lib.spvo_cache_slot.argtypes = [ctypes.c_int, ctypes.c_int32, P, P, ctypes.c_int]
+        lib.spvo_cache_slot.restype = ctypes.c_int
         lib.spvo_verify_chain_batch.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_double, P, P, P, P, P, P, P]
         lib.spvo_verify_greedy_batch.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -195,6 +197,24 @@ def fanout_topk(draft, exclude, fanout, threads: int | None = None) -> dict:
 
     _run(one, B * K1, threads)
     return dict(ids=ids, status=status)
+
+
+def cache_slots(accept_count, out_tokens, cache_ids, fanout) -> np.ndarray:
+    """Speculation-cache lookup of each sequence's verify outcome (k, t*):
+    the index of the entry (position k, token t*) in cache_ids[b] (k-major
+    lists of fanout[k] candidates), or -1.  accept_count [B], out_tokens
+    [B, gamma+1], cache_ids [B, sum F]; fanout: gamma+1 ints."""
+    k = np.asarray(accept_count, dtype=np.int64).reshape(-1)
+    toks = np.asarray(out_tokens, dtype=np.int64).reshape(k.shape[0], -1)
+    F = np.ascontiguousarray(np.asarray(fanout, dtype=np.int32))
+    ids = np.ascontiguousarray(np.asarray(cache_ids, dtype=np.int32).reshape(k.shape[0], int(F.sum())))
+    K = F.shape[0] - 1
+    lib = _load()
+    out = np.full(k.shape[0], -1, np.int32)
+    for b in range(k.shape[0]):
+        t = int(toks[b, k[b]]) if k[b] >= 0 else -1
+        out[b] = lib.spvo_cache_slot(int(k[b]), t, _ptr(ids[b]), _ptr(F), K)
+    return out
 
 
 def _run(fn, n, threads):

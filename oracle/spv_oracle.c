@@ -16,8 +16,9 @@
  *         distance" (Theorem 3.5).
  *   [SPD] "Speculative Pipeline Decoding: Higher-Accuracy Drafting with Hidden
  *         Latency via Pipeline Parallelism" -- the streaming-verification
- *         section (greedy: exact argmax match; sampling: standard rejection
- *         sampling) and "Evaluation" (temperature T).
+ *         section (at T = 0 a draft token stands only if it is the target's
+ *         most likely token; at T > 0 the usual rejection rule decides) and
+ *         "Evaluation" (temperature T).
  *   [SSD] "Speculative Speculative Decoding" (review of arXiv 2603.03251) --
  *         Figure 2 / "Core Technical Barrier" (geometric fan-out
  *         F_k = F_0 * a_p^(k/(1+r)), top-ranked draft tokens excluding the
@@ -215,8 +216,8 @@ static int race_sample(const double *w, int V, uint64_t key, uint32_t s_block, u
 }
 
 /* ------------------------------------------------------------------------ */
-/* Greedy verify (T = 0), [SPD] streaming verification: "under greedy
- * decoding we require an exact argmax match".  a_i = argmax z_i (lowest id on
+/* Greedy verify (T = 0), [SPD] streaming verification: a draft token stands
+ * only if it is the target's most likely token.  a_i = argmax z_i (lowest id on
  * ties), accept x_i iff x_i == a_i, stop at the first mismatch and emit a_k
  * there, or the bonus a_gamma when every draft matched. */
 static int argmax_row(const float *z, int V, int *a)
@@ -253,10 +254,12 @@ int spvo_verify_greedy_seq(const float *tgt, const int32_t *tok, int gamma, int 
 
 /* ------------------------------------------------------------------------ */
 /* Chain verify for one sequence, T > 0.  [SD] "The four-phase loop":
- *   step 3: for each draft token x_i draw r_i and accept if
- *           r_i <= min(1, p_i(x_i)/q_i(x_i)); stop at the first rejection.
- *   step 4: all accepted -> bonus token from p_{gamma+1}; rejected at j ->
- *           resample from norm(max(0, p_j - q_j)).
+ *   step 3: draft token x_i stands when its uniform r_i is at most the
+ *           ratio p_i(x_i)/q_i(x_i) capped at 1; the chain ends at the first
+ *           token that fails.
+ *   step 4: with every token standing, one more token is drawn from
+ *           p_{gamma+1}; after a failure at j the replacement is drawn from
+ *           norm(max(0, p_j - q_j)).
  * Inputs : tgt [(gamma+1) * V], drf [gamma * V] (row-major), tok [gamma],
  *          r [gamma], seq_key, T > 0.
  * Outputs: k, tokens [gamma+1] (k+1 ids then -1), pq [2*gamma] (p_i(x_i),
@@ -384,6 +387,25 @@ int spvo_fanout_row(const float *d, int V, int exclude, int F, int32_t *ids_out)
 double spvo_fanout_size(int F0, double a, double r, int k)
 {
     return (double)F0 * pow(a, (double)k / (1.0 + r));
+}
+
+/* ------------------------------------------------------------------------ */
+/* Speculation-cache lookup, [SSD] Algorithm 1 ("if verify_outcome in cache")
+ * and Figure 2: the cache holds one branch per (k, t) pair, for every
+ * position k = 0..K and each of the F_k fan-out candidates t listed for it,
+ * in k-major order.  The verify outcome (k accepted, emitted token t*) hits
+ * when one of the entries is the pair (k, t*); the result is that entry's
+ * index in the row of cache ids, else -1.  A bad row (k < 0) never hits. */
+int spvo_cache_slot(int k, int32_t t_star, const int32_t *cache_ids, const int32_t *fanout, int K)
+{
+    if (k < 0) return -1;
+    int slot = 0;
+    for (int pos = 0; pos <= K; ++pos) {
+        for (int j = 0; j < fanout[pos]; ++j, ++slot) {
+            if (pos == k && cache_ids[slot] == t_star) return slot;
+        }
+    }
+    return -1;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -47,6 +47,13 @@ MUTANTS = {
                          ["test_fanout_vs_numpy_lexsort"]),
     "greedy_last_tie": ("if (best < 0 || v > bv) { best = x; bv = v; }", "if (best < 0 || v >= bv) { best = x; bv = v; }",
                         ["test_greedy_matches_numpy_argmax"]),
+    "cache_wrong_position": ("if (pos == k && cache_ids[slot] == t_star) return slot;",
+                             "if (pos == k + 1 && cache_ids[slot] == t_star) return slot;",
+                             ["test_cache_full_fanout_always_hits", "test_cache_hit_rate_closed_form"]),
+    "cache_slot_within_position": ("if (pos == k && cache_ids[slot] == t_star) return slot;",
+                                   "if (pos == k && cache_ids[slot] == t_star) return j;",
+                                   ["test_cache_full_fanout_always_hits",
+                                    "test_cache_slot_first_entry_of_the_outcome_position"]),
     "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
                        ["test_fanout_sizes_golden"]),
 }

@@ -397,7 +397,7 @@ def test_race_keys_are_independent_and_deterministic():
 
 # ----------------------------------------------------------------- greedy
 def test_greedy_matches_numpy_argmax():
-    """T = 0: exact argmax match (first occurrence on ties, as numpy.argmax)."""
+    """T = 0: a draft token stands only if it is the target argmax (first occurrence on ties, as numpy.argmax)."""
     rng = np.random.default_rng(14)
     B, g, V = 50, 4, 777
     z = rng.integers(-4, 4, (B, g + 1, V)).astype(np.float32)  # many ties
@@ -471,3 +471,89 @@ def test_fanout_vs_numpy_lexsort(levels):
     d[1, 2, 9] = np.nan
     out = oracle.fanout_topk(d, ex, F)
     assert out["status"][1, 2] == 4 and (out["status"].sum() == 4)
+
+
+# ----------------------------------------------------------------- speculation cache
+def _cache_case(rng, B, g, V, z_std=1.5, noise=1.0):
+    """Distinct p_i / q_i per position, shared by all sequences (q also at the
+    bonus position g); draft tokens x_i ~ q_i drawn per sequence."""
+    zl = rng.normal(0, z_std, (g + 1, V)).astype(np.float32)
+    dl = (zl + rng.normal(0, noise, (g + 1, V))).astype(np.float32)
+    p = np.stack([_probs(zl[i]) for i in range(g + 1)])
+    q = np.stack([_probs(dl[i]) for i in range(g + 1)])
+    tok = np.stack([rng.choice(V, size=B, p=q[i]) for i in range(g)], axis=1).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    z = np.broadcast_to(zl, (B, g + 1, V)).astype(np.float32)
+    d = np.broadcast_to(dl[:g], (B, g, V)).astype(np.float32)
+    dfan = np.broadcast_to(dl, (B, g + 1, V)).astype(np.float32)
+    exclude = np.concatenate([tok, np.full((B, 1), -1, np.int32)], axis=1)
+    return z, d, dfan, tok, r, exclude, p, q
+
+
+def test_cache_full_fanout_always_hits():
+    """[SSD] Figure 2 cache with every candidate listed: F_k = V - 1 with the
+    verified token excluded (k < gamma), F_gamma = V.  A rejected token has
+    max(0, p - q) = 0 and is never re-emitted, so every outcome hits, at an
+    entry of its own position k holding the emitted token."""
+    rng = np.random.default_rng(21)
+    B, g, V = 3000, 3, 7
+    z, d, dfan, tok, r, exclude, p, q = _cache_case(rng, B, g, V, z_std=1.0, noise=1.2)
+    F = [V - 1] * g + [V]
+    lists = oracle.fanout_topk(dfan, exclude, F)["ids"]
+    out = _chain(z, d, tok, r, _keys(B, 31))
+    slot = oracle.cache_slots(out["accept_count"], out["out_tokens"], lists, F)
+    offs = np.concatenate([[0], np.cumsum(F)])
+    k = out["accept_count"]
+    t = out["out_tokens"][np.arange(B), k]
+    assert (slot >= 0).all()
+    assert (slot >= offs[k]).all() and (slot < offs[k + 1]).all()
+    assert (lists[np.arange(B), slot] == t).all()
+    assert len(np.unique(k)) == g + 1  # every position reached
+    # a bad row never hits
+    bad = out["accept_count"].copy()
+    bad[:5] = -1
+    assert (oracle.cache_slots(bad, out["out_tokens"], lists, F)[:5] == -1).all()
+
+
+def test_cache_hit_rate_closed_form():
+    """Hit rate of the fan-out cache against the closed form.  With the draft
+    tokens fixed, position i accepts with probability a_i = min(1, p_i/q_i)
+    at x_i ([SD] acceptance criterion), the first rejection at j emits from
+    norm(max(0, p_j - q_j)) and full acceptance emits from p_gamma, so
+      P(hit) = sum_j (prod_{i<j} a_i)(1 - a_j) R_j(C_j) + (prod_i a_i) p_gamma(C_gamma)
+    with C_k position k's candidates and R_j the residual distribution."""
+    rng = np.random.default_rng(22)
+    B, g, V = 30000, 3, 40
+    z, d, dfan, tok, r, exclude, p, q = _cache_case(rng, B, g, V)
+    F = [6, 4, 3, 3]
+    lists = oracle.fanout_topk(dfan, exclude, F)["ids"]
+    out = _chain(z, d, tok, r, _keys(B, 32))
+    slot = oracle.cache_slots(out["accept_count"], out["out_tokens"], lists, F)
+    offs = np.concatenate([[0], np.cumsum(F)])
+    resid = np.maximum(p[:g] - q[:g], 0.0)
+    resid /= resid.sum(axis=1, keepdims=True)
+    a = np.minimum(1.0, p[np.arange(g), tok] / q[np.arange(g), tok])  # [B, g]
+    h = np.zeros(B)
+    reach = np.ones(B)
+    for j in range(g):
+        c = lists[:, offs[j]:offs[j + 1]]
+        h += reach * (1 - a[:, j]) * resid[j][c].sum(axis=1)
+        reach = reach * a[:, j]
+    h += reach * p[g][lists[:, offs[g]:offs[g + 1]]].sum(axis=1)
+    hits = (slot >= 0).sum()
+    sigma = np.sqrt((h * (1 - h)).sum())
+    assert 0.05 < h.mean() < 0.95
+    assert abs(hits - h.sum()) < 5 * sigma, (hits, h.sum(), sigma)
+
+
+def test_cache_slot_first_entry_of_the_outcome_position():
+    """The slot is the first entry of position k equal to t*; the same token
+    listed under another position does not count."""
+    F = [3, 2, 0, 2]
+    ids = np.array([[4, 5, 6, 5, 9, 5, 5]], np.int32)
+    cases = [(0, 5, 1), (1, 5, 3), (1, 6, -1), (2, 5, -1), (3, 5, 5), (0, 9, -1), (1, 9, 4), (-1, 5, -1)]
+    for k, t, want in cases:
+        toks = np.full((1, 4), -1, np.int32)
+        if k >= 0:
+            toks[0, k] = t
+        assert oracle.cache_slots([k], toks, ids, F)[0] == want, (k, t)

@@ -431,6 +431,33 @@ def run_variants(spv, dev, stream, args):
     o = spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws)
     ms = time_graph(lambda: spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws, out=o))
     add("fanout B=8 K=4 fp32 F=[8,7,6,5,4]", ms, fanout_bytes(8, 5, fw.draft.shape[2], 4, sum(fw.fanout)), 8 * 5)
+    del fw, o, ws
+    # Verify fused with the speculation-cache lookup; the cache is the fan-out
+    # of the draft rows at positions 0..gamma.  The hit rate is a property of
+    # the synthetic workload (reported over 32 draws of the sampling keys).
+    for T in (1.0, 0.0):
+        w = workloads.sweep(B=64, device=dev, temperature=T, bonus_draft=True)
+        F = spv.fanout_sizes(8, 0.8, 0.5, w.gamma, w.V)
+        d, ex = workloads.cache_fanout_inputs(w)
+        lists = spv.spv_fanout_topk(d, ex, F)["ids"]
+        del d
+        ws = spv.new_workspace(spv.spv_chain_workspace_bytes(w.B, w.gamma, w.V), dev)
+        o = spv.spv_verify_chain_cached(w.target, w.draft, w.tokens, w.r, w.keys, T, lists, F, workspace=ws)
+        ms = time_graph(lambda: spv.spv_verify_chain_cached(w.target, w.draft, w.tokens, w.r, w.keys, T, lists, F,
+                                                            workspace=ws, out=o))
+        hits, n = 0, 0
+        gen = torch.Generator(device=dev).manual_seed(77)
+        for _ in range(32 if T > 0 else 1):
+            keys = torch.randint(-(2 ** 63), 2 ** 63 - 1, (w.B,), generator=gen, device=dev, dtype=torch.int64)
+            r = 1.0 - torch.rand(w.B, w.gamma, generator=gen, device=dev)
+            oo = spv.spv_verify_chain_cached(w.target, w.draft, w.tokens, r, keys, T, lists, F, workspace=ws)
+            hits += int((oo["cache_slot"] >= 0).sum())
+            n += w.B
+        add(f"cached verify sweep B=64 fp32 T={T:g} F={F}", ms,
+            chain_bytes(w.B, w.gamma, w.V, 4, T) + w.B * (sum(F) + 1) * 4, w.B * (w.gamma + 1))
+        res[-1]["cache_hit_rate"] = round(hits / n, 4)
+        res[-1]["cache_hit_sample"] = f"{n} verify outcomes"
+        del w, o, ws, lists
     torch.cuda.synchronize()
     return res
 

@@ -59,7 +59,7 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
  * For each sequence b and draft position i = 0..gamma-1:
  *   p_i = softmax(target[b,i,:] / T), q_i = softmax(draft[b,i,:] / T);
  *   x_i = draft_tokens[b,i] is accepted iff p_i(x_i) > 0 and
- *   r[b,i] * q_i(x_i) <= p_i(x_i)   ([SD] "accept if r_i <= min(1, p/q)").
+ *   r[b,i] * q_i(x_i) <= p_i(x_i)   ([SD] step 3's ratio test without a division).
  * k = number of leading accepted tokens (stop at the first rejection).
  * Emitted: x_0..x_{k-1}, then one more token:
  *   k <  gamma: a draw from norm(max(0, p_k - q_k))   (residual, [SD] step 4)
@@ -118,6 +118,38 @@ spv_status spv_verify_chain(const void *target_logits, const void *draft_logits,
 /* Workspace bytes spv_verify_chain needs (also valid for T == 0). */
 size_t spv_chain_workspace_bytes(int B, int gamma, int V);
 
+/*
+ * spv_verify_chain_cached -- spv_verify_chain followed, in the same kernels,
+ * by the speculation-cache lookup of [SSD] Algorithm 1 (the speculator's
+ * test whether the verify outcome is in its cache) with the cache of
+ * Figure 2: for each position k = 0..gamma, F_k candidate tokens.
+ *
+ * The outcome of sequence b is (k, t*): k = accept_count[b] and t* =
+ * out_tokens[b, k], the residual draw (k < gamma) or the bonus (k = gamma).
+ * The cache entries of sequence b are cache_ids[b, :], k-major: entries
+ * off_k .. off_k + F_k - 1 (off_k = F_0 + ... + F_{k-1}) are the candidates
+ * for position k -- exactly the layout spv_fanout_topk writes for the draft
+ * rows of positions 0..gamma with K = gamma.  The outcome hits when one of
+ * position k's entries equals t*; cache_slot[b] is then that entry's index
+ * in 0 .. sum_k F_k - 1 (the lowest one if the list repeats an id), else -1.
+ * A bad row never hits (cache_slot -1).
+ *
+ *   cache_ids   [B, sum_k F_k] int32 (device), any values (-1 never matches
+ *               an emitted token)
+ *   fanout      gamma + 1 ints, HOST array, 0 <= F_k <= SPV_MAX_FANOUT
+ *   cache_slot  [B] int32 out (device)
+ * All other arguments, the workspace and the T == 0 (greedy) semantics are
+ * those of spv_verify_chain.  A null cache_ids, fanout or cache_slot, or an
+ * F_k out of range, returns SPV_ERR_INVALID_ARG before any launch.
+ */
+spv_status spv_verify_chain_cached(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                                   const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
+                                   int B, int gamma, int V, float temperature,
+                                   int32_t *accept_count, int32_t *out_tokens, float *out_pq,
+                                   float *out_resid_norm, int32_t *row_status,
+                                   const int32_t *cache_ids, const int32_t *fanout, int32_t *cache_slot,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
 /* Bytes of device memory behind spv_verify_chain_noalloc (per GPU, held from
  * library load until process exit). */
 #define SPV_NOALLOC_SCRATCH_BYTES (4 * 1024 * 1024)
@@ -156,8 +188,8 @@ spv_status spv_verify_chain_noalloc(const void *target_logits, const void *draft
                                     float *out_resid_norm, int32_t *row_status, void *stream);
 
 /*
- * spv_verify_greedy -- T = 0 ([SPD] "under greedy decoding we require an
- * exact argmax match").  a_i = argmax_x target[b,i,x] (lowest id on ties,
+ * spv_verify_greedy -- T = 0 ([SPD] streaming verification: a draft token
+ * stands only if it is the target's most likely token).  a_i = argmax_x target[b,i,x] (lowest id on ties,
  * -0.0 equal to +0.0); x_i accepted iff x_i == a_i; stop at the first
  * mismatch k and emit a_k there (a_gamma when all matched).  Draft logits are
  * not needed.  Arguments as in spv_verify_chain; workspace of

@@ -48,6 +48,9 @@ def load_library():
     P, I, S = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
     lib.spv_verify_chain.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, P, P, P, P, S, P]
     lib.spv_verify_chain.restype = I
+    lib.spv_verify_chain_cached.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, P, P, P, P, P, P, P,
+                                            S, P]
+    lib.spv_verify_chain_cached.restype = I
     lib.spv_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, S, P]
     lib.spv_verify_greedy.restype = I
     lib.spv_fanout_topk.argtypes = [P, I, P, P, I, I, I, P, P, P, S, P]
@@ -140,6 +143,23 @@ def spv_verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, 
     dtype), draft_tokens [B, g] int32, r [B, g] float32, sample_keys [B] int64
     holding uint64 bit patterns.  Returns dict(accept_count, out_tokens, and
     pq / resid_norm / row_status when requested)."""
+    return _verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature, None, None,
+                         workspace, out, want_pq, want_resid_norm, want_status, stream)
+
+
+def spv_verify_chain_cached(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature: float,
+                            cache_ids, fanout, *, workspace=None, out=None, want_pq: bool = True,
+                            want_resid_norm: bool = False, want_status: bool = True, stream=None) -> dict:
+    """spv_verify_chain plus the speculation-cache lookup of the outcome
+    (see spv_verify_chain_cached in spv.h).  cache_ids [B, sum F] int32 (the
+    k-major candidate lists spv_fanout_topk writes), fanout: gamma+1 ints.
+    The result adds cache_slot [B] int32 (-1 = miss)."""
+    return _verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature, cache_ids,
+                         fanout, workspace, out, want_pq, want_resid_norm, want_status, stream)
+
+
+def _verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature, cache_ids, fanout,
+                  workspace, out, want_pq, want_resid_norm, want_status, stream) -> dict:
     target_logits = _cuda(target_logits, "target_logits")
     dev = target_logits.device
     if target_logits.dim() != 3:
@@ -159,6 +179,12 @@ def spv_verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, 
             raise ValueError("draft_logits [B,g,V], r [B,g], sample_keys [B] expected")
     else:
         draft_logits = r = sample_keys = None
+    cached = cache_ids is not None
+    if cached:
+        F = [int(f) for f in fanout]
+        cache_ids = _cuda(cache_ids, "cache_ids", torch.int32)
+        if len(F) != g + 1 or tuple(cache_ids.shape) != (B, sum(F)):
+            raise ValueError("fanout needs gamma+1 entries and cache_ids [B, sum(fanout)]")
     lib = load_library()
     need = lib.spv_chain_workspace_bytes(B, g, V)
     if workspace is None:
@@ -174,12 +200,20 @@ def spv_verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, 
         out["resid_norm"] = torch.empty(B, dtype=torch.float32, device=dev)
     if want_status and "row_status" not in out:
         out["row_status"] = torch.empty(B, dtype=torch.int32, device=dev)
-    st = lib.spv_verify_chain(_ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(r),
-                              _ptr(sample_keys), B, g, V, float(temperature), _ptr(out["accept_count"]),
-                              _ptr(out["out_tokens"]), _ptr(out.get("pq")), _ptr(out.get("resid_norm")),
-                              _ptr(out.get("row_status")), _ptr(workspace), workspace.numel(),
-                              _stream(stream, dev))
-    _check(st, "spv_verify_chain")
+    args = (_ptr(target_logits), _ptr(draft_logits), dt, _ptr(draft_tokens), _ptr(r), _ptr(sample_keys), B, g, V,
+            float(temperature), _ptr(out["accept_count"]), _ptr(out["out_tokens"]), _ptr(out.get("pq")),
+            _ptr(out.get("resid_norm")), _ptr(out.get("row_status")))
+    tail = (_ptr(workspace), workspace.numel(), _stream(stream, dev))
+    if cached:
+        if "cache_slot" not in out:
+            out["cache_slot"] = torch.empty(B, dtype=torch.int32, device=dev)
+        f_host = (ctypes.c_int32 * (g + 1))(*F)
+        st = lib.spv_verify_chain_cached(*args, _ptr(cache_ids), ctypes.addressof(f_host), _ptr(out["cache_slot"]),
+                                         *tail)
+        _check(st, "spv_verify_chain_cached")
+    else:
+        st = lib.spv_verify_chain(*args, *tail)
+        _check(st, "spv_verify_chain")
     return out
 
 

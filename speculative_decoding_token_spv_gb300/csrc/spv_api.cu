@@ -47,11 +47,16 @@ size_t spv_fanout_workspace_bytes(int B, int K, int V, int max_fanout)
     return spv::fanout_ws_bytes(B, K + 1, V, max_fanout);
 }
 
-spv_status spv_verify_chain(const void *target_logits, const void *draft_logits, spv_dtype dtype,
-                            const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys, int B,
-                            int gamma, int V, float temperature, int32_t *accept_count, int32_t *out_tokens,
-                            float *out_pq, float *out_resid_norm, int32_t *row_status, void *workspace,
-                            size_t workspace_bytes, void *stream)
+}  // extern "C"
+
+namespace {
+
+spv_status verify_chain_impl(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                             const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys, int B,
+                             int gamma, int V, float temperature, int32_t *accept_count, int32_t *out_tokens,
+                             float *out_pq, float *out_resid_norm, int32_t *row_status, const int32_t *cache_ids,
+                             const int32_t *fanout, int32_t *cache_slot, void *workspace, size_t workspace_bytes,
+                             void *stream)
 {
     if (!dtype_ok(dtype) || !target_logits || !draft_tokens || !accept_count || !out_tokens || !workspace)
         return SPV_ERR_INVALID_ARG;
@@ -63,6 +68,11 @@ spv_status spv_verify_chain(const void *target_logits, const void *draft_logits,
     if (workspace_bytes < need) return SPV_ERR_INVALID_ARG;
     if (!greedy && (!draft_logits || !r || !sample_keys)) return SPV_ERR_INVALID_ARG;
     if (!greedy && !(1.0f / temperature < INFINITY)) return SPV_ERR_INVALID_ARG;  // T too small to invert
+    if (cache_ids || fanout || cache_slot) {
+        if (!cache_ids || !fanout || !cache_slot) return SPV_ERR_INVALID_ARG;
+        for (int k = 0; k <= gamma; ++k)
+            if (fanout[k] < 0 || fanout[k] > SPV_MAX_FANOUT) return SPV_ERR_INVALID_ARG;
+    }
 
     spv::ChainLaunch L{};
     L.target = target_logits;
@@ -81,10 +91,41 @@ spv_status spv_verify_chain(const void *target_logits, const void *draft_logits,
     L.out_Z = out_resid_norm;
     L.row_status = row_status;
     L.ws = workspace;
+    L.cache_ids = cache_ids;
+    L.cache_fanout = fanout;
+    L.cache_slot = cache_slot;
     const bool rows16 = (static_cast<size_t>(V) * elem_bytes(dtype)) % 16 == 0;
     L.tma = rows16 && aligned16(target_logits) && (greedy || aligned16(draft_logits));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     return cuda_status(greedy ? spv::launch_greedy(L, st) : spv::launch_chain(L, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+spv_status spv_verify_chain(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                            const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys, int B,
+                            int gamma, int V, float temperature, int32_t *accept_count, int32_t *out_tokens,
+                            float *out_pq, float *out_resid_norm, int32_t *row_status, void *workspace,
+                            size_t workspace_bytes, void *stream)
+{
+    return verify_chain_impl(target_logits, draft_logits, dtype, draft_tokens, r, sample_keys, B, gamma, V,
+                             temperature, accept_count, out_tokens, out_pq, out_resid_norm, row_status, nullptr,
+                             nullptr, nullptr, workspace, workspace_bytes, stream);
+}
+
+spv_status spv_verify_chain_cached(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                                   const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
+                                   int B, int gamma, int V, float temperature, int32_t *accept_count,
+                                   int32_t *out_tokens, float *out_pq, float *out_resid_norm, int32_t *row_status,
+                                   const int32_t *cache_ids, const int32_t *fanout, int32_t *cache_slot,
+                                   void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!cache_ids || !fanout || !cache_slot) return SPV_ERR_INVALID_ARG;
+    return verify_chain_impl(target_logits, draft_logits, dtype, draft_tokens, r, sample_keys, B, gamma, V,
+                             temperature, accept_count, out_tokens, out_pq, out_resid_norm, row_status, cache_ids,
+                             fanout, cache_slot, workspace, workspace_bytes, stream);
 }
 
 spv_status spv_verify_greedy(const void *target_logits, spv_dtype dtype, const int32_t *draft_tokens, int B,

@@ -9,18 +9,27 @@
 //   r_i q_i(x_i) <= p_i(x_i) for every draft token, finds the first
 //   rejection with a warp ballot, and draws the emitted token: the bonus from
 //   p_gamma, or the residual norm(max(0, p_k - q_k)) by rejection trials from
-//   p_k (eight trials at a time, one per warp).  Draws use the two-level
-//   exponential race over the per-block statistics plus a re-read of one
-//   1024-logit block, so no row is read twice from HBM.
+//   p_k (one trial per warp per round).  Draws use the three-level
+//   exponential race (blocks from the per-block statistics, then sub-blocks
+//   and ids inside a re-read 1024-logit block), so no row is read twice in
+//   full from HBM.
 //
 // Greedy verify, "Speculative Pipeline Decoding", streaming verification
-// ("under greedy decoding we require an exact argmax match"): the same pass
-// over the target rows keeps per-block (max, lowest argmax id); the finalize
-// CTA of a sequence compares each draft token with its row argmax.
+// (T = 0: a draft token stands only if it is the target argmax): the same
+// pass over the target rows keeps per-block (max, lowest argmax id); the
+// finalize CTA of a sequence compares each draft token with its row argmax.
+//
+// Both finalizers can also key the outcome (k, emitted token) against the
+// sequence's speculation-cache entries ("Speculative Speculative Decoding",
+// Algorithm 1 and Figure 2) and write the hit slot.
 #include "spv_internal.h"
 #include "spv_stream.cuh"
 
 #include <climits>
+
+#include "spv.h"
+
+static_assert(spv::CACHE_POSITIONS >= SPV_MAX_GAMMA + 1, "cache offsets must cover gamma + 1 positions");
 
 namespace spv {
 
@@ -43,6 +52,7 @@ struct ChainParams {
     int32_t *row_status;
     float2 *stats;   // [B*R*nb] (block max of z, sum exp((z - max)/T)); NaN max = bad block
     float *resid;    // [B*nb] residual block masses (direct draw / normaliser only)
+    CacheLookup cache;
 };
 
 constexpr int FW = 16;            // widest chain finalize CTA (warps; one residual trial each per round)
@@ -433,6 +443,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 sm.zt[lane] = sm.zd[lane] = 0.f;
             }
         }
+        if (warp == 1) cache_prefetch(P.cache, b, lane);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
@@ -504,6 +515,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
                 if (P.out_Z) P.out_Z[b] = __int_as_float(0x7fffffff);
             }
+            if (warp == 0) cache_lookup(P.cache, b, -1, -1, lane);
             return;
         }
         // C. Accept tests for every draft position; first rejection by ballot.
@@ -596,6 +608,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             if (P.row_status) P.row_status[b] = 0;
             if (P.out_Z) P.out_Z[b] = (k == g) ? 1.0f : sm.Z;
         }
+        if (warp == FWV - 1) cache_lookup(P.cache, b, k, res, lane);
     }
 };
 
@@ -611,6 +624,7 @@ struct GreedyParams {
     int B, gamma, R;  // R = gamma + 1
     int32_t *accept_count, *out_tokens, *row_status;
     int2 *best;  // [B*R*nb] (max value bits, argmax id); id -2 marks a bad block
+    CacheLookup cache;
 };
 
 struct GreedySmem {
@@ -683,6 +697,7 @@ template <int DT> struct GreedyOp {
         const int g = P.gamma, R = P.R, nb = P.nb;
         if (threadIdx.x == 0) sm.bad = 0;
         if (warp == 0 && lane < g) sm.x[lane] = P.tokens[static_cast<size_t>(b) * g + lane];
+        if (warp == 1) cache_prefetch(P.cache, b, lane);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         consumer_sync();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
@@ -726,6 +741,7 @@ template <int DT> struct GreedyOp {
                     P.accept_count[b] = -1;
                     if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
                 }
+                cache_lookup(P.cache, b, -1, -1, lane);
             } else {
                 const bool acc = lane < g && sm.x[lane] == sm.a[lane];
                 const unsigned mask = __ballot_sync(0xffffffffu, acc);
@@ -741,6 +757,7 @@ template <int DT> struct GreedyOp {
                     P.accept_count[b] = k;
                     if (P.row_status) P.row_status[b] = 0;
                 }
+                cache_lookup(P.cache, b, k, sm.a[k], lane);
             }
         }
     }
@@ -763,6 +780,20 @@ size_t greedy_ws_bytes(int B, int gamma, int V)
 {
     const size_t nb = blocks_per_row(V), R = static_cast<size_t>(gamma) + 1;
     return WS_HEADER + align256(static_cast<size_t>(B) * R * nb * 8);
+}
+
+// Offsets of the fan-out positions in a sequence's candidate row.
+static void fill_cache(CacheLookup &C, const ChainLaunch &L)
+{
+    C.ids = L.cache_ids;
+    C.slot = L.cache_slot;
+    C.n = 0;
+    if (!L.cache_ids) return;
+    for (int k = 0; k <= L.gamma; ++k) {
+        C.off[k] = C.n;
+        C.n += L.cache_fanout[k];
+    }
+    C.off[L.gamma + 1] = C.n;
 }
 
 cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
@@ -794,6 +825,7 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
     P.out_pq = L.out_pq;
     P.out_Z = L.out_Z;
     P.row_status = L.row_status;
+    fill_cache(P.cache, L);
     // One finalize CTA per sequence: the 16-warp CTA (one per SM) while the
     // sequences fit on the SMs at once, else the 8-warp CTA (two per SM).
     int sms = 0;
@@ -825,6 +857,7 @@ cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st)
     P.accept_count = L.accept_count;
     P.out_tokens = L.out_tokens;
     P.row_status = L.row_status;
+    fill_cache(P.cache, L);
     return L.dtype == 0 ? launch_stream_finalize<GreedyOp<0>, GreedyOp<0>, 0>(P, L.tma, L.B, st)
                         : launch_stream_finalize<GreedyOp<1>, GreedyOp<1>, 1>(P, L.tma, L.B, st);
 }

@@ -28,6 +28,10 @@ struct ChainLaunch {
     int32_t *row_status;
     void *ws;
     bool tma;  // rows are 16-byte aligned and V * elem_bytes % 16 == 0
+    // Optional speculation-cache lookup (null cache_ids: none).
+    const int32_t *cache_ids;
+    const int32_t *cache_fanout;  // host, gamma + 1 entries
+    int32_t *cache_slot;
 };
 
 struct FanoutLaunch {

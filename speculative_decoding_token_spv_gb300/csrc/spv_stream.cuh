@@ -38,6 +38,50 @@ constexpr int SUB = 32;                       // sampler sub-block: ids per sub-
 constexpr uint32_t STREAM_BLOCK = 1, STREAM_SUB = 2, STREAM_TOKEN = 3, STREAM_ACCEPT = 4, STREAM_FB_BLOCK = 5,
                    STREAM_FB_SUB = 6, STREAM_FB_TOKEN = 7;
 
+// Speculation-cache lookup fused into the verify finalize ([SSD] Algorithm 1,
+// "if verify_outcome in cache"; Figure 2).  The cache of sequence b is its
+// fan-out candidate list: for each position k = 0..gamma, F_k candidate
+// tokens, k-major (the layout spv_fanout_topk writes).  The verify outcome
+// (k accepted, emitted token t) hits the entry of position k that holds t.
+constexpr int CACHE_POSITIONS = 33;  // gamma + 1 positions at most
+struct CacheLookup {
+    const int32_t *ids;              // [B, n] candidate ids, or null: no lookup
+    int32_t *slot;                   // [B] out: entry index in the row of ids, -1 = miss or bad row
+    int n;                           // sum_k F_k
+    int off[CACHE_POSITIONS + 1];    // off[k] = sum_{j<k} F_j
+};
+
+// Pull sequence b's candidate row towards L2 (inputs: safe before the
+// dependent-grid wait).  One warp.
+__device__ __forceinline__ void cache_prefetch(const CacheLookup &C, int b, int lane)
+{
+    if (!C.ids) return;
+    const char *base = reinterpret_cast<const char *>(C.ids + static_cast<size_t>(b) * C.n);
+    for (int o = lane * 128; o < C.n * 4; o += 32 * 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(base + o));
+}
+
+// Slot of the outcome (k, t) of sequence b (k < 0: bad row, no hit).  One
+// warp; candidate lists hold distinct ids, the lowest matching entry wins
+// otherwise.
+__device__ __forceinline__ void cache_lookup(const CacheLookup &C, int b, int k, int t, int lane)
+{
+    if (!C.ids) return;
+    int slot = -1;
+    if (k >= 0) {
+        const int o0 = C.off[k], n = C.off[k + 1] - o0;
+        const int32_t *row = C.ids + static_cast<size_t>(b) * C.n + o0;
+        for (int j0 = 0; j0 < n; j0 += 32) {
+            const int j = j0 + lane;
+            const unsigned m = __ballot_sync(0xffffffffu, j < n && __ldg(row + j) == t);
+            if (m) {
+                slot = o0 + j0 + __ffs(m) - 1;
+                break;
+            }
+        }
+    }
+    if (lane == 0) C.slot[b] = slot;
+}
+
 template <int DT> struct DType;
 template <> struct DType<0> {  // fp32
     using T = float;

@@ -16,6 +16,8 @@ Workloads (stand-ins for the pages' evaluation sets, which are not used):
           softmax(d[b,k]) for k < 4, -1 at k = 4; F = round(8 * 0.8^(k/1.5))
   sweep   the spd distributions at gamma=4, V=151936, fp32 / bf16,
           B in {1, 8, 64, 128, 256}
+Any chain workload can also draw the draft row of the bonus position
+(``bonus_draft``), which the speculation-cache fan-out ranks.
 All draws are fp32 from seeded ``torch.Generator`` s on the requested device,
 then cast to the workload dtype; V is the last, contiguous axis.
 """
@@ -28,6 +30,7 @@ import torch
 SEEDS = dict(tiny=(100, 101, 0, 1), spd=(200, 201, 0, 1), eagle=(300, 301, 2, 3), sweep=(200, 201, 0, 1))
 PEAK_SEED = 202
 FANOUT_SEEDS = (400, 4)
+BONUS_SEED_OFFSET = 7919  # seed of the bonus-position draft row = draft seed + this
 
 
 @dataclass
@@ -40,6 +43,7 @@ class ChainInputs:
     keys: torch.Tensor            # [B] int64 holding uint64 bit patterns
     temperature: float
     meta: dict = field(default_factory=dict)
+    draft_bonus: torch.Tensor | None = None  # [B, 1, V] draft logits at position gamma (fan-out input)
 
     @property
     def B(self):
@@ -87,9 +91,11 @@ def _uniforms_and_keys(B, g, seed, device):
 
 
 def chain_from_params(name, B, gamma, V, dtype, temperature, z_std, d_scale, d_std, peaks, seeds,
-                      device="cpu") -> ChainInputs:
+                      device="cpu", bonus_draft=False) -> ChainInputs:
     """Generic generator: z ~ N(0, z_std^2) [B, gamma+1, V] (+8 on `peaks` ids
-    per target row), d = d_scale * z[:, :gamma] + N(0, d_std^2)."""
+    per target row), d = d_scale * z[:, :gamma] + N(0, d_std^2).  With
+    `bonus_draft` also the draft row of position gamma, d_scale * z[:, gamma]
+    + N(0, d_std^2), from its own seed (the other draws are unchanged)."""
     s_z, s_d, s_tok, s_u = seeds
     z = torch.randn(B, gamma + 1, V, generator=_gen(device, s_z), device=device) * z_std
     if peaks:
@@ -99,6 +105,12 @@ def chain_from_params(name, B, gamma, V, dtype, temperature, z_std, d_scale, d_s
         del score, idx
     d = torch.randn(B, gamma, V, generator=_gen(device, s_d), device=device) * d_std
     d.add_(z[:, :gamma], alpha=d_scale)
+    draft_bonus = None
+    if bonus_draft:
+        db = torch.randn(B, 1, V, generator=_gen(device, s_d + BONUS_SEED_OFFSET), device=device) * d_std
+        db.add_(z[:, gamma:], alpha=d_scale)
+        draft_bonus = db.to(dtype)
+        del db
     target = z.to(dtype)
     del z
     draft = d.to(dtype)
@@ -107,27 +119,40 @@ def chain_from_params(name, B, gamma, V, dtype, temperature, z_std, d_scale, d_s
     r, keys = _uniforms_and_keys(B, gamma, s_u, device)
     return ChainInputs(name, target, draft, tokens, r, keys, float(temperature),
                        dict(B=B, gamma=gamma, V=V, dtype=str(dtype).replace("torch.", ""),
-                            T=float(temperature)))
+                            T=float(temperature)), draft_bonus)
 
 
-def tiny(device="cpu", temperature=1.0) -> ChainInputs:
+def tiny(device="cpu", temperature=1.0, bonus_draft=False) -> ChainInputs:
     return chain_from_params("tiny", 1, 4, 1000, torch.float32, temperature, 2.0, 1.0, 0.5, 0,
-                             SEEDS["tiny"], device)
+                             SEEDS["tiny"], device, bonus_draft)
 
 
-def spd(device="cpu", temperature=1.0, B=64) -> ChainInputs:
+def spd(device="cpu", temperature=1.0, B=64, bonus_draft=False) -> ChainInputs:
     return chain_from_params("spd", B, 1, 151936, torch.bfloat16, temperature, 3.0, 1.0, 1.0, 20,
-                             SEEDS["spd"], device)
+                             SEEDS["spd"], device, bonus_draft)
 
 
-def eagle(gamma=7, device="cpu", temperature=1.0, B=32) -> ChainInputs:
+def eagle(gamma=7, device="cpu", temperature=1.0, B=32, bonus_draft=False) -> ChainInputs:
     return chain_from_params(f"eagle_g{gamma}", B, gamma, 128256, torch.bfloat16, temperature, 2.5, 0.8,
-                             1.5, 0, SEEDS["eagle"], device)
+                             1.5, 0, SEEDS["eagle"], device, bonus_draft)
 
 
-def sweep(B=64, dtype=torch.float32, device="cpu", temperature=1.0, V=151936, gamma=4) -> ChainInputs:
+def sweep(B=64, dtype=torch.float32, device="cpu", temperature=1.0, V=151936, gamma=4,
+          bonus_draft=False) -> ChainInputs:
     return chain_from_params(f"sweep_B{B}_{str(dtype).replace('torch.', '')}", B, gamma, V, dtype,
-                             temperature, 3.0, 1.0, 1.0, 20, SEEDS["sweep"], device)
+                             temperature, 3.0, 1.0, 1.0, 20, SEEDS["sweep"], device, bonus_draft)
+
+
+def cache_fanout_inputs(w: ChainInputs):
+    """Fan-out inputs of the speculation cache for a chain workload drawn with
+    `bonus_draft`: draft rows of positions 0..gamma [B, gamma+1, V] and the
+    token to skip at each, the verified draft token (k < gamma) or none (-1,
+    position gamma)."""
+    if w.draft_bonus is None:
+        raise ValueError("workload drawn without bonus_draft")
+    d = torch.cat([w.draft, w.draft_bonus], dim=1)
+    ex = torch.cat([w.tokens, torch.full((w.B, 1), -1, dtype=torch.int32, device=w.tokens.device)], dim=1)
+    return d, ex
 
 
 def fanout(device="cpu", B=8, K=4, V=128256, fanout_sizes=(8, 7, 6, 5, 4)) -> FanoutInputs:

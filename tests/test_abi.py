@@ -95,3 +95,34 @@ def test_invalid_arguments_rejected_on_host(lib):
     assert fan(fake, 0, fake, ctypes.cast(f_big, P), 2, 1, 10, fake, None, ws, big, None) == INV   # F > V-1
     assert fan(fake, 0, fake, ctypes.cast(f_big, P), 2, 64, 1000, fake, None, ws, big, None) == INV
     assert fan(fake, 0, fake, ctypes.cast(f_big, P), 2, 1, 2_000_000, fake, None, ws, big, None) == 3
+
+
+def test_cached_verify_arguments_rejected_on_host(lib):
+    """spv_verify_chain_cached: the cache arguments are all required, F_k in
+    [0, SPV_MAX_FANOUT]; the usual chain checks still apply."""
+    P = ctypes.c_void_p
+    fake = P(4096)
+    ws = P(1 << 20)
+    big = 1 << 40
+    INV = 1
+    f_ok = (ctypes.c_int32 * 5)(8, 7, 6, 5, 4)
+    f_neg = (ctypes.c_int32 * 5)(8, 7, -1, 5, 4)
+    f_big = (ctypes.c_int32 * 5)(8, 7, 65, 5, 4)
+    ok_args = dict(t=fake, d=fake, dt=0, tok=fake, r=fake, keys=fake, B=4, g=4, V=1000, T=1.0, k=fake,
+                   out=fake, pq=None, z=None, st=None, ids=fake, fan=ctypes.cast(f_ok, P), slot=fake, ws=ws,
+                   wsb=big, stream=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.spv_verify_chain_cached(a["t"], a["d"], a["dt"], a["tok"], a["r"], a["keys"], a["B"], a["g"],
+                                           a["V"], ctypes.c_float(a["T"]), a["k"], a["out"], a["pq"], a["z"],
+                                           a["st"], a["ids"], a["fan"], a["slot"], a["ws"], a["wsb"], a["stream"])
+
+    assert call(ids=None) == INV
+    assert call(fan=None) == INV
+    assert call(slot=None) == INV
+    assert call(fan=ctypes.cast(f_neg, P)) == INV
+    assert call(fan=ctypes.cast(f_big, P)) == INV
+    assert call(g=0) == INV
+    assert call(t=None) == INV
+    assert call(T=0.0, wsb=16) == INV

@@ -49,7 +49,8 @@ def _oracle_chain(w, want_Z=False):
 
 def _to(w, dev):
     return workloads.ChainInputs(w.name, w.target.to(dev), w.draft.to(dev), w.tokens.to(dev), w.r.to(dev),
-                                 w.keys.to(dev), w.temperature, w.meta)
+                                 w.keys.to(dev), w.temperature, w.meta,
+                                 None if w.draft_bonus is None else w.draft_bonus.to(dev))
 
 
 def check_chain(spv, w, want_Z=False, expect_bad=None, z_atol=0.0):

@@ -65,6 +65,11 @@ def _load():
         lib.spvo_cache_slot.restype = ctypes.c_int
         lib.spvo_verify_chain_batch.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                 ctypes.c_int, ctypes.c_double, P, P, P, P, P, P, P]
+        lib.spvo_filter_row.argtypes = [P, ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_double, P, P, P]
+        lib.spvo_filter_row.restype = ctypes.c_int
+        lib.spvo_verify_filtered_batch.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                   ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_double,
+                                                   P, P, P, P, P, P]
         lib.spvo_verify_greedy_batch.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  P, P, P]
         _lib = lib
@@ -136,6 +141,60 @@ def verify_chain(target, draft, tokens, r, keys, temperature: float, want_Z: boo
                                     float(temperature), _ptr(out["accept_count"]), _ptr(out["out_tokens"]),
                                     _ptr(out["pq"]), _ptr(Z) if want_Z else None, _ptr(out["margin"]),
                                     _ptr(out["trials"]), _ptr(out["status"]))
+
+    _run_ranges(run, B, threads)
+    if want_Z:
+        out["Z"] = Z
+    return out
+
+
+MAX_TOP_K = 64
+STREAM_FILTERED = 8
+
+
+def filter_row(z, temperature: float, top_k: int, top_p: float = 1.0):
+    """Top-k / top-p filter of one row: (ids, probs) of the kept ids in rank
+    order (logit descending, ties to the lower id), probs renormalised; None
+    for a bad row.  Also returns the top-p cut margin."""
+    z = _f32(z).reshape(-1)
+    if not 1 <= top_k <= MAX_TOP_K:
+        raise ValueError("top_k out of range")
+    K = min(top_k, z.size)
+    ids = np.zeros(K, np.int32)
+    probs = np.zeros(K)
+    margin = np.full(1, np.inf)
+    n = _load().spvo_filter_row(_ptr(z), z.size, float(temperature), int(top_k), float(top_p), _ptr(ids),
+                                _ptr(probs), _ptr(margin))
+    if n < 0:
+        return None
+    return ids[:n].copy(), probs[:n].copy(), float(margin[0])
+
+
+def verify_filtered(target, draft, tokens, r, keys, temperature: float, top_k: int, top_p: float = 1.0,
+                    want_Z: bool = False, threads: int | None = None) -> dict:
+    """Chain verify on top-k / top-p filtered target and draft distributions
+    (T > 0; T == 0 routes to :func:`verify_greedy`, which no top-k filter
+    changes).  Arguments and outputs as :func:`verify_chain` (no trials)."""
+    if temperature == 0:
+        return verify_greedy(target, tokens, threads=threads)
+    if not 1 <= top_k <= MAX_TOP_K or not 0.0 < top_p <= 1.0:
+        raise ValueError("top_k in [1, 64] and top_p in (0, 1] expected")
+    target, draft = _f32(target), _f32(draft)
+    B, g1, V = target.shape
+    g = g1 - 1
+    tokens = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32)).reshape(B, g)
+    r = _f32(r).reshape(B, g)
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.uint64)).reshape(B)
+    out = dict(accept_count=np.zeros(B, np.int32), out_tokens=np.zeros((B, g + 1), np.int32),
+               pq=np.zeros((B, g, 2)), margin=np.zeros(B), status=np.zeros(B, np.int32))
+    Z = np.zeros(B) if want_Z else None
+    lib = _load()
+
+    def run(b0, b1):
+        lib.spvo_verify_filtered_batch(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(r), _ptr(keys), b0, b1, g, V,
+                                       float(temperature), int(top_k), float(top_p), _ptr(out["accept_count"]),
+                                       _ptr(out["out_tokens"]), _ptr(out["pq"]), _ptr(Z) if want_Z else None,
+                                       _ptr(out["margin"]), _ptr(out["status"]))
 
     _run_ranges(run, B, threads)
     if want_Z:

@@ -67,6 +67,7 @@
 #define SPVO_STREAM_FB_BLOCK 5u
 #define SPVO_STREAM_FB_SUB 6u
 #define SPVO_STREAM_FB_TOKEN 7u
+#define SPVO_STREAM_FILTERED 8u
 
 #define SPVO_OK 0
 #define SPVO_BAD_ROW 4
@@ -334,14 +335,21 @@ int spvo_verify_chain_seq(const float *tgt, const float *drf, const int32_t *tok
             double d = w[x] - prob(dj, x, T, Md[k], Sd[k]);
             w[x] = d > 0 ? d : 0.0;
         }
-        if (emitted < 0)
+        ksum Z = { 0, 0 };
+        for (int x = 0; x < V; ++x) ksum_add(&Z, w[x]);
+        if (emitted < 0) {
+            /* No positive residual mass: impossible when x_k was drawn from
+             * q_k (then sum (p-q)+ = sum (q-p)+ >= q(x_k) - p(x_k) > 0), but a
+             * caller may pass a token outside q's support; the row is bad. */
+            if (!(ksum_val(&Z) > 0)) {
+                free(w);
+                for (int i = 0; i < 2 * gamma; ++i) pq_out[i] = NAN;
+                return SPVO_BAD_ROW;
+            }
             emitted = race_sample(w, V, seq_key, SPVO_STREAM_FB_BLOCK, SPVO_STREAM_FB_SUB, SPVO_STREAM_FB_TOKEN, 0,
                                   (uint32_t)k, &margin);
-        if (Z_out) {
-            ksum Z = { 0, 0 };
-            for (int x = 0; x < V; ++x) ksum_add(&Z, w[x]);
-            *Z_out = ksum_val(&Z);
         }
+        if (Z_out) *Z_out = ksum_val(&Z);
     }
     free(w);
     for (int i = 0; i < k; ++i) tokens_out[i] = tok[i];
@@ -390,6 +398,167 @@ double spvo_fanout_size(int F0, double a, double r, int k)
 }
 
 /* ------------------------------------------------------------------------ */
+/* Top-k / top-p filtered rows, [SPD] "Evaluation": the sampled runs (T = 1)
+ * draw from the target and draft distributions restricted by top-k = 50 and
+ * top-p = 1.0.  The filter of one row at temperature T > 0:
+ *   1. rank the ids by logit (descending, -0.0 equal to +0.0, ties to the
+ *      lower id) and keep the first top_k;
+ *   2. give them the probabilities renormalised over the kept ids,
+ *      P(x) = exp(y_x - y_max) / sum_kept exp(y_j - y_max), y = z / T;
+ *   3. if top_p < 1, keep only the shortest prefix (in rank order) whose
+ *      probability sum reaches top_p, and renormalise over that prefix.
+ * Every other id has probability 0.  Writes the kept ids and probabilities
+ * in rank order and returns their count, or -1 for a bad row (NaN or +inf
+ * anywhere, or no finite logit among the kept ids).  The top-p cut is the
+ * only floating-point decision; its margin min(top_p - C_{n-1}, C_n - top_p)
+ * (C_j = probability sum of the first j kept ids) is recorded. */
+int spvo_filter_row(const float *z, int V, double T, int top_k, double top_p, int32_t *ids_out,
+                    double *probs_out, double *margin)
+{
+    vid *all = (vid *)malloc(sizeof(vid) * (size_t)V);
+    for (int x = 0; x < V; ++x) {
+        double v = (double)z[x];
+        if (isnan(v) || (isinf(v) && v > 0)) { free(all); return -1; }
+        all[x].v = v + 0.0;
+        all[x].id = x;
+    }
+    qsort(all, (size_t)V, sizeof(vid), cmp_vid);
+    int n = top_k < V ? top_k : V;
+    if (isinf(all[0].v)) { free(all); return -1; } /* no finite logit at all */
+    double ymax = all[0].v / T;
+    ksum S = { 0, 0 };
+    for (int j = 0; j < n; ++j) {
+        ids_out[j] = all[j].id;
+        probs_out[j] = exp(all[j].v / T - ymax);
+        ksum_add(&S, probs_out[j]);
+    }
+    free(all);
+    double s = ksum_val(&S);
+    for (int j = 0; j < n; ++j) probs_out[j] /= s;
+    if (top_p < 1.0) {
+        ksum C = { 0, 0 };
+        int cut = n;
+        for (int j = 0; j < n; ++j) {
+            double before = ksum_val(&C);
+            ksum_add(&C, probs_out[j]);
+            double after = ksum_val(&C);
+            if (after >= top_p) {
+                note_margin(margin, top_p - before);
+                note_margin(margin, after - top_p);
+                cut = j + 1;
+                break;
+            }
+        }
+        n = cut;
+        ksum S2 = { 0, 0 };
+        for (int j = 0; j < n; ++j) ksum_add(&S2, probs_out[j]);
+        double s2 = ksum_val(&S2);
+        for (int j = 0; j < n; ++j) probs_out[j] /= s2;
+    }
+    return n;
+}
+
+/* Probability of id x under a filtered row (0 when x is not kept). */
+static double filtered_prob(const int32_t *ids, const double *probs, int n, int x)
+{
+    for (int j = 0; j < n; ++j)
+        if (ids[j] == x) return probs[j];
+    return 0.0;
+}
+
+/* Chain verify of one sequence on the filtered distributions p'_i, q'_i of
+ * spvo_filter_row (the same top_k, top_p for target and draft): [SD] steps
+ * 3 and 4 unchanged -- accept x_i iff p'_i(x_i) > 0 and r_i q'_i(x_i) <=
+ * p'_i(x_i), stop at the first rejection, then one draw from
+ * norm(max(0, p'_k - q'_k)) (rejection at k) or from p'_gamma (bonus).  The
+ * draw is an exponential race over the kept target ids: the id x with the
+ * smallest E_x / w(x) wins (E_x = -ln U for draw n = x of stream
+ * SPVO_STREAM_FILTERED, trial 0, position k; ties to the lower id), which is
+ * exactly distributed as w / sum w.  Outputs as spvo_verify_chain_seq (pq
+ * holds p'_i(x_i), q'_i(x_i)); the margin also covers the top-p cuts of the
+ * rows read. */
+int spvo_verify_filtered_seq(const float *tgt, const float *drf, const int32_t *tok, const float *r,
+                             uint64_t seq_key, int gamma, int V, double T, int top_k, double top_p,
+                             int32_t *k_out, int32_t *tokens_out, double *pq_out, double *Z_out,
+                             double *margin_out)
+{
+    for (int i = 0; i <= gamma; ++i) tokens_out[i] = -1;
+    for (int i = 0; i < 2 * gamma; ++i) pq_out[i] = NAN;
+    *k_out = -1;
+    *margin_out = INFINITY;
+    if (Z_out) *Z_out = NAN;
+    for (int i = 0; i < gamma; ++i)
+        if (tok[i] < 0 || tok[i] >= V) return SPVO_BAD_ROW;
+    int K = top_k < V ? top_k : V;
+    int32_t *ids = (int32_t *)malloc(sizeof(int32_t) * (size_t)K * (size_t)(2 * gamma + 1));
+    double *pr = (double *)malloc(sizeof(double) * (size_t)K * (size_t)(2 * gamma + 1));
+    int n[129];
+    double margin = INFINITY;
+    int bad = 0;
+    /* rows 0..gamma: target; gamma+1..2gamma: draft */
+    for (int row = 0; row <= 2 * gamma && !bad; ++row) {
+        const float *z = row <= gamma ? tgt + (size_t)row * V : drf + (size_t)(row - gamma - 1) * V;
+        n[row] = spvo_filter_row(z, V, T, top_k, top_p, ids + (size_t)row * K, pr + (size_t)row * K, &margin);
+        if (n[row] < 0) bad = 1;
+    }
+    if (bad) { free(ids); free(pr); return SPVO_BAD_ROW; }
+
+    int k = gamma;
+    for (int i = 0; i < gamma; ++i) {
+        double p = filtered_prob(ids + (size_t)i * K, pr + (size_t)i * K, n[i], tok[i]);
+        double q = filtered_prob(ids + (size_t)(gamma + 1 + i) * K, pr + (size_t)(gamma + 1 + i) * K,
+                                 n[gamma + 1 + i], tok[i]);
+        pq_out[2 * i] = p;
+        pq_out[2 * i + 1] = q;
+        int acc = (p > 0) && ((double)r[i] * q <= p);
+        if (i < k) {
+            note_margin(&margin, (q > 0) ? fabs((double)r[i] - p / q) : INFINITY);
+            if (!acc) k = i;
+        }
+    }
+    /* draw over the kept target ids of row k, taken in ascending id order */
+    const int32_t *ti = ids + (size_t)k * K;
+    const double *tp = pr + (size_t)k * K;
+    int m = n[k];
+    int order[64 + 1];
+    double w[64 + 1], arr[64 + 1];
+    for (int j = 0; j < m; ++j) order[j] = j;
+    for (int a = 1; a < m; ++a)          /* insertion sort by id */
+        for (int b2 = a; b2 > 0 && ti[order[b2 - 1]] > ti[order[b2]]; --b2) {
+            int t = order[b2]; order[b2] = order[b2 - 1]; order[b2 - 1] = t;
+        }
+    ksum Z = { 0, 0 };
+    for (int j = 0; j < m; ++j) {
+        int x = ti[order[j]];
+        double wx = tp[order[j]];
+        if (k < gamma) {
+            double qx = filtered_prob(ids + (size_t)(gamma + 1 + k) * K, pr + (size_t)(gamma + 1 + k) * K,
+                                      n[gamma + 1 + k], x);
+            wx = wx - qx > 0 ? wx - qx : 0.0;
+        }
+        w[j] = wx;
+        ksum_add(&Z, wx);
+        arr[j] = wx > 0 ? expo(seq_key, SPVO_STREAM_FILTERED, 0, (uint32_t)k, (uint64_t)x) / wx : INFINITY;
+    }
+    if (!(ksum_val(&Z) > 0)) { /* no positive residual mass (token outside q's support): bad row */
+        free(ids);
+        free(pr);
+        for (int i = 0; i < 2 * gamma; ++i) pq_out[i] = NAN;
+        return SPVO_BAD_ROW;
+    }
+    int jw = race_winner(arr, m, &margin);
+    int emitted = ti[order[jw]];
+    if (Z_out) *Z_out = (k == gamma) ? 1.0 : ksum_val(&Z);
+    free(ids);
+    free(pr);
+    for (int i = 0; i < k; ++i) tokens_out[i] = tok[i];
+    tokens_out[k] = emitted;
+    *k_out = k;
+    *margin_out = margin;
+    return SPVO_OK;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Speculation-cache lookup, [SSD] Algorithm 1 ("if verify_outcome in cache")
  * and Figure 2: the cache holds one branch per (k, t) pair, for every
  * position k = 0..K and each of the F_k fan-out candidates t listed for it,
@@ -422,6 +591,20 @@ void spvo_verify_chain_batch(const float *tgt, const float *drf, const int32_t *
             tok + (size_t)b * gamma, r + (size_t)b * gamma, keys[b], gamma, V, T, &k_out[b],
             tokens_out + (size_t)b * (gamma + 1), pq_out + (size_t)b * 2 * gamma, Z_out ? &Z_out[b] : 0,
             &margin_out[b], &trials_out[b]);
+    }
+}
+
+void spvo_verify_filtered_batch(const float *tgt, const float *drf, const int32_t *tok, const float *r,
+                                const uint64_t *keys, int b0, int b1, int gamma, int V, double T, int top_k,
+                                double top_p, int32_t *k_out, int32_t *tokens_out, double *pq_out, double *Z_out,
+                                double *margin_out, int32_t *status_out)
+{
+    for (int b = b0; b < b1; ++b) {
+        status_out[b] = spvo_verify_filtered_seq(
+            tgt + (size_t)b * (size_t)(gamma + 1) * (size_t)V, drf + (size_t)b * (size_t)gamma * (size_t)V,
+            tok + (size_t)b * gamma, r + (size_t)b * gamma, keys[b], gamma, V, T, top_k, top_p, &k_out[b],
+            tokens_out + (size_t)b * (gamma + 1), pq_out + (size_t)b * 2 * gamma, Z_out ? &Z_out[b] : 0,
+            &margin_out[b]);
     }
 }
 

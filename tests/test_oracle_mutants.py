@@ -54,6 +54,15 @@ MUTANTS = {
                                    "if (pos == k && cache_ids[slot] == t_star) return j;",
                                    ["test_cache_full_fanout_always_hits",
                                     "test_cache_slot_first_entry_of_the_outcome_position"]),
+    "filter_not_renormalised": ("    for (int j = 0; j < n; ++j) probs_out[j] /= s;\n",
+                                "\n",
+                                ["test_filter_row_vs_torch_topk_softmax"]),
+    "top_p_cut_one_late": ("if (after >= top_p) {", "if (before >= top_p) {", ["test_filter_top_p_closed_form"]),
+    "filtered_residual_sign": ("wx = wx - qx > 0 ? wx - qx : 0.0;", "wx = qx - wx > 0 ? qx - wx : 0.0;",
+                               ["test_filtered_residual_on_forced_rejection"]),
+    "filtered_race_weight": ("expo(seq_key, SPVO_STREAM_FILTERED, 0, (uint32_t)k, (uint64_t)x) / wx",
+                             "expo(seq_key, SPVO_STREAM_FILTERED, 0, (uint32_t)k, (uint64_t)x) * wx",
+                             ["test_filtered_first_token_and_bonus_are_exact"]),
     "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
                        ["test_fanout_sizes_golden"]),
 }
@@ -65,6 +74,8 @@ def _calls(name):
         return [lambda: fn(1.0), lambda: fn(0.6)]
     if name == "test_fanout_vs_numpy_lexsort":
         return [lambda: fn(None), lambda: fn(8)]
+    if name == "test_filter_row_vs_torch_topk_softmax":
+        return [lambda: fn(1.0)]
     return [fn]
 
 

@@ -557,3 +557,198 @@ def test_cache_slot_first_entry_of_the_outcome_position():
         if k >= 0:
             toks[0, k] = t
         assert oracle.cache_slots([k], toks, ids, F)[0] == want, (k, t)
+
+
+# ----------------------------------------------------------------- top-k / top-p filtered verify
+def _torch_filtered_probs(z, T, top_k):
+    """p' from library routines: torch.topk then torch.softmax over the kept
+    logits (rows without ties), scattered back to a length-V vector."""
+    zt = torch.from_numpy(np.asarray(z, np.float64))
+    v, i = torch.topk(zt, top_k)
+    p = torch.zeros_like(zt)
+    p[i] = torch.softmax(v / T, dim=0)
+    return p.numpy()
+
+
+@pytest.mark.parametrize("T", [1.0, 0.7])
+def test_filter_row_vs_torch_topk_softmax(T):
+    rng = np.random.default_rng(30)
+    for V, k in [(1000, 50), (300, 1), (64, 64), (5000, 7)]:
+        z = rng.normal(0, 2, V).astype(np.float32)
+        ids, probs, margin = oracle.filter_row(z, T, k)
+        ref = _torch_filtered_probs(z, T, k)
+        order = np.argsort(-z.astype(np.float64), kind="stable")[:k]
+        assert list(ids) == list(order)
+        np.testing.assert_allclose(probs, ref[ids], rtol=1e-12, atol=0)
+        assert abs(probs.sum() - 1) < 1e-12 and margin == np.inf
+
+
+def test_filter_top_p_closed_form():
+    """Nucleus cut on p = (0.5, 0.3, 0.15, 0.05): the shortest prefix whose
+    mass reaches top_p, renormalised; applied after the top-k cut."""
+    z = np.log(np.array([0.5, 0.3, 0.15, 0.05]))[[2, 0, 3, 1]].astype(np.float32)  # ids 1, 3, 0, 2 by rank
+    cases = [(4, 0.4, [1], [1.0]),
+             (4, 0.75, [1, 3], [0.625, 0.375]),
+             (4, 0.9, [1, 3, 0], [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95]),
+             (4, 1.0, [1, 3, 0, 2], [0.5, 0.3, 0.15, 0.05]),
+             (3, 0.9, [1, 3, 0], [0.5 / 0.95, 0.3 / 0.95, 0.15 / 0.95]),  # top-3 mass (0.526, 0.842, 1.0)
+             (2, 0.6, [1], [1.0]),                                          # top-2 mass (0.625, 1.0)
+             (2, 0.7, [1, 3], [0.625, 0.375])]
+    for k, top_p, want_ids, want_p in cases:
+        ids, probs, _ = oracle.filter_row(z, 1.0, k, top_p)
+        assert list(ids) == want_ids, (k, top_p)
+        np.testing.assert_allclose(probs, want_p, rtol=1e-6)
+
+
+def test_filter_ties_and_bad_rows():
+    z = np.array([1.0, 3.0, 3.0, -0.0, 0.0, 3.0], np.float32)
+    ids, probs, _ = oracle.filter_row(z, 1.0, 2)
+    assert list(ids) == [1, 2]   # ties to the lower id
+    ids, probs, _ = oracle.filter_row(z, 1.0, 6)
+    assert list(ids) == [1, 2, 5, 0, 3, 4]   # -0.0 ranks equal to +0.0
+    for bad in (np.nan, np.inf):
+        zz = z.copy()
+        zz[4] = bad
+        assert oracle.filter_row(zz, 1.0, 2) is None
+    assert oracle.filter_row(np.full(10, -np.inf, np.float32), 1.0, 3) is None
+    ids, probs, _ = oracle.filter_row(np.array([-np.inf, 0.5, -np.inf], np.float32), 1.0, 3)
+    assert list(ids) == [1, 0, 2] and list(probs) == [1.0, 0.0, 0.0]
+
+
+def _filtered_case(rng, B, g, V, top_k, z_std=1.5, noise=1.0, T=1.0):
+    zl = rng.normal(0, z_std, (g + 1, V)).astype(np.float32)
+    dl = (zl[:g] + rng.normal(0, noise, (g, V))).astype(np.float32)
+    p = np.stack([_torch_filtered_probs(zl[i], T, top_k) for i in range(g + 1)])
+    q = np.stack([_torch_filtered_probs(dl[i], T, top_k) for i in range(g)])
+    tok = np.stack([rng.choice(V, size=B, p=q[i]) for i in range(g)], axis=1).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    z = np.broadcast_to(zl, (B, g + 1, V)).astype(np.float32)
+    d = np.broadcast_to(dl, (B, g, V)).astype(np.float32)
+    return z, d, tok, r, p, q
+
+
+def test_filtered_top1_is_greedy():
+    """top_k = 1 makes p' and q' point masses on the argmaxes: a draft token
+    stands iff it is the target argmax, and the emitted token at the first
+    mismatch (or the bonus) is the target argmax -- the T = 0 rule."""
+    rng = np.random.default_rng(31)
+    B, g, V = 400, 3, 50
+    z = rng.integers(-3, 4, (B, g + 1, V)).astype(np.float32)   # ties: the lowest id is the argmax
+    a = np.argmax(z, axis=2)
+    d = rng.integers(-3, 4, (B, g, V)).astype(np.float32)
+    agree = rng.random((B, g)) < 0.7
+    bb, ii = np.nonzero(agree)
+    d[bb, ii, a[bb, ii]] = 9.0                                    # the draft argmax is the target's
+    tok = np.argmax(d, axis=2).astype(np.int32)                   # drawn from q' = point mass
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    out = oracle.verify_filtered(z, d, tok, r, _keys(B, 41), 1.0, 1)
+    for b in range(B):
+        k = 0
+        while k < g and tok[b, k] == a[b, k]:
+            k += 1
+        assert out["accept_count"][b] == k
+        assert list(out["out_tokens"][b, :k]) == list(tok[b, :k]) and out["out_tokens"][b, k] == a[b, k]
+
+
+@pytest.mark.parametrize("top_k", [10, 40])
+def test_filtered_acceptance_rate_is_one_minus_tvd(top_k):
+    """Theorem 3.5 on the filtered distributions: P(accept) = sum min(p', q')."""
+    rng = np.random.default_rng(32)
+    B, V = 30000, 200
+    z, d, tok, r, p, q = _filtered_case(rng, B, 1, V, top_k)
+    out = oracle.verify_filtered(z, d, tok, r, _keys(B, 42), 1.0, top_k)
+    np.testing.assert_allclose(out["pq"][:, 0, 0], p[0][tok[:, 0]], rtol=1e-12, atol=1e-300)
+    np.testing.assert_allclose(out["pq"][:, 0, 1], q[0][tok[:, 0]], rtol=1e-12, atol=1e-300)
+    alpha = np.minimum(p[0], q[0]).sum()
+    emp = (out["accept_count"] == 1).mean()
+    assert abs(emp - alpha) < 5 * np.sqrt(alpha * (1 - alpha) / B), (emp, alpha)
+
+
+def test_filtered_first_token_and_bonus_are_exact():
+    """Exactness on the filtered distributions: the first emitted token ~ p'_1
+    and the bonus ~ p'_2 (chi-square)."""
+    rng = np.random.default_rng(33)
+    B, V, k = 30000, 300, 12
+    z, d, tok, r, p, q = _filtered_case(rng, B, 1, V, k, noise=0.7)
+    out = oracle.verify_filtered(z, d, tok, r, _keys(B, 43), 1.0, k)
+    first = out["out_tokens"][:, 0]
+    ok, pv = _chi2_ok(np.bincount(first, minlength=V), p[0])
+    assert ok, pv
+    full = out["accept_count"] == 1
+    ok, pv = _chi2_ok(np.bincount(out["out_tokens"][full, 1], minlength=V), p[1])
+    assert ok and full.sum() > 5000, pv
+
+
+def test_filtered_residual_on_forced_rejection():
+    """A rejected position emits from norm(max(0, p' - q')); Z = TVD(p', q')."""
+    rng = np.random.default_rng(34)
+    B, V, k = 20000, 400, 16
+    z, d, tok, r, p, q = _filtered_case(rng, B, 1, V, k, noise=1.5)
+    x_rej = int(np.argmax(q[0] - p[0]))
+    tok[:] = x_rej
+    r[:] = 1.0
+    out = oracle.verify_filtered(z, d, tok, r, _keys(B, 44), 1.0, k, want_Z=True)
+    assert (out["accept_count"] == 0).all()
+    w = np.maximum(p[0] - q[0], 0)
+    np.testing.assert_allclose(out["Z"], 0.5 * np.abs(p[0] - q[0]).sum(), rtol=1e-10)
+    ok, pv = _chi2_ok(np.bincount(out["out_tokens"][:, 0], minlength=V), w / w.sum())
+    assert ok and (out["out_tokens"][:, 0] != x_rej).all(), pv
+
+
+def test_filtered_nucleus_first_token():
+    """With top_p < 1 the first emitted token follows the nucleus-restricted,
+    renormalised target distribution (chi-square)."""
+    rng = np.random.default_rng(35)
+    B, V, k, top_p = 30000, 200, 30, 0.8
+    z, d, tok, r, _, _ = _filtered_case(rng, B, 1, V, k)
+    ids, probs, _ = oracle.filter_row(z[0, 0], 1.0, k, top_p)
+    # independent nucleus: sort the torch top-k probabilities, cut where the cumulative sum reaches top_p
+    pk = _torch_filtered_probs(z[0, 0], 1.0, k)
+    srt = np.argsort(-pk, kind="stable")
+    n = int(np.searchsorted(np.cumsum(pk[srt]), top_p) + 1)
+    nucleus = np.zeros(V)
+    nucleus[srt[:n]] = pk[srt[:n]] / pk[srt[:n]].sum()
+    assert sorted(ids) == sorted(srt[:n])
+    q_ids, q_probs, _ = oracle.filter_row(d[0, 0], 1.0, k, top_p)
+    qv = np.zeros(V)
+    qv[q_ids] = q_probs
+    tok = rng.choice(V, size=(B, 1), p=qv).astype(np.int32)
+    out = oracle.verify_filtered(z, d, tok, r, _keys(B, 45), 1.0, k, top_p)
+    ok, pv = _chi2_ok(np.bincount(out["out_tokens"][:, 0], minlength=V), nucleus)
+    assert ok, pv
+
+
+def test_filtered_without_cut_is_the_softmax():
+    """top_k >= V and top_p = 1: p', q' are the plain temperature softmax."""
+    rng = np.random.default_rng(36)
+    B, g, V = 50, 2, 60
+    z = rng.normal(0, 2, (B, g + 1, V)).astype(np.float32)
+    d = rng.normal(0, 2, (B, g, V)).astype(np.float32)
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    out = oracle.verify_filtered(z, d, tok, r, _keys(B, 46), 0.8, 64)
+    bb = np.arange(B)[:, None]
+    gg = np.arange(g)[None, :]
+    np.testing.assert_allclose(out["pq"][..., 0], softmax(z[:, :g].astype(np.float64) / 0.8, axis=2)[bb, gg, tok],
+                               rtol=1e-12)
+    np.testing.assert_allclose(out["pq"][..., 1], softmax(d.astype(np.float64) / 0.8, axis=2)[bb, gg, tok],
+                               rtol=1e-12)
+
+
+def test_zero_residual_mass_is_a_bad_row():
+    """A draft token outside q's support (q(x) = 0) with p(x) = 0 is rejected,
+    and when p = q everywhere else the residual max(0, p - q) has no mass:
+    nothing can be drawn, so the sequence is a bad row (chain and filtered)."""
+    V = 40
+    rng = np.random.default_rng(37)
+    zl = rng.normal(0, 1, V).astype(np.float32)
+    zl[7] = -np.inf
+    z = np.stack([zl, zl])[None]
+    d = zl[None, None].copy()
+    out = oracle.verify_chain(z, d, np.array([[7]], np.int32), np.ones((1, 1), np.float32), _keys(1), 1.0)
+    assert out["status"][0] == 4 and out["accept_count"][0] == -1 and (out["out_tokens"] == -1).all()
+    out = oracle.verify_filtered(z, d, np.array([[7]], np.int32), np.ones((1, 1), np.float32), _keys(1), 1.0, 64)
+    assert out["status"][0] == 4 and out["accept_count"][0] == -1
+    # the same row with a token inside the support is fine
+    out = oracle.verify_chain(z, d, np.array([[3]], np.int32), np.ones((1, 1), np.float32), _keys(1), 1.0)
+    assert out["status"][0] == 0 and out["accept_count"][0] == 1

@@ -81,6 +81,16 @@ template <int FWV> __device__ __forceinline__ void fin_sync()
     asm volatile("bar.sync 1, %0;" ::"n"(FWV * 32) : "memory");
 }
 
+// Residual mass max(0, p(x) - q(x)) from the logits of x: p and q are each
+// rounded to fp32 before the difference (no fused multiply-add across them),
+// so identical target and draft logits give exactly 0.
+__device__ __forceinline__ float resid_mass(float zt, float zd, float Mt, float it, float Md, float id, float invT)
+{
+    const float p = __fmul_rn(expf((zt - Mt) * invT), it);
+    const float q = __fmul_rn(expf((zd - Md) * invT), id);
+    return fmaxf(__fsub_rn(p, q), 0.f);
+}
+
 template <int DT> struct ChainOp {
     using Params = ChainParams;
     using Smem = ChainSmem;
@@ -350,6 +360,7 @@ template <int DT> struct ChainOp {
             }
         }
         warp_argmin(best, bi);
+        if (bi == INT_MAX) return -1;  // no block with positive residual mass
         load_block(P, tp, bi, tb, lane);
         load_block(P, dp, bi, db, lane);
         const float it = 1.f / St, id = 1.f / Sd;
@@ -357,7 +368,7 @@ template <int DT> struct ChainOp {
         float ws = 0.f;
         for (int i = 0; i < SUB; ++i) {
             const int o = SUB * lane + ((i + lane) & (SUB - 1));
-            ws += fmaxf(expf((tb[o] - Mt) * P.invT) * it - expf((db[o] - Md) * P.invT) * id, 0.f);
+            ws += resid_mass(tb[o], db[o], Mt, it, Md, id, P.invT);
         }
         const uint32_t n = static_cast<uint32_t>(base / SUB + lane);
         uint32_t w[4];
@@ -367,7 +378,7 @@ template <int DT> struct ChainOp {
         warp_argmin(A, si);
         const int x = base + SUB * si + lane;
         const int o = SUB * si + lane;
-        const float wx = x < P.V ? fmaxf(expf((tb[o] - Mt) * P.invT) * it - expf((db[o] - Md) * P.invT) * id, 0.f) : 0.f;
+        const float wx = x < P.V ? resid_mass(tb[o], db[o], Mt, it, Md, id, P.invT) : 0.f;
         philox_group(w, key, STREAM_FB_TOKEN, 0, pos, static_cast<uint32_t>(x) >> 2);
         float Ax = wx > 0.f ? arrival(expo(w[x & 3]), 1.f / wx) : INFINITY;
         int xi = x;
@@ -399,11 +410,8 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         for (int beta = warp; beta < P.nb; beta += FWV) {
             float part = 0.f;
             const int hi = min(P.V, (beta + 1) * G);
-            for (int x = beta * G + lane; x < hi; x += 32) {
-                const float p = expf((DType<DT>::load(tp, x) - Mt) * P.invT) * it;
-                const float q = expf((DType<DT>::load(dp, x) - Md) * P.invT) * id;
-                part += fmaxf(p - q, 0.f);
-            }
+            for (int x = beta * G + lane; x < hi; x += 32)
+                part += resid_mass(DType<DT>::load(tp, x), DType<DT>::load(dp, x), Mt, it, Md, id, P.invT);
             part = warp_sum(part);
             if (lane == 0) P.resid[static_cast<size_t>(b) * P.nb + beta] = part;
         }
@@ -419,6 +427,23 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
 
     static constexpr int FIN_WARPS = FWV;
     static constexpr int FIN_BUF_FLOATS = 2 * FWV * G;  // per warp: one target and one draft block
+
+    // Outputs of a bad row: -1 ids and count, NaN p / q / Z, status, cache miss.
+    __device__ static void write_bad_row(const Params &P, int b, int warp, int lane)
+    {
+        constexpr int NT = FWV * 32;
+        const int g = P.gamma;
+        for (int i = threadIdx.x; i <= g; i += NT) P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
+        if (P.out_pq)
+            for (int i = threadIdx.x; i < 2 * g; i += NT)
+                P.out_pq[static_cast<size_t>(b) * 2 * g + i] = __int_as_float(0x7fffffff);
+        if (threadIdx.x == 0) {
+            P.accept_count[b] = -1;
+            if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
+            if (P.out_Z) P.out_Z[b] = __int_as_float(0x7fffffff);
+        }
+        if (warp == 0) cache_lookup(P.cache, b, -1, -1, lane);
+    }
 
     __device__ static void finalize(const Params &P, int b, Smem &sm, float *buf, int warp, int lane)
     {
@@ -506,16 +531,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         }
         fin_sync<FWV>();
         if (sm.bad) {
-            for (int i = threadIdx.x; i <= g; i += NT) P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
-            if (P.out_pq)
-                for (int i = threadIdx.x; i < 2 * g; i += NT)
-                    P.out_pq[static_cast<size_t>(b) * 2 * g + i] = __int_as_float(0x7fffffff);
-            if (threadIdx.x == 0) {
-                P.accept_count[b] = -1;
-                if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
-                if (P.out_Z) P.out_Z[b] = __int_as_float(0x7fffffff);
-            }
-            if (warp == 0) cache_lookup(P.cache, b, -1, -1, lane);
+            write_bad_row(P, b, warp, lane);
             return;
         }
         // C. Accept tests for every draft position; first rejection by ballot.
@@ -595,8 +611,13 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 }
             }
         }
-        // E. Outputs.
+        // E. Outputs.  No residual mass at all (a draft token outside q's
+        //    support with p = q elsewhere) leaves nothing to draw: bad row.
         const int res = sm.result;
+        if (res < 0) {
+            write_bad_row(P, b, warp, lane);
+            return;
+        }
         for (int i = threadIdx.x; i <= g; i += NT) {
             int v = -1;
             if (i < k) v = sm.x[i];

@@ -261,3 +261,24 @@ def test_invalid_arguments_raise(spv):
         spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, -1.0)
     with pytest.raises(spv.SpvError):
         spv.spv_fanout_topk(w.draft, torch.zeros(2, 2, dtype=torch.int32, device="cuda"), [1, 100])
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_zero_residual_mass_is_a_bad_row(spv, dtype):
+    """A draft token with p = q = 0 is rejected and, with p = q elsewhere, the
+    residual has no mass: every trial fails, the direct draw finds no block
+    with mass, and the sequence is reported as a bad row (as by the oracle)."""
+    gen = torch.Generator(device="cpu").manual_seed(11)
+    V = 5000
+    zl = torch.randn(V, generator=gen)
+    zl[7] = float("-inf")
+    B, g = 3, 2
+    tgt = zl.repeat(B, g + 1, 1).to(dtype)
+    drf = zl.repeat(B, g, 1).to(dtype)
+    tok = torch.tensor([[7, 3], [3, 7], [3, 4]], dtype=torch.int32)
+    r = torch.full((B, g), 0.5)   # p = q: accepted with margin 0.5
+    keys = torch.tensor([5, 6, 7], dtype=torch.int64)
+    w = workloads.ChainInputs("zero_resid", tgt, drf, tok, r, keys, 1.0, {})
+    w = _to(w, "cuda")
+    got, ref = check_chain(spv, w, want_Z=True, expect_bad=[0, 1])
+    assert list(_np(got["accept_count"])) == [-1, -1, 2]

@@ -432,6 +432,23 @@ def run_variants(spv, dev, stream, args):
     ms = time_graph(lambda: spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws, out=o))
     add("fanout B=8 K=4 fp32 F=[8,7,6,5,4]", ms, fanout_bytes(8, 5, fw.draft.shape[2], 4, sum(fw.fanout)), 8 * 5)
     del fw, o, ws
+    # Verify on top-k / top-p filtered distributions (the SPD sampling setup:
+    # top-k 50, top-p 1.0 at T = 1); same logit bytes as the unfiltered call.
+    fcases = [("filtered spd B=64 g=1 bf16 T=1 top-k 50", lambda: workloads.spd(device=dev, top_k=50), 50, 1.0),
+              ("filtered sweep B=64 fp32 T=1 top-k 50", lambda: workloads.sweep(B=64, device=dev, top_k=50), 50, 1.0),
+              ("filtered sweep B=64 bf16 T=1 top-k 50",
+               lambda: workloads.sweep(B=64, dtype=torch.bfloat16, device=dev, top_k=50), 50, 1.0),
+              ("filtered sweep B=256 fp32 T=1 top-k 50", lambda: workloads.sweep(B=256, device=dev, top_k=50), 50, 1.0),
+              ("filtered eagle B=32 g=15 bf16 T=1 top-k 50 top-p 0.9",
+               lambda: workloads.eagle(gamma=15, device=dev, top_k=50, top_p=0.9), 50, 0.9)]
+    for name, mk, fk, fp in fcases:
+        w = mk()
+        ws = spv.new_workspace(spv.spv_filtered_workspace_bytes(w.B, w.gamma, w.V), dev)
+        o = spv.spv_verify_chain_filtered(w.target, w.draft, w.tokens, w.r, w.keys, 1.0, fk, fp, workspace=ws)
+        ms = time_graph(lambda: spv.spv_verify_chain_filtered(w.target, w.draft, w.tokens, w.r, w.keys, 1.0, fk, fp,
+                                                              workspace=ws, out=o))
+        add(name, ms, chain_bytes(w.B, w.gamma, w.V, w.target.element_size(), 1.0), w.B * (w.gamma + 1))
+        del w, o, ws
     # Verify fused with the speculation-cache lookup; the cache is the fan-out
     # of the draft rows at positions 0..gamma.  The hit rate is a property of
     # the synthetic workload (reported over 32 draws of the sampling keys).
@@ -545,15 +562,22 @@ def profile_case(args):
         for _ in range(args.iters):
             spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws)
     else:
+        fk = dict(top_k=args.top_k, top_p=args.top_p) if args.top_k else {}
         if name == "sweep":
-            w = workloads.sweep(B=B, dtype=dt, device=dev, temperature=T)
+            w = workloads.sweep(B=B, dtype=dt, device=dev, temperature=T, **fk)
         elif name == "spd":
-            w = workloads.spd(device=dev, temperature=T)
+            w = workloads.spd(device=dev, temperature=T, **fk)
         else:
-            w = workloads.eagle(gamma=int(name[5:] or 7), device=dev, temperature=T)
-        ws = spv.new_workspace(spv.spv_chain_workspace_bytes(w.B, w.gamma, w.V), dev)
-        for _ in range(args.iters):
-            spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature, workspace=ws)
+            w = workloads.eagle(gamma=int(name[5:] or 7), device=dev, temperature=T, **fk)
+        if args.top_k:
+            ws = spv.new_workspace(spv.spv_filtered_workspace_bytes(w.B, w.gamma, w.V), dev)
+            for _ in range(args.iters):
+                spv.spv_verify_chain_filtered(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature, args.top_k,
+                                              args.top_p, workspace=ws)
+        else:
+            ws = spv.new_workspace(spv.spv_chain_workspace_bytes(w.B, w.gamma, w.V), dev)
+            for _ in range(args.iters):
+                spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature, workspace=ws)
     torch.cuda.synchronize()
     print("profile case done:", name, args.dtype, B, T, args.iters)
 
@@ -570,6 +594,8 @@ def main(argv=None):
     ap.add_argument("--dtype", default="float32")
     ap.add_argument("--B", type=int, default=64)
     ap.add_argument("--T", type=float, default=1.0)
+    ap.add_argument("--top-k", type=int, default=0, help="profile case: filtered verify with this top_k")
+    ap.add_argument("--top-p", type=float, default=1.0)
     ap.add_argument("--iters", type=int, default=4)
     args = ap.parse_args(argv)
     if args.profile_case:

@@ -52,6 +52,7 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
 #define SPV_SAMPLER_BLOCK 1024 /* ids per sampler block (part of the sampling rule) */
 #define SPV_SAMPLER_SUB 32     /* ids per sampler sub-block (part of the sampling rule) */
 #define SPV_MAX_TRIALS 64    /* residual rejection trials before the direct draw */
+#define SPV_MAX_TOP_K 64     /* top_k of spv_verify_chain_filtered */
 
 /*
  * spv_verify_chain -- [SD] steps 3 and 4 for B independent sequences.
@@ -149,6 +150,45 @@ spv_status spv_verify_chain_cached(const void *target_logits, const void *draft_
                                    float *out_resid_norm, int32_t *row_status,
                                    const int32_t *cache_ids, const int32_t *fanout, int32_t *cache_slot,
                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * spv_verify_chain_filtered -- spv_verify_chain on top-k / top-p filtered
+ * distributions ([SPD] "Evaluation": the sampled runs use top-k = 50 and
+ * top-p = 1.0 at T = 1).  Each target row i = 0..gamma and draft row
+ * i = 0..gamma-1 is filtered the same way:
+ *   1. keep the top_k ids by logit (descending, -0.0 equal to +0.0, ties to
+ *      the lower id);
+ *   2. p'(x) = exp((z_x - z_max) / T) / sum over the kept ids;
+ *   3. if top_p < 1, keep only the shortest prefix of them (in that order)
+ *      whose p' sum reaches top_p, and renormalise over it.
+ * Every other id has probability 0.  [SD] steps 3 and 4 then run on p', q':
+ * x_i stands iff p'_i(x_i) > 0 and r_i q'_i(x_i) <= p'_i(x_i); at the first
+ * rejection k one token is drawn from norm(max(0, p'_k - q'_k)), else the
+ * bonus from p'_gamma.  The draw is an exponential race over the kept ids
+ * of target row k: the id x with the smallest E_x / w(x) wins (w the
+ * residual or bonus mass, E_x = -ln U with U from Philox4x32-10 as for
+ * spv_verify_chain, counter (x / 4, 8, 0, k), word x % 4; ties to the lower
+ * id).  A rejection whose residual has no mass (a draft token outside q's
+ * support with p' = q' elsewhere) makes the row bad.
+ *
+ *   top_k       1 .. SPV_MAX_TOP_K (top_k >= V keeps every id)
+ *   top_p       in (0, 1]; 1 disables the nucleus cut
+ *   out_pq      p'_i(x_i), q'_i(x_i); out_resid_norm: sum max(0, p'_k - q'_k)
+ *               (k < gamma) or 1 (bonus) -- free here, no extra read
+ *   workspace   >= spv_filtered_workspace_bytes(B, gamma, V) bytes, 256-byte
+ *               aligned, zero-filled once (first 4 bytes: error word)
+ * T == 0 selects the greedy rule of spv_verify_greedy (no top-k filter
+ * changes an argmax).  Other arguments as spv_verify_chain.
+ */
+spv_status spv_verify_chain_filtered(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                                     const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
+                                     int B, int gamma, int V, float temperature, int top_k, float top_p,
+                                     int32_t *accept_count, int32_t *out_tokens, float *out_pq,
+                                     float *out_resid_norm, int32_t *row_status,
+                                     void *workspace, size_t workspace_bytes, void *stream);
+
+/* Workspace bytes spv_verify_chain_filtered needs (also valid for T == 0). */
+size_t spv_filtered_workspace_bytes(int B, int gamma, int V);
 
 /* Bytes of device memory behind spv_verify_chain_noalloc (per GPU, held from
  * library load until process exit). */

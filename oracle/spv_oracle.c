@@ -510,10 +510,10 @@ int spvo_verify_filtered_seq(const float *tgt, const float *drf, const int32_t *
                                  n[gamma + 1 + i], tok[i]);
         pq_out[2 * i] = p;
         pq_out[2 * i + 1] = q;
-        int acc = (p > 0) && ((double)r[i] * q <= p);
+        int stands = (p > 0) && ((double)r[i] * q <= p);
         if (i < k) {
             note_margin(&margin, (q > 0) ? fabs((double)r[i] - p / q) : INFINITY);
-            if (!acc) k = i;
+            if (!stands) k = i;
         }
     }
     /* draw over the kept target ids of row k, taken in ascending id order */

@@ -26,6 +26,7 @@ SPV_MAX_FANOUT_ROWS = 64
 SPV_SAMPLER_BLOCK = 1024
 SPV_SAMPLER_SUB = 32
 SPV_MAX_TRIALS = 64
+SPV_MAX_TOP_K = 64
 
 _lib = None
 
@@ -51,6 +52,11 @@ def load_library():
     lib.spv_verify_chain_cached.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, P, P, P, P, P, P, P,
                                             S, P]
     lib.spv_verify_chain_cached.restype = I
+    lib.spv_verify_chain_filtered.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, I, ctypes.c_float, P, P, P,
+                                              P, P, P, S, P]
+    lib.spv_verify_chain_filtered.restype = I
+    lib.spv_filtered_workspace_bytes.argtypes = [I, I, I]
+    lib.spv_filtered_workspace_bytes.restype = S
     lib.spv_verify_greedy.argtypes = [P, I, P, I, I, I, P, P, P, P, S, P]
     lib.spv_verify_greedy.restype = I
     lib.spv_fanout_topk.argtypes = [P, I, P, P, I, I, I, P, P, P, S, P]
@@ -214,6 +220,57 @@ def _verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, tem
     else:
         st = lib.spv_verify_chain(*args, *tail)
         _check(st, "spv_verify_chain")
+    return out
+
+
+def spv_filtered_workspace_bytes(B: int, gamma: int, V: int) -> int:
+    return load_library().spv_filtered_workspace_bytes(B, gamma, V)
+
+
+def spv_verify_chain_filtered(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature: float,
+                              top_k: int, top_p: float = 1.0, *, workspace=None, out=None, want_pq: bool = True,
+                              want_resid_norm: bool = False, want_status: bool = True, stream=None) -> dict:
+    """Chain verify on top-k / top-p filtered target and draft distributions
+    (see spv_verify_chain_filtered in spv.h); arguments and outputs as
+    :func:`spv_verify_chain`."""
+    target_logits = _cuda(target_logits, "target_logits")
+    dev = target_logits.device
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, gamma+1, V]")
+    B, g1, V = target_logits.shape
+    g = g1 - 1
+    greedy = float(temperature) == 0.0
+    draft_tokens = _cuda(draft_tokens, "draft_tokens", torch.int32)
+    if tuple(draft_tokens.shape) != (B, g):
+        raise ValueError("draft_tokens must be [B, gamma]")
+    if not greedy:
+        draft_logits = _cuda(draft_logits, "draft_logits", target_logits.dtype)
+        r = _cuda(r, "r", torch.float32)
+        sample_keys = _cuda(sample_keys, "sample_keys", torch.int64)
+        if tuple(draft_logits.shape) != (B, g, V) or tuple(r.shape) != (B, g) or tuple(sample_keys.shape) != (B,):
+            raise ValueError("draft_logits [B,g,V], r [B,g], sample_keys [B] expected")
+    else:
+        draft_logits = r = sample_keys = None
+    lib = load_library()
+    if workspace is None:
+        workspace = new_workspace(lib.spv_filtered_workspace_bytes(B, g, V), dev)
+    out = dict(out) if out else {}
+    if "accept_count" not in out:
+        out["accept_count"] = torch.empty(B, dtype=torch.int32, device=dev)
+    if "out_tokens" not in out:
+        out["out_tokens"] = torch.empty(B, g + 1, dtype=torch.int32, device=dev)
+    if want_pq and not greedy and "pq" not in out:
+        out["pq"] = torch.empty(B, g, 2, dtype=torch.float32, device=dev)
+    if want_resid_norm and not greedy and "resid_norm" not in out:
+        out["resid_norm"] = torch.empty(B, dtype=torch.float32, device=dev)
+    if want_status and "row_status" not in out:
+        out["row_status"] = torch.empty(B, dtype=torch.int32, device=dev)
+    st = lib.spv_verify_chain_filtered(_ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits),
+                                       _ptr(draft_tokens), _ptr(r), _ptr(sample_keys), B, g, V, float(temperature),
+                                       int(top_k), float(top_p), _ptr(out["accept_count"]), _ptr(out["out_tokens"]),
+                                       _ptr(out.get("pq")), _ptr(out.get("resid_norm")), _ptr(out.get("row_status")),
+                                       _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(st, "spv_verify_chain_filtered")
     return out
 
 

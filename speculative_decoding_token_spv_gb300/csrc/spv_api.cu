@@ -128,6 +128,57 @@ spv_status spv_verify_chain_cached(const void *target_logits, const void *draft_
                              fanout, cache_slot, workspace, workspace_bytes, stream);
 }
 
+size_t spv_filtered_workspace_bytes(int B, int gamma, int V)
+{
+    if (B < 1 || gamma < 1 || gamma > SPV_MAX_GAMMA || V < 2) return 0;
+    return spv::filtered_ws_bytes(B, gamma, V);
+}
+
+spv_status spv_verify_chain_filtered(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                                     const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
+                                     int B, int gamma, int V, float temperature, int top_k, float top_p,
+                                     int32_t *accept_count, int32_t *out_tokens, float *out_pq,
+                                     float *out_resid_norm, int32_t *row_status, void *workspace,
+                                     size_t workspace_bytes, void *stream)
+{
+    if (!dtype_ok(dtype) || !target_logits || !draft_tokens || !accept_count || !out_tokens || !workspace)
+        return SPV_ERR_INVALID_ARG;
+    if (gamma < 1 || gamma > SPV_MAX_GAMMA || !sizes_ok(B, 2 * gamma + 1, V)) return SPV_ERR_INVALID_ARG;
+    if (!(temperature >= 0.0f) || std::isinf(temperature)) return SPV_ERR_INVALID_ARG;
+    if (top_k < 1 || top_k > SPV_MAX_TOP_K || !(top_p > 0.0f) || !(top_p <= 1.0f)) return SPV_ERR_INVALID_ARG;
+    if (!aligned256(workspace)) return SPV_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.0f;
+    const size_t need = greedy ? spv::greedy_ws_bytes(B, gamma, V) : spv::filtered_ws_bytes(B, gamma, V);
+    if (workspace_bytes < need) return SPV_ERR_INVALID_ARG;
+    if (!greedy && (!draft_logits || !r || !sample_keys)) return SPV_ERR_INVALID_ARG;
+    if (!greedy && !(1.0f / temperature < INFINITY)) return SPV_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * (2 * gamma + 1) * spv::chunks_per_row(V) > 0x7fffffffLL) return SPV_ERR_UNSUPPORTED;
+
+    spv::ChainLaunch L{};
+    L.target = target_logits;
+    L.draft = draft_logits;
+    L.dtype = dtype == SPV_F32 ? 0 : 1;
+    L.tokens = draft_tokens;
+    L.r = r;
+    L.keys = sample_keys;
+    L.B = B;
+    L.gamma = gamma;
+    L.V = V;
+    L.T = temperature;
+    L.top_k = top_k;
+    L.top_p = top_p;
+    L.accept_count = accept_count;
+    L.out_tokens = out_tokens;
+    L.out_pq = out_pq;
+    L.out_Z = out_resid_norm;
+    L.row_status = row_status;
+    L.ws = workspace;
+    const bool rows16 = (static_cast<size_t>(V) * elem_bytes(dtype)) % 16 == 0;
+    L.tma = rows16 && aligned16(target_logits) && (greedy || aligned16(draft_logits));
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return cuda_status(greedy ? spv::launch_greedy(L, st) : spv::launch_filtered(L, st));
+}
+
 spv_status spv_verify_greedy(const void *target_logits, spv_dtype dtype, const int32_t *draft_tokens, int B,
                              int gamma, int V, int32_t *accept_count, int32_t *out_tokens, int32_t *row_status,
                              void *workspace, size_t workspace_bytes, void *stream)

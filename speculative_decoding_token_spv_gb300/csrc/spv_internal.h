@@ -32,6 +32,9 @@ struct ChainLaunch {
     const int32_t *cache_ids;
     const int32_t *cache_fanout;  // host, gamma + 1 entries
     int32_t *cache_slot;
+    // Top-k / top-p filter (spv_verify_chain_filtered only).
+    int top_k;
+    float top_p;
 };
 
 struct FanoutLaunch {
@@ -50,9 +53,11 @@ struct FanoutLaunch {
 size_t chain_ws_bytes(int B, int gamma, int V);
 size_t greedy_ws_bytes(int B, int gamma, int V);
 size_t fanout_ws_bytes(int B, int K1, int V, int Fmax);
+size_t filtered_ws_bytes(int B, int gamma, int V);
 
 cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st);
 cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st);
 cudaError_t launch_fanout(const FanoutLaunch &L, cudaStream_t st);
+cudaError_t launch_filtered(const ChainLaunch &L, cudaStream_t st);
 
 }  // namespace spv

@@ -17,7 +17,9 @@ Workloads (stand-ins for the pages' evaluation sets, which are not used):
   sweep   the spd distributions at gamma=4, V=151936, fp32 / bf16,
           B in {1, 8, 64, 128, 256}
 Any chain workload can also draw the draft row of the bonus position
-(``bonus_draft``), which the speculation-cache fan-out ranks.
+(``bonus_draft``), which the speculation-cache fan-out ranks, and can draw its
+draft tokens from the top_k / top_p restricted draft distribution (the
+filtered verify's input).
 All draws are fp32 from seeded ``torch.Generator`` s on the requested device,
 then cast to the workload dtype; V is the last, contiguous axis.
 """
@@ -72,15 +74,25 @@ def _gen(device, seed):
     return g
 
 
-def _draft_tokens(d: torch.Tensor, temperature: float, seed: int, device) -> torch.Tensor:
+def _draft_tokens(d: torch.Tensor, temperature: float, seed: int, device, top_k=None, top_p=1.0) -> torch.Tensor:
+    """The draft model's sampler: softmax(d / T), optionally restricted to the
+    top_k logits and the top_p nucleus of those (torch.topk order)."""
     B, g, V = d.shape
     if g == 0:
         return torch.zeros(B, 0, dtype=torch.int32, device=device)
     flat = d.float().reshape(B * g, V)
     if temperature == 0:
         return flat.argmax(dim=1).to(torch.int32).reshape(B, g)
-    probs = torch.softmax(flat / temperature, dim=1)
-    return torch.multinomial(probs, 1, generator=_gen(device, seed)).to(torch.int32).reshape(B, g)
+    if top_k is None:
+        probs = torch.softmax(flat / temperature, dim=1)
+        return torch.multinomial(probs, 1, generator=_gen(device, seed)).to(torch.int32).reshape(B, g)
+    vals, ids = torch.topk(flat, min(top_k, V), dim=1)
+    probs = torch.softmax(vals / temperature, dim=1)
+    if top_p < 1.0:
+        before = torch.cumsum(probs, dim=1) - probs
+        probs = torch.where(before < top_p, probs, torch.zeros_like(probs))
+    pick = torch.multinomial(probs, 1, generator=_gen(device, seed))
+    return ids.gather(1, pick).to(torch.int32).reshape(B, g)
 
 
 def _uniforms_and_keys(B, g, seed, device):
@@ -91,7 +103,7 @@ def _uniforms_and_keys(B, g, seed, device):
 
 
 def chain_from_params(name, B, gamma, V, dtype, temperature, z_std, d_scale, d_std, peaks, seeds,
-                      device="cpu", bonus_draft=False) -> ChainInputs:
+                      device="cpu", bonus_draft=False, top_k=None, top_p=1.0) -> ChainInputs:
     """Generic generator: z ~ N(0, z_std^2) [B, gamma+1, V] (+8 on `peaks` ids
     per target row), d = d_scale * z[:, :gamma] + N(0, d_std^2).  With
     `bonus_draft` also the draft row of position gamma, d_scale * z[:, gamma]
@@ -115,32 +127,33 @@ def chain_from_params(name, B, gamma, V, dtype, temperature, z_std, d_scale, d_s
     del z
     draft = d.to(dtype)
     del d
-    tokens = _draft_tokens(draft, temperature, s_tok, device)
+    tokens = _draft_tokens(draft, temperature, s_tok, device, top_k, top_p)
     r, keys = _uniforms_and_keys(B, gamma, s_u, device)
-    return ChainInputs(name, target, draft, tokens, r, keys, float(temperature),
-                       dict(B=B, gamma=gamma, V=V, dtype=str(dtype).replace("torch.", ""),
-                            T=float(temperature)), draft_bonus)
+    meta = dict(B=B, gamma=gamma, V=V, dtype=str(dtype).replace("torch.", ""), T=float(temperature))
+    if top_k is not None:
+        meta.update(top_k=top_k, top_p=top_p)
+    return ChainInputs(name, target, draft, tokens, r, keys, float(temperature), meta, draft_bonus)
 
 
-def tiny(device="cpu", temperature=1.0, bonus_draft=False) -> ChainInputs:
+def tiny(device="cpu", temperature=1.0, bonus_draft=False, top_k=None, top_p=1.0) -> ChainInputs:
     return chain_from_params("tiny", 1, 4, 1000, torch.float32, temperature, 2.0, 1.0, 0.5, 0,
-                             SEEDS["tiny"], device, bonus_draft)
+                             SEEDS["tiny"], device, bonus_draft, top_k, top_p)
 
 
-def spd(device="cpu", temperature=1.0, B=64, bonus_draft=False) -> ChainInputs:
+def spd(device="cpu", temperature=1.0, B=64, bonus_draft=False, top_k=None, top_p=1.0) -> ChainInputs:
     return chain_from_params("spd", B, 1, 151936, torch.bfloat16, temperature, 3.0, 1.0, 1.0, 20,
-                             SEEDS["spd"], device, bonus_draft)
+                             SEEDS["spd"], device, bonus_draft, top_k, top_p)
 
 
-def eagle(gamma=7, device="cpu", temperature=1.0, B=32, bonus_draft=False) -> ChainInputs:
+def eagle(gamma=7, device="cpu", temperature=1.0, B=32, bonus_draft=False, top_k=None, top_p=1.0) -> ChainInputs:
     return chain_from_params(f"eagle_g{gamma}", B, gamma, 128256, torch.bfloat16, temperature, 2.5, 0.8,
-                             1.5, 0, SEEDS["eagle"], device, bonus_draft)
+                             1.5, 0, SEEDS["eagle"], device, bonus_draft, top_k, top_p)
 
 
 def sweep(B=64, dtype=torch.float32, device="cpu", temperature=1.0, V=151936, gamma=4,
-          bonus_draft=False) -> ChainInputs:
+          bonus_draft=False, top_k=None, top_p=1.0) -> ChainInputs:
     return chain_from_params(f"sweep_B{B}_{str(dtype).replace('torch.', '')}", B, gamma, V, dtype,
-                             temperature, 3.0, 1.0, 1.0, 20, SEEDS["sweep"], device, bonus_draft)
+                             temperature, 3.0, 1.0, 1.0, 20, SEEDS["sweep"], device, bonus_draft, top_k, top_p)
 
 
 def cache_fanout_inputs(w: ChainInputs):

@@ -126,3 +126,30 @@ def test_cached_verify_arguments_rejected_on_host(lib):
     assert call(g=0) == INV
     assert call(t=None) == INV
     assert call(T=0.0, wsb=16) == INV
+
+
+def test_filtered_verify_arguments_rejected_on_host(lib):
+    """spv_verify_chain_filtered: 1 <= top_k <= SPV_MAX_TOP_K, 0 < top_p <= 1,
+    plus the chain checks; its workspace size covers the segment lists."""
+    import speculative_decoding_token_spv_gb300 as spv
+    P = ctypes.c_void_p
+    fake = P(4096)
+    ws = P(1 << 20)
+    big = 1 << 40
+    INV = 1
+    ok_args = dict(t=fake, d=fake, dt=0, tok=fake, r=fake, keys=fake, B=4, g=4, V=1000, T=1.0, k=50, p=1.0,
+                   acc=fake, out=fake, pq=None, z=None, st=None, ws=ws, wsb=big, stream=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.spv_verify_chain_filtered(a["t"], a["d"], a["dt"], a["tok"], a["r"], a["keys"], a["B"], a["g"],
+                                             a["V"], ctypes.c_float(a["T"]), a["k"], ctypes.c_float(a["p"]),
+                                             a["acc"], a["out"], a["pq"], a["z"], a["st"], a["ws"], a["wsb"],
+                                             a["stream"])
+
+    for kw in (dict(k=0), dict(k=65), dict(p=0.0), dict(p=-0.5), dict(p=1.0001), dict(p=float("nan")),
+               dict(t=None), dict(g=33), dict(T=-1.0), dict(d=None), dict(wsb=16), dict(ws=P((1 << 20) + 8))):
+        assert call(**kw) == INV, kw
+    n = spv.spv_filtered_workspace_bytes(64, 4, 151936)
+    assert n >= 64 * 9 * 19 * 64 * 8 and n >= spv.spv_greedy_workspace_bytes(64, 4, 151936)
+    assert spv.spv_filtered_workspace_bytes(0, 4, 100) == 0

@@ -63,6 +63,9 @@ MUTANTS = {
     "filtered_race_weight": ("expo(seq_key, SPVO_STREAM_FILTERED, 0, (uint32_t)k, (uint64_t)x) / wx",
                              "expo(seq_key, SPVO_STREAM_FILTERED, 0, (uint32_t)k, (uint64_t)x) * wx",
                              ["test_filtered_first_token_and_bonus_are_exact"]),
+    "filtered_accept_transposed": ("int stands = (p > 0) && ((double)r[i] * q <= p);",
+                                   "int stands = (p > 0) && ((double)r[i] * p <= q);",
+                                   ["test_filtered_acceptance_rate_is_one_minus_tvd"]),
     "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
                        ["test_fanout_sizes_golden"]),
 }
@@ -76,6 +79,8 @@ def _calls(name):
         return [lambda: fn(None), lambda: fn(8)]
     if name == "test_filter_row_vs_torch_topk_softmax":
         return [lambda: fn(1.0)]
+    if name == "test_filtered_acceptance_rate_is_one_minus_tvd":
+        return [lambda: fn(10), lambda: fn(40)]
     return [fn]
 
 

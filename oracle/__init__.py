@@ -70,6 +70,9 @@ def _load():
         lib.spvo_verify_filtered_batch.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                    ctypes.c_int, ctypes.c_double, ctypes.c_int, ctypes.c_double,
                                                    P, P, P, P, P, P]
+        lib.spvo_verify_saguaro_batch.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_double, P, P, ctypes.c_int, ctypes.c_double,
+                                                  P, P, P, P, P, P, P]
         lib.spvo_verify_greedy_batch.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  P, P, P]
         _lib = lib
@@ -195,6 +198,46 @@ def verify_filtered(target, draft, tokens, r, keys, temperature: float, top_k: i
                                        float(temperature), int(top_k), float(top_p), _ptr(out["accept_count"]),
                                        _ptr(out["out_tokens"]), _ptr(out["pq"]), _ptr(Z) if want_Z else None,
                                        _ptr(out["margin"]), _ptr(out["status"]))
+
+    _run_ranges(run, B, threads)
+    if want_Z:
+        out["Z"] = Z
+    return out
+
+
+def verify_saguaro(target, draft, tokens, r, keys, temperature: float, cache_ids, fanout, C: float,
+                   want_Z: bool = False, threads: int | None = None) -> dict:
+    """Chain verify against Saguaro-sampled drafts: the draft distribution
+    at position i divides the probability of that position's cached
+    candidates (cache_ids [B, sum F], k-major, fanout: gamma+1 ints; the
+    first gamma positions are used) by C and renormalises.  T == 0 routes to
+    :func:`verify_greedy` (the argmax rule ignores the draft distribution).
+    Outputs as :func:`verify_chain`."""
+    if temperature == 0:
+        return verify_greedy(target, tokens, threads=threads)
+    target, draft = _f32(target), _f32(draft)
+    B, g1, V = target.shape
+    g = g1 - 1
+    F = np.ascontiguousarray(np.asarray(fanout, dtype=np.int32))
+    if F.shape[0] != g + 1:
+        raise ValueError("fanout needs gamma+1 entries")
+    sumF = int(F.sum())
+    ids = np.ascontiguousarray(np.asarray(cache_ids, dtype=np.int32).reshape(B, sumF))
+    tokens = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32)).reshape(B, g)
+    r = _f32(r).reshape(B, g)
+    keys = np.ascontiguousarray(np.asarray(keys, dtype=np.uint64)).reshape(B)
+    out = dict(accept_count=np.zeros(B, np.int32), out_tokens=np.zeros((B, g + 1), np.int32),
+               pq=np.zeros((B, g, 2)), margin=np.zeros(B), trials=np.zeros(B, np.int32),
+               status=np.zeros(B, np.int32))
+    Z = np.zeros(B) if want_Z else None
+    lib = _load()
+
+    def run(b0, b1):
+        lib.spvo_verify_saguaro_batch(_ptr(target), _ptr(draft), _ptr(tokens), _ptr(r), _ptr(keys), b0, b1, g, V,
+                                      float(temperature), _ptr(ids), _ptr(F), sumF, float(C),
+                                      _ptr(out["accept_count"]), _ptr(out["out_tokens"]), _ptr(out["pq"]),
+                                      _ptr(Z) if want_Z else None, _ptr(out["margin"]), _ptr(out["trials"]),
+                                      _ptr(out["status"]))
 
     _run_ranges(run, B, threads)
     if want_Z:

@@ -559,6 +559,144 @@ int spvo_verify_filtered_seq(const float *tgt, const float *drf, const int32_t *
 }
 
 /* ------------------------------------------------------------------------ */
+/* Saguaro sampling, [SSD] "Key Innovations" / Table 7b (logit bonus C,
+ * Theorem 15: the cache hit rate grows with C, C = 1 being plain sampling).
+ * Reading: at draft position i the draft samples from
+ *   q_C(x) = q(x) w(x) / sum_y q(y) w(y),   w(x) = 1/C if x is one of the
+ * position's cached candidates S_i, else 1,
+ * i.e. the cached candidates' draft logits are lowered by T ln C.  The verify
+ * step is [SD] steps 3 and 4 with q_C in place of q -- exact for the draft
+ * tokens drawn from q_C -- so a rejection's residual max(0, p - q_C) leans
+ * towards the cached candidates.  S_i = the ids of cache_ids[off_i ..
+ * off_i + F_i) (k-major lists, as for the cache lookup) that lie in [0, V),
+ * counted once.  Same outputs, sampling rule and streams as
+ * spvo_verify_chain_seq; pq holds p_i(x_i), q_C,i(x_i). */
+static double sag_prob(const float *z, const unsigned char *inS, int x, double T, double M, double S, double invC)
+{
+    return exp((double)z[x] / T - M) * (inS[x] ? invC : 1.0) / S;
+}
+
+int spvo_verify_saguaro_seq(const float *tgt, const float *drf, const int32_t *tok, const float *r, uint64_t seq_key,
+                            int gamma, int V, double T, const int32_t *cache_ids, const int32_t *fanout, double C,
+                            int32_t *k_out, int32_t *tokens_out, double *pq_out, double *Z_out, double *margin_out,
+                            int32_t *trials_out)
+{
+    for (int i = 0; i <= gamma; ++i) tokens_out[i] = -1;
+    for (int i = 0; i < 2 * gamma; ++i) pq_out[i] = NAN;
+    *k_out = -1;
+    *margin_out = INFINITY;
+    *trials_out = 0;
+    if (Z_out) *Z_out = NAN;
+    for (int i = 0; i < gamma; ++i)
+        if (tok[i] < 0 || tok[i] >= V) return SPVO_BAD_ROW;
+    const double invC = 1.0 / C;
+    double Mt[65], St[65], Md[64], Sd[64];
+    for (int i = 0; i <= gamma; ++i)
+        if (spvo_softmax_stats(tgt + (size_t)i * V, V, T, &Mt[i], &St[i]) != SPVO_OK) return SPVO_BAD_ROW;
+    /* membership of each draft position's cached candidates, and q_C's normaliser */
+    unsigned char *inS = (unsigned char *)calloc((size_t)gamma * (size_t)V, 1);
+    int off = 0;
+    for (int i = 0; i < gamma; ++i) {
+        for (int j = 0; j < fanout[i]; ++j) {
+            int x = cache_ids[off + j];
+            if (x >= 0 && x < V) inS[(size_t)i * V + x] = 1;
+        }
+        off += fanout[i];
+    }
+    for (int i = 0; i < gamma; ++i) {
+        const float *d = drf + (size_t)i * V;
+        double M = -INFINITY;
+        for (int x = 0; x < V; ++x) {
+            double v = (double)d[x];
+            if (isnan(v) || (isinf(v) && v > 0)) { free(inS); return SPVO_BAD_ROW; }
+            if (v / T > M) M = v / T;
+        }
+        if (isinf(M)) { free(inS); return SPVO_BAD_ROW; }
+        ksum S = { 0, 0 };
+        for (int x = 0; x < V; ++x) ksum_add(&S, exp((double)d[x] / T - M) * (inS[(size_t)i * V + x] ? invC : 1.0));
+        Md[i] = M;
+        Sd[i] = ksum_val(&S);
+    }
+
+    int k = gamma;
+    double margin = INFINITY;
+    for (int i = 0; i < gamma; ++i) {
+        double p = prob(tgt + (size_t)i * V, tok[i], T, Mt[i], St[i]);
+        double q = sag_prob(drf + (size_t)i * V, inS + (size_t)i * V, tok[i], T, Md[i], Sd[i], invC);
+        pq_out[2 * i] = p;
+        pq_out[2 * i + 1] = q;
+        int stands = (p > 0) && ((double)r[i] * q <= p);
+        if (i < k) {
+            note_margin(&margin, (q > 0) ? fabs((double)r[i] - p / q) : INFINITY);
+            if (!stands) k = i;
+        }
+    }
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    int emitted;
+    if (k == gamma) {
+        const float *tb = tgt + (size_t)gamma * V;
+        for (int x = 0; x < V; ++x) w[x] = prob(tb, x, T, Mt[gamma], St[gamma]);
+        emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,
+                              (uint32_t)gamma, &margin);
+        if (Z_out) *Z_out = 1.0;
+    } else {
+        const float *tj = tgt + (size_t)k * V, *dj = drf + (size_t)k * V;
+        const unsigned char *sj = inS + (size_t)k * V;
+        for (int x = 0; x < V; ++x) w[x] = prob(tj, x, T, Mt[k], St[k]);
+        emitted = -1;
+        int t;
+        for (t = 0; t < SPVO_MAX_TRIALS; ++t) {
+            int x = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, (uint32_t)t,
+                                (uint32_t)k, &margin);
+            double v = spvo_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
+            double p = w[x], q = sag_prob(dj, sj, x, T, Md[k], Sd[k], invC);
+            note_margin(&margin, fabs((1.0 - v) - q / p));
+            if (q <= (1.0 - v) * p) { emitted = x; break; }
+        }
+        *trials_out = (emitted >= 0) ? t + 1 : SPVO_MAX_TRIALS + 1;
+        for (int x = 0; x < V; ++x) {
+            double d = w[x] - sag_prob(dj, sj, x, T, Md[k], Sd[k], invC);
+            w[x] = d > 0 ? d : 0.0;
+        }
+        ksum Z = { 0, 0 };
+        for (int x = 0; x < V; ++x) ksum_add(&Z, w[x]);
+        if (emitted < 0) {
+            if (!(ksum_val(&Z) > 0)) {
+                free(w);
+                free(inS);
+                for (int i = 0; i < 2 * gamma; ++i) pq_out[i] = NAN;
+                return SPVO_BAD_ROW;
+            }
+            emitted = race_sample(w, V, seq_key, SPVO_STREAM_FB_BLOCK, SPVO_STREAM_FB_SUB, SPVO_STREAM_FB_TOKEN, 0,
+                                  (uint32_t)k, &margin);
+        }
+        if (Z_out) *Z_out = ksum_val(&Z);
+    }
+    free(w);
+    free(inS);
+    for (int i = 0; i < k; ++i) tokens_out[i] = tok[i];
+    tokens_out[k] = emitted;
+    *k_out = k;
+    *margin_out = margin;
+    return SPVO_OK;
+}
+
+void spvo_verify_saguaro_batch(const float *tgt, const float *drf, const int32_t *tok, const float *r,
+                               const uint64_t *keys, int b0, int b1, int gamma, int V, double T,
+                               const int32_t *cache_ids, const int32_t *fanout, int sumF, double C,
+                               int32_t *k_out, int32_t *tokens_out, double *pq_out, double *Z_out,
+                               double *margin_out, int32_t *trials_out, int32_t *status_out)
+{
+    for (int b = b0; b < b1; ++b) {
+        status_out[b] = spvo_verify_saguaro_seq(
+            tgt + (size_t)b * (size_t)(gamma + 1) * (size_t)V, drf + (size_t)b * (size_t)gamma * (size_t)V,
+            tok + (size_t)b * gamma, r + (size_t)b * gamma, keys[b], gamma, V, T, cache_ids + (size_t)b * sumF,
+            fanout, C, &k_out[b], tokens_out + (size_t)b * (gamma + 1), pq_out + (size_t)b * 2 * gamma,
+            Z_out ? &Z_out[b] : 0, &margin_out[b], &trials_out[b]);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Speculation-cache lookup, [SSD] Algorithm 1 ("if verify_outcome in cache")
  * and Figure 2: the cache holds one branch per (k, t) pair, for every
  * position k = 0..K and each of the F_k fan-out candidates t listed for it,

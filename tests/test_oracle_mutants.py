@@ -66,6 +66,12 @@ MUTANTS = {
     "filtered_accept_transposed": ("int stands = (p > 0) && ((double)r[i] * q <= p);",
                                    "int stands = (p > 0) && ((double)r[i] * p <= q);",
                                    ["test_filtered_acceptance_rate_is_one_minus_tvd"]),
+    "saguaro_weight_inverted": ("return exp((double)z[x] / T - M) * (inS[x] ? invC : 1.0) / S;",
+                                "return exp((double)z[x] / T - M) * (inS[x] ? 1.0 / invC : 1.0) / S;",
+                                ["test_saguaro_draft_probabilities"]),
+    "saguaro_normaliser_unweighted": ("exp((double)d[x] / T - M) * (inS[(size_t)i * V + x] ? invC : 1.0));",
+                                      "exp((double)d[x] / T - M));",
+                                      ["test_saguaro_draft_probabilities"]),
     "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
                        ["test_fanout_sizes_golden"]),
 }
@@ -79,6 +85,8 @@ def _calls(name):
         return [lambda: fn(None), lambda: fn(8)]
     if name == "test_filter_row_vs_torch_topk_softmax":
         return [lambda: fn(1.0)]
+    if name == "test_saguaro_draft_probabilities":
+        return [lambda: fn(2.0), lambda: fn(8.0)]
     if name == "test_filtered_acceptance_rate_is_one_minus_tvd":
         return [lambda: fn(10), lambda: fn(40)]
     return [fn]

@@ -752,3 +752,113 @@ def test_zero_residual_mass_is_a_bad_row():
     # the same row with a token inside the support is fine
     out = oracle.verify_chain(z, d, np.array([[3]], np.int32), np.ones((1, 1), np.float32), _keys(1), 1.0)
     assert out["status"][0] == 0 and out["accept_count"][0] == 1
+
+
+# ----------------------------------------------------------------- Saguaro sampling
+def _saguaro_case(rng, B, g, V, F, z_std=1.5, noise=1.0):
+    """Per-position p_i, q_i shared by all sequences; cached candidates S_i =
+    the top-F_i draft ids (no exclusion); q_C and tokens drawn from it are
+    built per C by the caller."""
+    zl = rng.normal(0, z_std, (g + 1, V)).astype(np.float32)
+    dl = (zl + rng.normal(0, noise, (g + 1, V))).astype(np.float32)
+    p = np.stack([_probs(zl[i]) for i in range(g + 1)])
+    q = np.stack([_probs(dl[i]) for i in range(g + 1)])
+    lists = [np.argsort(-dl[i].astype(np.float64), kind="stable")[:F[i]] for i in range(g + 1)]
+    ids = np.concatenate(lists).astype(np.int32)
+    return zl, dl, p, q, lists, np.broadcast_to(ids, (B, ids.size)).copy()
+
+
+def _q_C(q, S, C):
+    w = np.ones_like(q)
+    w[S] = 1.0 / C
+    qc = q * w
+    return qc / qc.sum()
+
+
+def test_saguaro_C1_is_plain_chain():
+    """C = 1 leaves the draft distribution as it is: identical outputs."""
+    rng = np.random.default_rng(40)
+    B, g, V = 300, 3, 500
+    F = [6, 5, 4, 3]
+    zl, dl, p, q, lists, ids = _saguaro_case(rng, B, g, V, F)
+    z = np.broadcast_to(zl, (B, g + 1, V)).astype(np.float32)
+    d = np.broadcast_to(dl[:g], (B, g, V)).astype(np.float32)
+    tok = np.stack([rng.choice(V, size=B, p=q[i]) for i in range(g)], axis=1).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    a = oracle.verify_saguaro(z, d, tok, r, _keys(B, 50), 1.0, ids, F, 1.0, want_Z=True)
+    b = oracle.verify_chain(z, d, tok, r, _keys(B, 50), 1.0, want_Z=True)
+    for key in ("accept_count", "out_tokens", "status", "trials"):
+        assert np.array_equal(a[key], b[key]), key
+    np.testing.assert_allclose(a["pq"], b["pq"], rtol=1e-13)
+    np.testing.assert_allclose(a["Z"], b["Z"], rtol=1e-12)
+
+
+@pytest.mark.parametrize("C", [2.0, 8.0, 0.5])
+def test_saguaro_draft_probabilities(C):
+    """q_C(x) = q(x) w(x) / sum q w with w = 1/C on the cached candidates,
+    computed here from the softmax probabilities (scipy)."""
+    rng = np.random.default_rng(41)
+    B, g, V = 40, 2, 300
+    F = [9, 4, 2]
+    zl, dl, p, q, lists, ids = _saguaro_case(rng, B, g, V, F)
+    z = np.broadcast_to(zl, (B, g + 1, V)).astype(np.float32)
+    d = np.broadcast_to(dl[:g], (B, g, V)).astype(np.float32)
+    tok = rng.integers(0, V, (B, g)).astype(np.int32)
+    tok[:, 0] = lists[0][rng.integers(0, F[0], B)]          # many cached tokens
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    out = oracle.verify_saguaro(z, d, tok, r, _keys(B, 51), 1.0, ids, F, C)
+    for i in range(g):
+        qc = _q_C(q[i], lists[i], C)
+        np.testing.assert_allclose(out["pq"][:, i, 1], qc[tok[:, i]], rtol=1e-12)
+        np.testing.assert_allclose(out["pq"][:, i, 0], p[i][tok[:, i]], rtol=1e-12)
+
+
+def test_saguaro_preserves_the_target_distribution():
+    """With tokens drawn from q_C the first emitted token is still
+    distributed as p_1 (the [SD] exactness argument with q_C as the draft)."""
+    rng = np.random.default_rng(42)
+    B, V, C = 30000, 200, 4.0
+    F = [12, 12]
+    zl, dl, p, q, lists, ids = _saguaro_case(rng, B, 1, V, F, noise=0.8)
+    qc = _q_C(q[0], lists[0], C)
+    z = np.broadcast_to(zl, (B, 2, V)).astype(np.float32)
+    d = np.broadcast_to(dl[:1], (B, 1, V)).astype(np.float32)
+    tok = rng.choice(V, size=(B, 1), p=qc).astype(np.int32)
+    r = (1 - rng.random((B, 1))).astype(np.float32)
+    out = oracle.verify_saguaro(z, d, tok, r, _keys(B, 52), 1.0, ids, F, C)
+    ok, pv = _chi2_ok(np.bincount(out["out_tokens"][:, 0], minlength=V), p[0])
+    assert ok, pv
+    alpha = np.minimum(p[0], qc).sum()
+    emp = (out["accept_count"] == 1).mean()
+    assert abs(emp - alpha) < 5 * np.sqrt(alpha * (1 - alpha) / B), (emp, alpha)
+
+
+def _saguaro_hit_closed_form(p, q, lists, C, g):
+    reach, h = 1.0, 0.0
+    for j in range(g):
+        qc = _q_C(q[j], lists[j], C)
+        a = np.minimum(p[j], qc).sum()
+        res = np.maximum(p[j] - qc, 0.0)
+        h += reach * (1 - a) * res[lists[j]].sum() / res.sum()
+        reach *= a
+    return h + reach * p[g][lists[g]].sum()
+
+
+def test_saguaro_hit_rate_grows_with_C():
+    """Theorem 15: the cache hit rate increases with C (closed form over
+    C = 1, 2, 4, 8), and the oracle's hit frequency matches the closed form
+    at C = 1 and C = 4 (5 sigma)."""
+    rng = np.random.default_rng(43)
+    B, g, V = 20000, 3, 60
+    F = [6, 5, 4, 3]
+    zl, dl, p, q, lists, ids = _saguaro_case(rng, B, g, V, F)
+    h = [_saguaro_hit_closed_form(p, q, lists, C, g) for C in (1.0, 2.0, 4.0, 8.0)]
+    assert all(b > a for a, b in zip(h, h[1:])), h
+    z = np.broadcast_to(zl, (B, g + 1, V)).astype(np.float32)
+    d = np.broadcast_to(dl[:g], (B, g, V)).astype(np.float32)
+    for C, want in ((1.0, h[0]), (4.0, h[2])):
+        tok = np.stack([rng.choice(V, size=B, p=_q_C(q[i], lists[i], C)) for i in range(g)], axis=1).astype(np.int32)
+        r = (1 - rng.random((B, g))).astype(np.float32)
+        out = oracle.verify_saguaro(z, d, tok, r, _keys(B, 53 + int(C)), 1.0, ids, F, C)
+        hits = (oracle.cache_slots(out["accept_count"], out["out_tokens"], ids, F) >= 0).mean()
+        assert abs(hits - want) < 5 * np.sqrt(want * (1 - want) / B), (C, hits, want)

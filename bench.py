@@ -475,6 +475,34 @@ def run_variants(spv, dev, stream, args):
         res[-1]["cache_hit_rate"] = round(hits / n, 4)
         res[-1]["cache_hit_sample"] = f"{n} verify outcomes"
         del w, o, ws, lists
+    # Saguaro sampling: drafts drawn with the cached candidates' probability
+    # divided by C; acceptance falls and the cache hit rate rises with C.
+    w = workloads.sweep(B=64, device=dev, bonus_draft=True)
+    F = [8, 7, 6, 5, 4]
+    d, _ = workloads.cache_fanout_inputs(w)
+    lists = spv.spv_fanout_topk(d, torch.full((w.B, w.gamma + 1), -1, dtype=torch.int32, device=dev), F)["ids"]
+    del d
+    ws = spv.new_workspace(spv.spv_chain_workspace_bytes(w.B, w.gamma, w.V), dev)
+    for C in (1.0, 2.0, 4.0, 8.0):
+        gen = torch.Generator(device=dev).manual_seed(91)
+        hits, acc, n = 0, 0, 0
+        for rep in range(16):
+            tok = workloads.saguaro_tokens(w, lists, F, C, seed=100 + rep)
+            keys = torch.randint(-(2 ** 63), 2 ** 63 - 1, (w.B,), generator=gen, device=dev, dtype=torch.int64)
+            r = 1.0 - torch.rand(w.B, w.gamma, generator=gen, device=dev)
+            oo = spv.spv_verify_chain_saguaro(w.target, w.draft, tok, r, keys, 1.0, lists, F, C, workspace=ws)
+            hits += int((oo["cache_slot"] >= 0).sum())
+            acc += int(oo["accept_count"].sum())
+            n += w.B
+        o = spv.spv_verify_chain_saguaro(w.target, w.draft, tok, w.r, w.keys, 1.0, lists, F, C, workspace=ws)
+        ms = time_graph(lambda: spv.spv_verify_chain_saguaro(w.target, w.draft, tok, w.r, w.keys, 1.0, lists, F, C,
+                                                             workspace=ws, out=o))
+        add(f"saguaro verify sweep B=64 fp32 T=1 C={C:g} F={F}", ms,
+            chain_bytes(w.B, w.gamma, w.V, 4, 1.0) + w.B * (sum(F) + 1) * 4, w.B * (w.gamma + 1))
+        res[-1]["cache_hit_rate"] = round(hits / n, 4)
+        res[-1]["mean_accepted"] = round(acc / n, 4)
+        res[-1]["sample"] = f"{n} verify outcomes"
+    del w, ws, lists
     torch.cuda.synchronize()
     return res
 

@@ -120,6 +120,31 @@ spv_status spv_verify_chain(const void *target_logits, const void *draft_logits,
 size_t spv_chain_workspace_bytes(int B, int gamma, int V);
 
 /*
+ * spv_verify_chain_saguaro -- spv_verify_chain_cached for drafts drawn by
+ * Saguaro sampling ([SSD] "Key Innovations" / Table 7b, logit bonus C,
+ * Theorem 15: the cache hit rate grows with C; C = 1 is plain sampling).
+ * Reading: at draft position i the draft drew x_i from
+ *   q_C,i(x) = q_i(x) w_i(x) / sum_y q_i(y) w_i(y),  w_i(x) = 1/C if x is one
+ * of position i's cached candidates (cache_ids entries off_i .. off_i + F_i
+ * - 1, ids outside [0, V) ignored, repeats counted once), else 1.
+ * The verify step runs on (p_i, q_C,i) -- [SD] steps 3 and 4 with q_C as the
+ * draft distribution, so the emitted tokens stay distributed as p -- and the
+ * outcome is looked up in the cache as by spv_verify_chain_cached.  out_pq
+ * holds p_i(x_i), q_C,i(x_i); out_resid_norm sum max(0, p_k - q_C,k).
+ *   C           > 0, finite (C > 1 moves residual mass onto the cached ids)
+ *   V           <= 1,048,576 (else SPV_ERR_UNSUPPORTED)
+ * Other arguments, the workspace and T == 0 (greedy; C plays no part) as
+ * spv_verify_chain_cached.
+ */
+spv_status spv_verify_chain_saguaro(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                                    const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
+                                    int B, int gamma, int V, float temperature,
+                                    const int32_t *cache_ids, const int32_t *fanout, float C,
+                                    int32_t *accept_count, int32_t *out_tokens, float *out_pq,
+                                    float *out_resid_norm, int32_t *row_status, int32_t *cache_slot,
+                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * spv_verify_chain_cached -- spv_verify_chain followed, in the same kernels,
  * by the speculation-cache lookup of [SSD] Algorithm 1 (the speculator's
  * test whether the verify outcome is in its cache) with the cache of

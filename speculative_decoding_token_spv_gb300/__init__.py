@@ -52,6 +52,9 @@ def load_library():
     lib.spv_verify_chain_cached.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, P, P, P, P, P, P, P,
                                             S, P]
     lib.spv_verify_chain_cached.restype = I
+    lib.spv_verify_chain_saguaro.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, ctypes.c_float, P, P,
+                                             P, P, P, P, P, S, P]
+    lib.spv_verify_chain_saguaro.restype = I
     lib.spv_verify_chain_filtered.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, I, ctypes.c_float, P, P, P,
                                               P, P, P, S, P]
     lib.spv_verify_chain_filtered.restype = I
@@ -164,8 +167,19 @@ def spv_verify_chain_cached(target_logits, draft_logits, draft_tokens, r, sample
                          fanout, workspace, out, want_pq, want_resid_norm, want_status, stream)
 
 
+def spv_verify_chain_saguaro(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature: float,
+                             cache_ids, fanout, C: float, *, workspace=None, out=None, want_pq: bool = True,
+                             want_resid_norm: bool = False, want_status: bool = True, stream=None) -> dict:
+    """Verify of Saguaro-sampled drafts (the draft probability of each
+    position's cached candidates divided by C) with the cache lookup; see
+    spv_verify_chain_saguaro in spv.h.  Arguments and outputs as
+    :func:`spv_verify_chain_cached` plus C."""
+    return _verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature, cache_ids,
+                         fanout, workspace, out, want_pq, want_resid_norm, want_status, stream, sag_C=float(C))
+
+
 def _verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature, cache_ids, fanout,
-                  workspace, out, want_pq, want_resid_norm, want_status, stream) -> dict:
+                  workspace, out, want_pq, want_resid_norm, want_status, stream, sag_C=None) -> dict:
     target_logits = _cuda(target_logits, "target_logits")
     dev = target_logits.device
     if target_logits.dim() != 3:
@@ -214,9 +228,14 @@ def _verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, tem
         if "cache_slot" not in out:
             out["cache_slot"] = torch.empty(B, dtype=torch.int32, device=dev)
         f_host = (ctypes.c_int32 * (g + 1))(*F)
-        st = lib.spv_verify_chain_cached(*args, _ptr(cache_ids), ctypes.addressof(f_host), _ptr(out["cache_slot"]),
-                                         *tail)
-        _check(st, "spv_verify_chain_cached")
+        if sag_C is None:
+            st = lib.spv_verify_chain_cached(*args, _ptr(cache_ids), ctypes.addressof(f_host),
+                                             _ptr(out["cache_slot"]), *tail)
+            _check(st, "spv_verify_chain_cached")
+        else:
+            st = lib.spv_verify_chain_saguaro(*args[:10], _ptr(cache_ids), ctypes.addressof(f_host), sag_C, *args[10:],
+                                              _ptr(out["cache_slot"]), *tail)
+            _check(st, "spv_verify_chain_saguaro")
     else:
         st = lib.spv_verify_chain(*args, *tail)
         _check(st, "spv_verify_chain")

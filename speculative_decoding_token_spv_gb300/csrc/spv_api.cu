@@ -56,7 +56,7 @@ spv_status verify_chain_impl(const void *target_logits, const void *draft_logits
                              int gamma, int V, float temperature, int32_t *accept_count, int32_t *out_tokens,
                              float *out_pq, float *out_resid_norm, int32_t *row_status, const int32_t *cache_ids,
                              const int32_t *fanout, int32_t *cache_slot, void *workspace, size_t workspace_bytes,
-                             void *stream)
+                             void *stream, float sag_C = 0.0f)
 {
     if (!dtype_ok(dtype) || !target_logits || !draft_tokens || !accept_count || !out_tokens || !workspace)
         return SPV_ERR_INVALID_ARG;
@@ -94,6 +94,8 @@ spv_status verify_chain_impl(const void *target_logits, const void *draft_logits
     L.cache_ids = cache_ids;
     L.cache_fanout = fanout;
     L.cache_slot = cache_slot;
+    L.sag = sag_C > 0.0f ? 1 : 0;
+    L.sag_C = sag_C;
     const bool rows16 = (static_cast<size_t>(V) * elem_bytes(dtype)) % 16 == 0;
     L.tma = rows16 && aligned16(target_logits) && (greedy || aligned16(draft_logits));
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -126,6 +128,21 @@ spv_status spv_verify_chain_cached(const void *target_logits, const void *draft_
     return verify_chain_impl(target_logits, draft_logits, dtype, draft_tokens, r, sample_keys, B, gamma, V,
                              temperature, accept_count, out_tokens, out_pq, out_resid_norm, row_status, cache_ids,
                              fanout, cache_slot, workspace, workspace_bytes, stream);
+}
+
+spv_status spv_verify_chain_saguaro(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                                    const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys, int B,
+                                    int gamma, int V, float temperature, const int32_t *cache_ids,
+                                    const int32_t *fanout, float C, int32_t *accept_count, int32_t *out_tokens,
+                                    float *out_pq, float *out_resid_norm, int32_t *row_status, int32_t *cache_slot,
+                                    void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!cache_ids || !fanout || !cache_slot) return SPV_ERR_INVALID_ARG;
+    if (!(C > 0.0f) || std::isinf(C) || !(1.0f / C > 0.0f) || std::isinf(1.0f / C)) return SPV_ERR_INVALID_ARG;
+    if (spv::blocks_per_row(V) > 1024) return SPV_ERR_UNSUPPORTED;  // V > 1,048,576
+    return verify_chain_impl(target_logits, draft_logits, dtype, draft_tokens, r, sample_keys, B, gamma, V,
+                             temperature, accept_count, out_tokens, out_pq, out_resid_norm, row_status, cache_ids,
+                             fanout, cache_slot, workspace, workspace_bytes, stream, C);
 }
 
 size_t spv_filtered_workspace_bytes(int B, int gamma, int V)

@@ -53,6 +53,8 @@ struct ChainParams {
     float2 *stats;   // [B*R*nb] (block max of z, sum exp((z - max)/T)); NaN max = bad block
     float *resid;    // [B*nb] residual block masses (direct draw / normaliser only)
     CacheLookup cache;
+    int sag;         // Saguaro sampling: the draft distribution at position i divides its
+    float invC;      // cached candidates' (cache lists) probability by C (invC = 1/C)
 };
 
 constexpr int FW = 16;            // widest chain finalize CTA (warps; one residual trial each per round)
@@ -73,12 +75,20 @@ struct ChainSmem {
     int result;
     float Z;
     uint64_t key;
+    int sag_id[32][64];  // Saguaro: cached candidates of draft position i (-1: none / repeated)
 };
 
 // Barrier of the FWV warps of a chain finalize CTA.
 template <int FWV> __device__ __forceinline__ void fin_sync()
 {
     asm volatile("bar.sync 1, %0;" ::"n"(FWV * 32) : "memory");
+}
+
+// Whether id x is among a Saguaro position's cached candidates (whole warp,
+// same x).
+__device__ __forceinline__ bool sag_member(const int *ids, int x, int lane)
+{
+    return __any_sync(0xffffffffu, ids[lane] == x || ids[32 + lane] == x);
 }
 
 // Residual mass max(0, p(x) - q(x)) from the logits of x: p and q are each
@@ -88,6 +98,15 @@ __device__ __forceinline__ float resid_mass(float zt, float zd, float Mt, float 
 {
     const float p = __fmul_rn(expf((zt - Mt) * invT), it);
     const float q = __fmul_rn(expf((zd - Md) * invT), id);
+    return fmaxf(__fsub_rn(p, q), 0.f);
+}
+
+// The same with the draft probability scaled by wq (Saguaro: 1/C on cached ids).
+__device__ __forceinline__ float resid_mass_w(float zt, float zd, float Mt, float it, float Md, float id, float invT,
+                                              float wq)
+{
+    const float p = __fmul_rn(expf((zt - Mt) * invT), it);
+    const float q = __fmul_rn(__fmul_rn(expf((zd - Md) * invT), id), wq);
     return fmaxf(__fsub_rn(p, q), 0.f);
 }
 
@@ -335,7 +354,7 @@ template <int DT> struct ChainOp {
     // and ids of the winning block (target and draft logits in tb / db).
     __device__ static int race_resid(const Params &P, int b, const unsigned char *tp, const unsigned char *dp, float Mt,
                                      float St, float Md, float Sd, uint64_t key, uint32_t pos, float *tb, float *db,
-                                     int lane)
+                                     const int *sids, int lane)
     {
         float best = INFINITY;
         int bi = INT_MAX;
@@ -365,10 +384,18 @@ template <int DT> struct ChainOp {
         load_block(P, dp, bi, db, lane);
         const float it = 1.f / St, id = 1.f / Sd;
         const int base = bi * G;
+        // Saguaro: bit e of lane l marks a cached id at base + 32 l + e (its q is scaled by 1/C)
+        uint32_t smask = 0u;
+        if (sids) {
+            for (int j = 0; j < 64; ++j) {
+                const int x = sids[j] - base;
+                if (x >= 0 && x < G && (x >> 5) == lane) smask |= 1u << (x & 31);
+            }
+        }
         float ws = 0.f;
         for (int i = 0; i < SUB; ++i) {
-            const int o = SUB * lane + ((i + lane) & (SUB - 1));
-            ws += resid_mass(tb[o], db[o], Mt, it, Md, id, P.invT);
+            const int e = (i + lane) & (SUB - 1), o = SUB * lane + e;
+            ws += resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((smask >> e) & 1u) ? P.invC : 1.f);
         }
         const uint32_t n = static_cast<uint32_t>(base / SUB + lane);
         uint32_t w[4];
@@ -378,7 +405,9 @@ template <int DT> struct ChainOp {
         warp_argmin(A, si);
         const int x = base + SUB * si + lane;
         const int o = SUB * si + lane;
-        const float wx = x < P.V ? resid_mass(tb[o], db[o], Mt, it, Md, id, P.invT) : 0.f;
+        const uint32_t wmask = __shfl_sync(0xffffffffu, smask, si);
+        const float wx =
+            x < P.V ? resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((wmask >> lane) & 1u) ? P.invC : 1.f) : 0.f;
         philox_group(w, key, STREAM_FB_TOKEN, 0, pos, static_cast<uint32_t>(x) >> 2);
         float Ax = wx > 0.f ? arrival(expo(w[x & 3]), 1.f / wx) : INFINITY;
         int xi = x;
@@ -404,7 +433,8 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
     // Residual masses w = max(0, p - q) of one row pair, per block, into
     // P.resid; returns Z = sum w in sm.Z.  All consumer warps.
     __device__ static void residual_pass(const Params &P, int b, const unsigned char *tp, const unsigned char *dp,
-                                         float Mt, float St, float Md, float Sd, Smem &sm, int warp, int lane)
+                                         float Mt, float St, float Md, float Sd, Smem &sm, int warp, int lane, float *tb,
+                                         int k)
     {
         const float it = 1.f / St, id = 1.f / Sd;
         for (int beta = warp; beta < P.nb; beta += FWV) {
@@ -417,10 +447,42 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         }
         fin_sync<FWV>();
         if (warp == 0) {
-            float z = 0.f;
-            for (int beta = lane; beta < P.nb; beta += 32) z += __ldcg(&P.resid[static_cast<size_t>(b) * P.nb + beta]);
-            z = warp_sum(z);
-            if (lane == 0) sm.Z = z;
+            float *rb = P.resid + static_cast<size_t>(b) * P.nb;
+            if (P.sag) {
+                // Saguaro: the cached ids' q is scaled by 1/C; correct their
+                // blocks' masses in a shared copy (in list order: deterministic).
+                for (int beta = lane; beta < P.nb; beta += 32) tb[beta] = __ldcg(&rb[beta]);
+                float dlt[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int x = sm.sag_id[k][32 * h + lane];
+                    dlt[h] = 0.f;
+                    if (x >= 0) {
+                        const float zt = DType<DT>::load(tp, x), zd = DType<DT>::load(dp, x);
+                        dlt[h] = resid_mass_w(zt, zd, Mt, it, Md, id, P.invT, P.invC) -
+                                 resid_mass(zt, zd, Mt, it, Md, id, P.invT);
+                    }
+                }
+                __syncwarp();
+                for (int j = 0; j < 64; ++j) {
+                    const float dj = __shfl_sync(0xffffffffu, dlt[j >> 5], j & 31);
+                    const int x = sm.sag_id[k][j];
+                    if (lane == 0 && x >= 0) tb[x / G] += dj;
+                }
+                __syncwarp();
+                float z = 0.f;
+                for (int beta = lane; beta < P.nb; beta += 32) {
+                    rb[beta] = tb[beta];
+                    z += tb[beta];
+                }
+                z = warp_sum(z);
+                if (lane == 0) sm.Z = z;
+            } else {
+                float z = 0.f;
+                for (int beta = lane; beta < P.nb; beta += 32) z += __ldcg(&rb[beta]);
+                z = warp_sum(z);
+                if (lane == 0) sm.Z = z;
+            }
         }
         fin_sync<FWV>();
     }
@@ -469,6 +531,43 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             }
         }
         if (warp == 1) cache_prefetch(P.cache, b, lane);
+        // Saguaro: each warp stages the cached ids of its draft positions
+        // (repeats and ids outside [0, V) dropped) and their draft logits.
+        constexpr int SAG_PER_WARP = (32 + FWV - 1) / FWV;
+        float sz[SAG_PER_WARP][2];
+        if (P.sag) {
+#pragma unroll
+            for (int u = 0; u < SAG_PER_WARP; ++u) {
+                const int i = warp + u * FWV;
+                sz[u][0] = sz[u][1] = 0.f;
+                if (i < g) {
+                    const int o0 = P.cache.off[i], F = P.cache.off[i + 1] - o0;
+                    const int32_t *ids = P.cache.ids + static_cast<size_t>(b) * P.cache.n + o0;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = 32 * h + lane;
+                        int x = j < F ? ids[j] : -1;
+                        if (x < 0 || x >= P.V) x = -1;
+                        sm.sag_id[i][j] = x;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int j = 32 * h + lane;
+                        const int x = sm.sag_id[i][j];
+                        bool rep = false;
+                        for (int j2 = 0; j2 < j && x >= 0; ++j2) rep |= sm.sag_id[i][j2] == x;
+                        if (x >= 0 && !rep) sz[u][h] = DType<DT>::load(row_of(P, b, g + 1 + i), x);
+                        else sz[u][h] = -INFINITY;
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (sz[u][h] == -INFINITY) sm.sag_id[i][32 * h + lane] = -1;
+                    __syncwarp();
+                }
+            }
+        }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
@@ -534,12 +633,34 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             write_bad_row(P, b, warp, lane);
             return;
         }
+        if (P.sag) {
+            // Saguaro: q_C's normaliser S - (1 - 1/C) * sum over the cached ids (at least S / C)
+#pragma unroll
+            for (int u = 0; u < SAG_PER_WARP; ++u) {
+                const int i = warp + u * FWV;
+                if (i < g) {
+                    const float Md = sm.M[g + 1 + i], Sd = sm.S[g + 1 + i];
+                    float c = 0.f;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h)
+                        if (sz[u][h] != -INFINITY) c += expf((sz[u][h] - Md) * P.invT);
+                    c = warp_sum(c);
+                    if (lane == 0) sm.S[g + 1 + i] = fmaxf(Sd - (1.f - P.invC) * c, Sd * P.invC);
+                }
+            }
+            fin_sync<FWV>();
+        }
         // C. Accept tests for every draft position; first rejection by ballot.
         if (warp == 0) {
             bool acc = false;
             if (lane < g) {
                 const float p = expf((sm.zt[lane] - sm.M[lane]) * P.invT) / sm.S[lane];
-                const float q = expf((sm.zd[lane] - sm.M[g + 1 + lane]) * P.invT) / sm.S[g + 1 + lane];
+                float q = expf((sm.zd[lane] - sm.M[g + 1 + lane]) * P.invT) / sm.S[g + 1 + lane];
+                if (P.sag) {
+                    bool in = false;
+                    for (int j = 0; j < 64; ++j) in |= sm.sag_id[lane][j] == sm.x[lane];
+                    if (in) q = __fmul_rn(q, P.invC);
+                }
                 acc = (p > 0.f) && (sm.rr[lane] * q <= p);
                 if (P.out_pq) {
                     P.out_pq[(static_cast<size_t>(b) * g + lane) * 2] = p;
@@ -581,10 +702,11 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 uint32_t aw = 0;
                 const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), key, STREAM_SUB, STREAM_TOKEN, t,
                                               static_cast<uint32_t>(k), lane, STREAM_ACCEPT, &aw);
+                const float wq = (P.sag && sag_member(sm.sag_id[k], x, lane)) ? P.invC : 1.f;
                 if (lane == 0) {
                     const float v = uniform24(aw);
                     const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
-                    const float q = expf((db[x - beta * G] - Md) * P.invT) / Sd;
+                    const float q = __fmul_rn(expf((db[x - beta * G] - Md) * P.invT) / Sd, wq);
                     sm.trial_x[warp] = x;
                     sm.trial_acc[warp] = (q <= (1.0f - v) * p) ? 1 : 0;
                 }
@@ -601,10 +723,11 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             }
             const bool fallback = sm.result < 0;
             if (fallback || P.out_Z) {
-                residual_pass(P, b, tp, dp, Mt, St, Md, Sd, sm, warp, lane);
+                residual_pass(P, b, tp, dp, Mt, St, Md, Sd, sm, warp, lane, tb, k);
                 if (fallback) {
                     if (warp == 0) {
-                        const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(k), tb, db, lane);
+                        const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(k), tb, db,
+                                                 P.sag ? sm.sag_id[k] : nullptr, lane);
                         if (lane == 0) sm.result = x;
                     }
                     fin_sync<FWV>();
@@ -847,6 +970,8 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
     P.out_Z = L.out_Z;
     P.row_status = L.row_status;
     fill_cache(P.cache, L);
+    P.sag = L.sag;
+    P.invC = L.sag ? 1.0f / L.sag_C : 1.0f;
     // One finalize CTA per sequence: the 16-warp CTA (one per SM) while the
     // sequences fit on the SMs at once, else the 8-warp CTA (two per SM).
     int sms = 0;

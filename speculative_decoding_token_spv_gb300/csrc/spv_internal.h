@@ -35,6 +35,10 @@ struct ChainLaunch {
     // Top-k / top-p filter (spv_verify_chain_filtered only).
     int top_k;
     float top_p;
+    // Saguaro sampling (spv_verify_chain_saguaro only): the cache lists are
+    // the cached candidates whose draft probability was divided by sag_C.
+    int sag;
+    float sag_C;
 };
 
 struct FanoutLaunch {

@@ -25,6 +25,7 @@ then cast to the workload dtype; V is the last, contiguous axis.
 """
 from __future__ import annotations
 
+import math
 from dataclasses import dataclass, field
 
 import torch
@@ -176,3 +177,23 @@ def fanout(device="cpu", B=8, K=4, V=128256, fanout_sizes=(8, 7, 6, 5, 4)) -> Fa
         probs = torch.softmax(d[:, :K].reshape(B * K, V), dim=1)
         ex[:, :K] = torch.multinomial(probs, 1, generator=_gen(device, s_x)).to(torch.int32).reshape(B, K)
     return FanoutInputs("fanout", d, ex, list(fanout_sizes))
+
+
+def saguaro_tokens(w: ChainInputs, cache_ids: torch.Tensor, fanout, C: float, seed: int = 9) -> torch.Tensor:
+    """The draft's Saguaro sampler (input generation): at position i draw from
+    softmax(draft_i / T) with the probability of position i's listed
+    candidates (cache_ids [B, sum F], k-major) divided by C."""
+    B, g, V = w.draft.shape
+    logits = w.draft.float() / w.temperature
+    offs = [0]
+    for f in fanout:
+        offs.append(offs[-1] + int(f))
+    for i in range(g):
+        ids = cache_ids[:, offs[i]:offs[i + 1]].long()
+        ok = (ids >= 0) & (ids < V)
+        pen = torch.zeros(B, V, device=logits.device)
+        pen.scatter_(1, ids.clamp(0, V - 1), torch.where(ok, -math.log(C), 0.0).float())
+        logits[:, i] += pen
+    probs = torch.softmax(logits.reshape(B * g, V), dim=1)
+    gen = _gen(w.draft.device, seed)
+    return torch.multinomial(probs, 1, generator=gen).to(torch.int32).reshape(B, g)

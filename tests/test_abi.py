@@ -153,3 +153,28 @@ def test_filtered_verify_arguments_rejected_on_host(lib):
     n = spv.spv_filtered_workspace_bytes(64, 4, 151936)
     assert n >= 64 * 9 * 19 * 64 * 8 and n >= spv.spv_greedy_workspace_bytes(64, 4, 151936)
     assert spv.spv_filtered_workspace_bytes(0, 4, 100) == 0
+
+
+def test_saguaro_arguments_rejected_on_host(lib):
+    """spv_verify_chain_saguaro: C > 0 finite, cache arguments required,
+    vocabularies up to 1,048,576."""
+    P = ctypes.c_void_p
+    fake = P(4096)
+    ws = P(1 << 20)
+    big = 1 << 40
+    f_ok = (ctypes.c_int32 * 5)(8, 7, 6, 5, 4)
+    ok_args = dict(t=fake, d=fake, dt=0, tok=fake, r=fake, keys=fake, B=4, g=4, V=1000, T=1.0, ids=fake,
+                   fan=ctypes.cast(f_ok, P), C=2.0, acc=fake, out=fake, pq=None, z=None, st=None, slot=fake, ws=ws,
+                   wsb=big, stream=None)
+
+    def call(**kw):
+        a = dict(ok_args, **kw)
+        return lib.spv_verify_chain_saguaro(a["t"], a["d"], a["dt"], a["tok"], a["r"], a["keys"], a["B"], a["g"],
+                                            a["V"], ctypes.c_float(a["T"]), a["ids"], a["fan"], ctypes.c_float(a["C"]),
+                                            a["acc"], a["out"], a["pq"], a["z"], a["st"], a["slot"], a["ws"], a["wsb"],
+                                            a["stream"])
+
+    for kw in (dict(C=0.0), dict(C=-2.0), dict(C=float("inf")), dict(C=float("nan")), dict(C=1e-45), dict(ids=None),
+               dict(fan=None), dict(slot=None), dict(t=None), dict(g=0)):
+        assert call(**kw) == 1, kw
+    assert call(V=2_000_000) == 3

@@ -73,6 +73,8 @@ def _load():
         lib.spvo_verify_saguaro_batch.argtypes = [P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                   ctypes.c_int, ctypes.c_double, P, P, ctypes.c_int, ctypes.c_double,
                                                   P, P, P, P, P, P, P]
+        lib.spvo_verify_tree_batch.argtypes = [P, P, P, P, P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_double, P, P, P, P, P, P]
         lib.spvo_verify_greedy_batch.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  P, P, P]
         _lib = lib
@@ -242,6 +244,34 @@ def verify_saguaro(target, draft, tokens, r, keys, temperature: float, cache_ids
     _run_ranges(run, B, threads)
     if want_Z:
         out["Z"] = Z
+    return out
+
+
+def verify_tree(target, draft, parent, tokens, r, keys, temperature: float, threads: int | None = None) -> dict:
+    """Tree verify (multi-round speculative sampling; greedy at T == 0).
+    target, draft [B, N, V] (row v: p, q at node v); parent [B, N] (-1 at the
+    root, parent[v] < v); tokens [B, N] (node v's token); r [B, N]; keys [B].
+    Returns accept_count [B], out_tokens [B, N], out_nodes [B, N], margin,
+    trials, status."""
+    target = _f32(target)
+    B, N, V = target.shape
+    draft = _f32(draft) if temperature > 0 else target
+    parent = np.ascontiguousarray(np.asarray(parent, dtype=np.int32)).reshape(B, N)
+    tokens = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32)).reshape(B, N)
+    r = _f32(r).reshape(B, N) if r is not None else np.ones((B, N), np.float32)
+    keys = np.ascontiguousarray(np.asarray(keys if keys is not None else np.zeros(B), dtype=np.uint64)).reshape(B)
+    out = dict(accept_count=np.zeros(B, np.int32), out_tokens=np.zeros((B, N), np.int32),
+               out_nodes=np.zeros((B, N), np.int32), margin=np.zeros(B), trials=np.zeros(B, np.int32),
+               status=np.zeros(B, np.int32))
+    lib = _load()
+
+    def run(b0, b1):
+        lib.spvo_verify_tree_batch(_ptr(target), _ptr(draft), _ptr(parent), _ptr(tokens), _ptr(r), _ptr(keys), b0, b1,
+                                   N, V, float(temperature), _ptr(out["accept_count"]), _ptr(out["out_tokens"]),
+                                   _ptr(out["out_nodes"]), _ptr(out["margin"]), _ptr(out["trials"]),
+                                   _ptr(out["status"]))
+
+    _run_ranges(run, B, threads)
     return out
 
 

@@ -697,6 +697,165 @@ void spvo_verify_saguaro_batch(const float *tgt, const float *drf, const int32_t
 }
 
 /* ------------------------------------------------------------------------ */
+/* Tree verify.  The pages name draft trees ([SPD] tree drafting of width 4;
+ * tree-style verification with k = 21 in the benchmark study the survey
+ * page cites) but give no verification rule.  This follows the published
+ * multi-round speculative sampling for token trees (Miao et al., SpecInfer,
+ * stochastic verification), restated: the children of node u were drawn
+ * i.i.d. from q_u and are tested in index order against a residual that
+ * shrinks with every rejection,
+ *   P_0 = p_u,  P_m(x) = max(0, p_u(x) - s_m q_u(x)) / N_m,
+ *   s_0 = 0, s_{m+1} = s_m + N_m, N_0 = 1, N_m = sum_x max(0, p_u - s_m q_u),
+ * child c (token x) being accepted iff P_m(x) > 0 and r_c q_u(x) <= P_m(x).
+ * The walk descends into the first accepted child; when every child of u is
+ * rejected (m = number of children) one token is drawn from P_m, and at a
+ * leaf the bonus token from p_u.  With one child per node this is [SD]
+ * steps 3 and 4 exactly (s_1 = 1: the residual max(0, p - q)).
+ * Draws use the race and rejection trials of the chain (trial t accepts x ~
+ * p_u iff s_m q_u(x) <= (1 - v) p_u(x)), position = the node's index.
+ * Inputs: tgt, drf [N * V] (row v: p, q at node v), parent [N] (parent[0] =
+ * -1, 0 <= parent[v] < v), tok [N] (token of node v >= 1), r [N].
+ * Outputs: k (accepted nodes), tokens_out [N] (their tokens, then the drawn
+ * one, then -1), nodes_out [N] (the accepted nodes, then -1). */
+static int tree_trials(const double *w, const float *dj, int V, double T, double Md, double Sd, double sres,
+                       uint64_t key, uint32_t pos, double *margin, int *trials)
+{
+    int t;
+    for (t = 0; t < SPVO_MAX_TRIALS; ++t) {
+        int x = race_sample(w, V, key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, (uint32_t)t, pos, margin);
+        double v = spvo_uniform(key, SPVO_STREAM_ACCEPT, (uint32_t)t, pos, 0);
+        double p = w[x], q = sres * prob(dj, x, T, Md, Sd);
+        note_margin(margin, fabs((1.0 - v) - q / p));
+        if (q <= (1.0 - v) * p) { *trials = t + 1; return x; }
+    }
+    *trials = SPVO_MAX_TRIALS + 1;
+    return -1;
+}
+
+int spvo_verify_tree_seq(const float *tgt, const float *drf, const int32_t *parent, const int32_t *tok, const float *r,
+                         uint64_t seq_key, int N, int V, double T, int32_t *k_out, int32_t *tokens_out,
+                         int32_t *nodes_out, double *margin_out, int32_t *trials_out)
+{
+    for (int i = 0; i < N; ++i) { tokens_out[i] = -1; nodes_out[i] = -1; }
+    *k_out = -1;
+    *margin_out = INFINITY;
+    *trials_out = 0;
+    if (N < 1 || parent[0] != -1) return SPVO_BAD_ROW;
+    for (int v = 1; v < N; ++v)
+        if (parent[v] < 0 || parent[v] >= v || tok[v] < 0 || tok[v] >= V) return SPVO_BAD_ROW;
+    double margin = INFINITY;
+    double *w = (double *)malloc(sizeof(double) * (size_t)V);
+    int u = 0, k = 0, emitted = -1, total_trials = 0;
+    for (;;) {
+        const float *tu = tgt + (size_t)u * V, *du = drf + (size_t)u * V;
+        double Mt, St;
+        if (spvo_softmax_stats(tu, V, T, &Mt, &St) != SPVO_OK) { free(w); return SPVO_BAD_ROW; }
+        int nkids = 0;
+        for (int c = u + 1; c < N; ++c) nkids += parent[c] == u;
+        for (int x = 0; x < V; ++x) w[x] = prob(tu, x, T, Mt, St);
+        if (nkids == 0) { /* leaf: the bonus token from p_u */
+            emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,
+                                  (uint32_t)u, &margin);
+            break;
+        }
+        double Md, Sd;
+        if (spvo_softmax_stats(du, V, T, &Md, &Sd) != SPVO_OK) { free(w); return SPVO_BAD_ROW; }
+        double s = 0.0, Nm = 1.0;
+        int next = -1;
+        for (int c = u + 1; c < N && next < 0; ++c) {
+            if (parent[c] != u) continue;
+            const int x = tok[c];
+            const double px = w[x], qx = prob(du, x, T, Md, Sd);
+            const double Pm = (s == 0.0) ? px : (px - s * qx > 0 ? (px - s * qx) / Nm : 0.0);
+            note_margin(&margin, (qx > 0) ? fabs((double)r[c] - Pm / qx) : INFINITY);
+            if (Pm > 0 && (double)r[c] * qx <= Pm) { next = c; break; }
+            /* rejected: the next residual */
+            s += Nm;
+            ksum Z = { 0, 0 };
+            for (int y = 0; y < V; ++y) {
+                double d = w[y] - s * prob(du, y, T, Md, Sd);
+                if (d > 0) ksum_add(&Z, d);
+            }
+            Nm = ksum_val(&Z);
+            if (!(Nm > 0)) { free(w); return SPVO_BAD_ROW; } /* no residual mass (token outside q's support) */
+        }
+        if (next >= 0) {
+            tokens_out[k] = tok[next];
+            nodes_out[k] = next;
+            ++k;
+            u = next;
+            continue;
+        }
+        /* every child rejected: one draw from P_m = max(0, p - s q) / N_m */
+        int tr = 0;
+        emitted = tree_trials(w, du, V, T, Md, Sd, s, seq_key, (uint32_t)u, &margin, &tr);
+        total_trials = tr;
+        if (emitted < 0) {
+            for (int y = 0; y < V; ++y) {
+                double d = w[y] - s * prob(du, y, T, Md, Sd);
+                w[y] = d > 0 ? d : 0.0;
+            }
+            emitted = race_sample(w, V, seq_key, SPVO_STREAM_FB_BLOCK, SPVO_STREAM_FB_SUB, SPVO_STREAM_FB_TOKEN, 0,
+                                  (uint32_t)u, &margin);
+        }
+        break;
+    }
+    free(w);
+    tokens_out[k] = emitted;
+    *k_out = k;
+    *margin_out = margin;
+    *trials_out = total_trials;
+    return SPVO_OK;
+}
+
+/* Greedy tree verify (T = 0): descend into the first child whose token is
+ * the argmax of p_u (lowest id on ties); emit the argmax of the last node. */
+int spvo_verify_tree_greedy_seq(const float *tgt, const int32_t *parent, const int32_t *tok, int N, int V,
+                                int32_t *k_out, int32_t *tokens_out, int32_t *nodes_out)
+{
+    for (int i = 0; i < N; ++i) { tokens_out[i] = -1; nodes_out[i] = -1; }
+    *k_out = -1;
+    if (N < 1 || parent[0] != -1) return SPVO_BAD_ROW;
+    for (int v = 1; v < N; ++v)
+        if (parent[v] < 0 || parent[v] >= v || tok[v] < 0 || tok[v] >= V) return SPVO_BAD_ROW;
+    int u = 0, k = 0, a;
+    for (;;) {
+        if (argmax_row(tgt + (size_t)u * V, V, &a) != SPVO_OK) return SPVO_BAD_ROW;
+        int next = -1;
+        for (int c = u + 1; c < N; ++c)
+            if (parent[c] == u && tok[c] == a) { next = c; break; }
+        if (next < 0) break;
+        tokens_out[k] = tok[next];
+        nodes_out[k] = next;
+        ++k;
+        u = next;
+    }
+    tokens_out[k] = a;
+    *k_out = k;
+    return SPVO_OK;
+}
+
+void spvo_verify_tree_batch(const float *tgt, const float *drf, const int32_t *parent, const int32_t *tok,
+                            const float *r, const uint64_t *keys, int b0, int b1, int N, int V, double T,
+                            int32_t *k_out, int32_t *tokens_out, int32_t *nodes_out, double *margin_out,
+                            int32_t *trials_out, int32_t *status_out)
+{
+    for (int b = b0; b < b1; ++b) {
+        const size_t o = (size_t)b * N;
+        if (T == 0.0) {
+            status_out[b] = spvo_verify_tree_greedy_seq(tgt + o * V, parent + o, tok + o, N, V, &k_out[b],
+                                                        tokens_out + o, nodes_out + o);
+            margin_out[b] = INFINITY;
+            trials_out[b] = 0;
+        } else {
+            status_out[b] = spvo_verify_tree_seq(tgt + o * V, drf + o * V, parent + o, tok + o, r + o, keys[b], N, V, T,
+                                                 &k_out[b], tokens_out + o, nodes_out + o, &margin_out[b],
+                                                 &trials_out[b]);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
 /* Speculation-cache lookup, [SSD] Algorithm 1 ("if verify_outcome in cache")
  * and Figure 2: the cache holds one branch per (k, t) pair, for every
  * position k = 0..K and each of the F_k fan-out candidates t listed for it,

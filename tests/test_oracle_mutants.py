@@ -72,6 +72,9 @@ MUTANTS = {
     "saguaro_normaliser_unweighted": ("exp((double)d[x] / T - M) * (inS[(size_t)i * V + x] ? invC : 1.0));",
                                       "exp((double)d[x] / T - M));",
                                       ["test_saguaro_draft_probabilities"]),
+    "tree_shift_by_one": ("            s += Nm;\n", "            s += 1.0;\n", ["test_tree_root_acceptance_closed_form"]),
+    "tree_residual_unnormalised": ("(px - s * qx) / Nm : 0.0);", "(px - s * qx) : 0.0);",
+                                   ["test_tree_root_acceptance_closed_form"]),
     "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
                        ["test_fanout_sizes_golden"]),
 }
@@ -85,6 +88,8 @@ def _calls(name):
         return [lambda: fn(None), lambda: fn(8)]
     if name == "test_filter_row_vs_torch_topk_softmax":
         return [lambda: fn(1.0)]
+    if name == "test_tree_root_acceptance_closed_form":
+        return [lambda: fn(2), lambda: fn(4)]
     if name == "test_saguaro_draft_probabilities":
         return [lambda: fn(2.0), lambda: fn(8.0)]
     if name == "test_filtered_acceptance_rate_is_one_minus_tvd":

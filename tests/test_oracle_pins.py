@@ -862,3 +862,127 @@ def test_saguaro_hit_rate_grows_with_C():
         out = oracle.verify_saguaro(z, d, tok, r, _keys(B, 53 + int(C)), 1.0, ids, F, C)
         hits = (oracle.cache_slots(out["accept_count"], out["out_tokens"], ids, F) >= 0).mean()
         assert abs(hits - want) < 5 * np.sqrt(want * (1 - want) / B), (C, hits, want)
+
+
+# ----------------------------------------------------------------- tree verify
+def _tree_star(B, W, V, rng, z_std=1.5, noise=1.0, depth2=0):
+    """Root with W children drawn i.i.d. from q_root; with depth2 > 0 each
+    child gets that many children drawn from its own q."""
+    zl = rng.normal(0, z_std, V).astype(np.float32)
+    dl = (zl + rng.normal(0, noise, V)).astype(np.float32)
+    N = 1 + W + W * depth2
+    z = np.zeros((B, N, V), np.float32)
+    d = np.zeros((B, N, V), np.float32)
+    parent = np.full((B, N), -1, np.int32)
+    tok = np.zeros((B, N), np.int32)
+    q0 = _probs(dl)
+    for b in range(B):
+        z[b, 0], d[b, 0] = zl, dl
+    for j in range(W):
+        v = 1 + j
+        parent[:, v] = 0
+        tok[:, v] = rng.choice(V, size=B, p=q0)
+        cz = rng.normal(0, z_std, V).astype(np.float32)
+        cd = (cz + rng.normal(0, noise, V)).astype(np.float32)
+        z[:, v], d[:, v] = cz, cd
+        for h in range(depth2):
+            w2 = 1 + W + j * depth2 + h
+            parent[:, w2] = v
+            tok[:, w2] = rng.choice(V, size=B, p=_probs(cd))
+            z[:, w2] = rng.normal(0, z_std, V).astype(np.float32)
+            d[:, w2] = z[:, w2]
+    r = (1 - rng.random((B, N))).astype(np.float32)
+    return z, d, parent, tok, r
+
+
+def test_tree_path_is_the_chain():
+    """A tree that is a single path is the chain: identical outputs."""
+    rng = np.random.default_rng(70)
+    B, g, V = 400, 4, 300
+    z = rng.normal(0, 2, (B, g + 1, V)).astype(np.float32)
+    d = (z[:, :g] + rng.normal(0, 1, (B, g, V))).astype(np.float32)
+    tok = np.stack([np.array([rng.choice(V, p=_probs(d[b, i])) for b in range(B)]) for i in range(g)], 1).astype(np.int32)
+    r = (1 - rng.random((B, g))).astype(np.float32)
+    keys = _keys(B, 71)
+    ref = oracle.verify_chain(z, d, tok, r, keys, 1.0)
+    dt = np.concatenate([d, np.zeros((B, 1, V), np.float32)], axis=1)
+    parent = np.tile(np.arange(-1, g, dtype=np.int32), (B, 1))
+    ttok = np.concatenate([np.zeros((B, 1), np.int32), tok], axis=1)
+    tr = np.concatenate([np.ones((B, 1), np.float32), r], axis=1)
+    out = oracle.verify_tree(z, dt, parent, ttok, tr, keys, 1.0)
+    assert np.array_equal(out["accept_count"], ref["accept_count"])
+    assert np.array_equal(out["out_tokens"], ref["out_tokens"])
+    assert np.array_equal(out["trials"], ref["trials"])
+    k = out["accept_count"]
+    assert all(list(out["out_nodes"][b, :k[b]]) == list(range(1, k[b] + 1)) for b in range(B))
+
+
+@pytest.mark.parametrize("W", [2, 4])
+def test_tree_root_acceptance_closed_form(W):
+    """Children drawn i.i.d. from q: child m is accepted with probability
+    sum min(P_m, q), P_0 = p, P_{m+1} = norm(max(0, P_m - q)) (normalising
+    after every step), so P(no child accepted) = prod_m (1 - alpha_m)."""
+    rng = np.random.default_rng(72)
+    B, V = 30000, 80
+    z, d, parent, tok, r = _tree_star(B, W, V, rng)
+    p, q = _probs(z[0, 0]), _probs(d[0, 0])
+    none, P = 1.0, p.copy()
+    for m in range(W):
+        alpha = np.minimum(P, q).sum()
+        none *= 1 - alpha
+        P = np.maximum(P - q, 0)
+        P /= P.sum()
+    out = oracle.verify_tree(z, d, parent, tok, r, _keys(B, 73), 1.0)
+    emp = (out["accept_count"] == 0).mean()
+    assert abs(emp - none) < 5 * np.sqrt(none * (1 - none) / B), (emp, none)
+
+
+@pytest.mark.parametrize("W", [3, 4])
+def test_tree_first_token_is_exact(W):
+    """With W children drawn i.i.d. from q_root the first emitted token is
+    distributed as p_root (chi-square)."""
+    rng = np.random.default_rng(74 + W)
+    B, V = 30000, 120
+    z, d, parent, tok, r = _tree_star(B, W, V, rng, noise=1.3)
+    out = oracle.verify_tree(z, d, parent, tok, r, _keys(B, 75), 1.0)
+    ok, pv = _chi2_ok(np.bincount(out["out_tokens"][:, 0], minlength=V), _probs(z[0, 0]))
+    assert ok, pv
+
+
+def test_tree_second_token_given_first_child():
+    """Two levels: given that root child c was accepted, the next emitted
+    token is distributed as p_c (chi-square over the sequences that took
+    child 1)."""
+    rng = np.random.default_rng(77)
+    B, V, W = 40000, 60, 3
+    z, d, parent, tok, r = _tree_star(B, W, V, rng, noise=0.9, depth2=2)
+    out = oracle.verify_tree(z, d, parent, tok, r, _keys(B, 78), 1.0)
+    took1 = (out["accept_count"] >= 1) & (out["out_nodes"][:, 0] == 1)
+    second = out["out_tokens"][took1, 1]
+    ok, pv = _chi2_ok(np.bincount(second, minlength=V), _probs(z[0, 1]))
+    assert ok and took1.sum() > 3000, (pv, took1.sum())
+
+
+def test_tree_greedy_walk():
+    """T = 0: descend into the first child whose token is the argmax
+    (numpy argmax, first occurrence); emit the last node's argmax."""
+    rng = np.random.default_rng(79)
+    B, N, V = 200, 9, 40
+    z = rng.integers(-3, 4, (B, N, V)).astype(np.float32)
+    parent = np.array([-1, 0, 0, 0, 1, 1, 2, 4, 4], np.int32)
+    P_ = np.tile(parent, (B, 1))
+    a = np.argmax(z, axis=2)
+    tok = np.where(rng.random((B, N)) < 0.6, a[:, np.maximum(parent, 0)], rng.integers(0, V, (B, N))).astype(np.int32)
+    out = oracle.verify_tree(z, None, P_, tok, None, None, 0.0)
+    for b in range(B):
+        u, k, path = 0, 0, []
+        while True:
+            nxt = [c for c in range(u + 1, N) if parent[c] == u and tok[b, c] == a[b, u]]
+            if not nxt:
+                break
+            path.append(nxt[0])
+            u = nxt[0]
+        assert out["accept_count"][b] == len(path)
+        assert list(out["out_nodes"][b, :len(path)]) == path
+        assert list(out["out_tokens"][b, :len(path)]) == [tok[b, c] for c in path]
+        assert out["out_tokens"][b, len(path)] == a[b, u]

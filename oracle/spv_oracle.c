@@ -743,6 +743,17 @@ int spvo_verify_tree_seq(const float *tgt, const float *drf, const int32_t *pare
     if (N < 1 || parent[0] != -1) return SPVO_BAD_ROW;
     for (int v = 1; v < N; ++v)
         if (parent[v] < 0 || parent[v] >= v || tok[v] < 0 || tok[v] >= V) return SPVO_BAD_ROW;
+    /* Every target row, and the draft row of every node with children, must
+     * be a distribution, whether or not the walk reaches it: the outcome of a
+     * sequence does not depend on where its bad rows sit. */
+    for (int v = 0; v < N; ++v) {
+        double M, S;
+        if (spvo_softmax_stats(tgt + (size_t)v * V, V, T, &M, &S) != SPVO_OK) return SPVO_BAD_ROW;
+    }
+    for (int v = 1; v < N; ++v) {
+        double M, S;
+        if (spvo_softmax_stats(drf + (size_t)parent[v] * V, V, T, &M, &S) != SPVO_OK) return SPVO_BAD_ROW;
+    }
     double margin = INFINITY;
     double *w = (double *)malloc(sizeof(double) * (size_t)V);
     int u = 0, k = 0, emitted = -1, total_trials = 0;
@@ -815,10 +826,13 @@ int spvo_verify_tree_greedy_seq(const float *tgt, const int32_t *parent, const i
 {
     for (int i = 0; i < N; ++i) { tokens_out[i] = -1; nodes_out[i] = -1; }
     *k_out = -1;
+    int a;
     if (N < 1 || parent[0] != -1) return SPVO_BAD_ROW;
     for (int v = 1; v < N; ++v)
         if (parent[v] < 0 || parent[v] >= v || tok[v] < 0 || tok[v] >= V) return SPVO_BAD_ROW;
-    int u = 0, k = 0, a;
+    for (int v = 0; v < N; ++v) /* every target row, reached or not (as in the sampled walk) */
+        if (argmax_row(tgt + (size_t)v * V, V, &a) != SPVO_OK) return SPVO_BAD_ROW;
+    int u = 0, k = 0;
     for (;;) {
         if (argmax_row(tgt + (size_t)u * V, V, &a) != SPVO_OK) return SPVO_BAD_ROW;
         int next = -1;

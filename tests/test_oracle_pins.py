@@ -986,3 +986,30 @@ def test_tree_greedy_walk():
         assert list(out["out_nodes"][b, :len(path)]) == path
         assert list(out["out_tokens"][b, :len(path)]) == [tok[b, c] for c in path]
         assert out["out_tokens"][b, len(path)] == a[b, u]
+
+
+def test_tree_bad_rows_anywhere():
+    """A bad target row, or a bad draft row of a node with children, makes the
+    sequence bad wherever it sits, reached by the walk or not; the draft row
+    of a leaf is never read."""
+    rng = np.random.default_rng(76)
+    B, V = 6, 50
+    parent = np.tile(np.array([-1, 0, 0, 1, 2], np.int32), (B, 1))
+    N = parent.shape[1]
+    z = rng.normal(0, 1, (B, N, V)).astype(np.float32)
+    d = rng.normal(0, 1, (B, N, V)).astype(np.float32)
+    tok = rng.integers(0, V, (B, N)).astype(np.int32)
+    r = np.ones((B, N), np.float32)
+    keys = _keys(B, 77)
+    z[1, 4, 3] = np.nan          # target row of a leaf
+    d[2, 2, 0] = np.inf          # draft row of an internal node
+    d[3, 3, :] = np.nan          # draft row of a leaf: not read
+    d[3, 4, :] = -np.inf
+    tok[4, 2] = V                # token out of range
+    parent[5, 3] = 3             # parent not before the node
+    out = oracle.verify_tree(z, d, parent, tok, r, keys, 1.0)
+    assert list(np.nonzero(out["status"])[0]) == [1, 2, 4, 5]
+    assert (out["accept_count"][[1, 2, 4, 5]] == -1).all()
+    assert (out["out_tokens"][[1, 2, 4, 5]] == -1).all()
+    g = oracle.verify_tree(z, None, parent, tok, None, None, 0.0)
+    assert list(np.nonzero(g["status"])[0]) == [1, 4, 5]

@@ -625,17 +625,17 @@ int spvo_verify_saguaro_seq(const float *tgt, const float *drf, const int32_t *t
         double q = sag_prob(drf + (size_t)i * V, inS + (size_t)i * V, tok[i], T, Md[i], Sd[i], invC);
         pq_out[2 * i] = p;
         pq_out[2 * i + 1] = q;
-        int stands = (p > 0) && ((double)r[i] * q <= p);
+        int holds = (p > 0) && ((double)r[i] * q <= p);
         if (i < k) {
             note_margin(&margin, (q > 0) ? fabs((double)r[i] - p / q) : INFINITY);
-            if (!stands) k = i;
+            if (!holds) k = i;
         }
     }
     double *w = (double *)malloc(sizeof(double) * (size_t)V);
     int emitted;
     if (k == gamma) {
-        const float *tb = tgt + (size_t)gamma * V;
-        for (int x = 0; x < V; ++x) w[x] = prob(tb, x, T, Mt[gamma], St[gamma]);
+        const float *last = tgt + (size_t)gamma * V;
+        for (int x = 0; x < V; ++x) w[x] = prob(last, x, T, Mt[gamma], St[gamma]);
         emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,
                               (uint32_t)gamma, &margin);
         if (Z_out) *Z_out = 1.0;
@@ -651,7 +651,10 @@ int spvo_verify_saguaro_seq(const float *tgt, const float *drf, const int32_t *t
             double v = spvo_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
             double p = w[x], q = sag_prob(dj, sj, x, T, Md[k], Sd[k], invC);
             note_margin(&margin, fabs((1.0 - v) - q / p));
-            if (q <= (1.0 - v) * p) { emitted = x; break; }
+            if (q <= (1.0 - v) * p) {
+                emitted = x;
+                break;
+            }
         }
         *trials_out = (emitted >= 0) ? t + 1 : SPVO_MAX_TRIALS + 1;
         for (int x = 0; x < V; ++x) {

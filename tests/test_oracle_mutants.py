@@ -66,6 +66,15 @@ MUTANTS = {
     "filtered_accept_transposed": ("int stands = (p > 0) && ((double)r[i] * q <= p);",
                                    "int stands = (p > 0) && ((double)r[i] * p <= q);",
                                    ["test_filtered_acceptance_rate_is_one_minus_tvd"]),
+    "saguaro_accept_transposed": ("int holds = (p > 0) && ((double)r[i] * q <= p);",
+                                  "int holds = (p > 0) && ((double)r[i] * p <= q);",
+                                  ["test_saguaro_preserves_the_target_distribution"]),
+    "saguaro_bonus_wrong_row": ("const float *last = tgt + (size_t)gamma * V;",
+                                "const float *last = tgt + (size_t)(gamma - 1) * V;",
+                                ["test_saguaro_C1_is_plain_chain"]),
+    "saguaro_trial_accept_inverted": ("if (q <= (1.0 - v) * p) {\n                emitted = x;",
+                                      "if (p <= (1.0 - v) * q) {\n                emitted = x;",
+                                      ["test_saguaro_preserves_the_target_distribution"]),
     "saguaro_weight_inverted": ("return exp((double)z[x] / T - M) * (inS[x] ? invC : 1.0) / S;",
                                 "return exp((double)z[x] / T - M) * (inS[x] ? 1.0 / invC : 1.0) / S;",
                                 ["test_saguaro_draft_probabilities"]),

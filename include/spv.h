@@ -53,6 +53,7 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
 #define SPV_SAMPLER_SUB 32     /* ids per sampler sub-block (part of the sampling rule) */
 #define SPV_MAX_TRIALS 64    /* residual rejection trials before the direct draw */
 #define SPV_MAX_TOP_K 64     /* top_k of spv_verify_chain_filtered */
+#define SPV_MAX_TREE_NODES 32 /* nodes of a spv_verify_tree draft tree (root included) */
 
 /*
  * spv_verify_chain -- [SD] steps 3 and 4 for B independent sequences.
@@ -214,6 +215,49 @@ spv_status spv_verify_chain_filtered(const void *target_logits, const void *draf
 
 /* Workspace bytes spv_verify_chain_filtered needs (also valid for T == 0). */
 size_t spv_filtered_workspace_bytes(int B, int gamma, int V);
+
+/*
+ * spv_verify_tree -- verify of a draft token tree per sequence.  The pages
+ * name draft trees ([SPD] tree drafting of width 4; tree verification with
+ * k = 21 nodes in the benchmark study) but give no verification rule; this
+ * follows the published multi-round speculative sampling for token trees
+ * (SpecInfer), which keeps the emitted tokens distributed as the target's.
+ * Node 0 is the root (the context); node v >= 1 holds token tokens[b,v] and
+ * hangs from parent[b,v] < v.  target row v is p at node v (the next-token
+ * distribution after the path to v), draft row v is q at node v, from which
+ * v's children were drawn i.i.d.  From the root: the children c of node u
+ * are tested in index order against
+ *   P_m = max(0, p_u - s_m q_u) / N_m,  s_0 = 0, N_0 = 1, s_{m+1} = s_m + N_m,
+ *   N_m = sum_x max(0, p_u(x) - s_m q_u(x)),
+ * m = children rejected so far: c (token x) is accepted iff P_m(x) > 0 and
+ * r[b,c] q_u(x) <= P_m(x), and the walk descends into it.  When every child
+ * of u is rejected one token is drawn from P_m (the chain's rejection trials
+ * from p_u with q scaled by s_m, then the direct residual race); at a leaf
+ * the bonus token from p_u.  Draws follow spv_verify_chain's sampling rule
+ * with position = the node index.  A tree that is one path is
+ * spv_verify_chain exactly (r[b, i+1] <-> r[b, i]).  T == 0: descend into the
+ * first child whose token is the argmax of p_u (lowest id on ties), emit the
+ * last node's argmax; draft_logits, r and sample_keys are then not read.
+ *   target_logits, draft_logits  [B, N, V] dtype (device)
+ *   parent, tokens               [B, N] int32 (device); parent[b,0] = -1
+ *   r                            [B, N] fp32 in (0, 1] (r[b,0] unused)
+ *   1 <= N <= SPV_MAX_TREE_NODES
+ *   accept_count [B] out: accepted nodes k (-1 for a bad row)
+ *   out_tokens   [B, N] out: the k accepted tokens, the drawn one, then -1
+ *   out_nodes    [B, N] out, optional: the k accepted nodes, then -1
+ *   row_status   [B] out, optional
+ *   workspace    >= spv_tree_workspace_bytes(B, N, V) bytes (zero-filled once)
+ * Bad rows: a parent outside [0, v) or a token outside [0, V); NaN / +inf or
+ * no finite logit in any target row, or in the draft row of a node with
+ * children; a rejection whose residual has no mass.
+ */
+spv_status spv_verify_tree(const void *target_logits, const void *draft_logits, spv_dtype dtype,
+                           const int32_t *parent, const int32_t *tokens, const float *r,
+                           const uint64_t *sample_keys, int B, int N, int V, float temperature,
+                           int32_t *accept_count, int32_t *out_tokens, int32_t *out_nodes, int32_t *row_status,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+size_t spv_tree_workspace_bytes(int B, int N, int V);
 
 /* Bytes of device memory behind spv_verify_chain_noalloc (per GPU, held from
  * library load until process exit). */

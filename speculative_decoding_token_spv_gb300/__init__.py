@@ -27,6 +27,7 @@ SPV_SAMPLER_BLOCK = 1024
 SPV_SAMPLER_SUB = 32
 SPV_MAX_TRIALS = 64
 SPV_MAX_TOP_K = 64
+SPV_MAX_TREE_NODES = 32
 
 _lib = None
 
@@ -55,6 +56,10 @@ def load_library():
     lib.spv_verify_chain_saguaro.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, ctypes.c_float, P, P,
                                              P, P, P, P, P, S, P]
     lib.spv_verify_chain_saguaro.restype = I
+    lib.spv_verify_tree.argtypes = [P, P, I, P, P, P, P, I, I, I, ctypes.c_float, P, P, P, P, P, S, P]
+    lib.spv_verify_tree.restype = I
+    lib.spv_tree_workspace_bytes.argtypes = [I, I, I]
+    lib.spv_tree_workspace_bytes.restype = S
     lib.spv_verify_chain_filtered.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, I, ctypes.c_float, P, P, P,
                                               P, P, P, S, P]
     lib.spv_verify_chain_filtered.restype = I
@@ -290,6 +295,54 @@ def spv_verify_chain_filtered(target_logits, draft_logits, draft_tokens, r, samp
                                        _ptr(out.get("pq")), _ptr(out.get("resid_norm")), _ptr(out.get("row_status")),
                                        _ptr(workspace), workspace.numel(), _stream(stream, dev))
     _check(st, "spv_verify_chain_filtered")
+    return out
+
+
+def spv_tree_workspace_bytes(B: int, N: int, V: int) -> int:
+    return load_library().spv_tree_workspace_bytes(B, N, V)
+
+
+def spv_verify_tree(target_logits, draft_logits, parent, tokens, r, sample_keys, temperature: float, *,
+                    workspace=None, out=None, want_nodes: bool = True, want_status: bool = True, stream=None) -> dict:
+    """Verify of a draft token tree per sequence (see spv_verify_tree in
+    spv.h).  target_logits, draft_logits [B, N, V]; parent, tokens [B, N]
+    int32; r [B, N] float32; sample_keys [B] int64.  Returns accept_count,
+    out_tokens [B, N], out_nodes [B, N] and row_status."""
+    target_logits = _cuda(target_logits, "target_logits")
+    dev = target_logits.device
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N, V]")
+    B, N, V = target_logits.shape
+    greedy = float(temperature) == 0.0
+    parent = _cuda(parent, "parent", torch.int32)
+    tokens = _cuda(tokens, "tokens", torch.int32)
+    if tuple(parent.shape) != (B, N) or tuple(tokens.shape) != (B, N):
+        raise ValueError("parent and tokens must be [B, N]")
+    if not greedy:
+        draft_logits = _cuda(draft_logits, "draft_logits", target_logits.dtype)
+        r = _cuda(r, "r", torch.float32)
+        sample_keys = _cuda(sample_keys, "sample_keys", torch.int64)
+        if tuple(draft_logits.shape) != (B, N, V) or tuple(r.shape) != (B, N) or tuple(sample_keys.shape) != (B,):
+            raise ValueError("draft_logits [B,N,V], r [B,N], sample_keys [B] expected")
+    else:
+        draft_logits = r = sample_keys = None
+    lib = load_library()
+    if workspace is None:
+        workspace = new_workspace(lib.spv_tree_workspace_bytes(B, N, V), dev)
+    out = dict(out) if out else {}
+    if "accept_count" not in out:
+        out["accept_count"] = torch.empty(B, dtype=torch.int32, device=dev)
+    if "out_tokens" not in out:
+        out["out_tokens"] = torch.empty(B, N, dtype=torch.int32, device=dev)
+    if want_nodes and "out_nodes" not in out:
+        out["out_nodes"] = torch.empty(B, N, dtype=torch.int32, device=dev)
+    if want_status and "row_status" not in out:
+        out["row_status"] = torch.empty(B, dtype=torch.int32, device=dev)
+    st = lib.spv_verify_tree(_ptr(target_logits), _ptr(draft_logits), _dtype_code(target_logits), _ptr(parent),
+                             _ptr(tokens), _ptr(r), _ptr(sample_keys), B, N, V, float(temperature),
+                             _ptr(out["accept_count"]), _ptr(out["out_tokens"]), _ptr(out.get("out_nodes")),
+                             _ptr(out.get("row_status")), _ptr(workspace), workspace.numel(), _stream(stream, dev))
+    _check(st, "spv_verify_tree")
     return out
 
 

@@ -145,6 +145,47 @@ spv_status spv_verify_chain_saguaro(const void *target_logits, const void *draft
                              fanout, cache_slot, workspace, workspace_bytes, stream, C);
 }
 
+size_t spv_tree_workspace_bytes(int B, int N, int V)
+{
+    if (B < 1 || N < 1 || N > SPV_MAX_TREE_NODES || V < 2) return 0;
+    return spv::tree_ws_bytes(B, N, V);
+}
+
+spv_status spv_verify_tree(const void *target_logits, const void *draft_logits, spv_dtype dtype, const int32_t *parent,
+                           const int32_t *tokens, const float *r, const uint64_t *sample_keys, int B, int N, int V,
+                           float temperature, int32_t *accept_count, int32_t *out_tokens, int32_t *out_nodes,
+                           int32_t *row_status, void *workspace, size_t workspace_bytes, void *stream)
+{
+    if (!dtype_ok(dtype) || !target_logits || !parent || !tokens || !accept_count || !out_tokens || !workspace)
+        return SPV_ERR_INVALID_ARG;
+    if (N < 1 || N > SPV_MAX_TREE_NODES || !sizes_ok(B, 2 * N, V)) return SPV_ERR_INVALID_ARG;
+    if (!(temperature >= 0.0f) || std::isinf(temperature)) return SPV_ERR_INVALID_ARG;
+    if (!aligned256(workspace) || workspace_bytes < spv::tree_ws_bytes(B, N, V)) return SPV_ERR_INVALID_ARG;
+    const bool greedy = temperature == 0.0f;
+    if (!greedy && (!draft_logits || !r || !sample_keys)) return SPV_ERR_INVALID_ARG;
+    if (!greedy && !(1.0f / temperature < INFINITY)) return SPV_ERR_INVALID_ARG;
+    spv::TreeLaunch L{};
+    L.target = target_logits;
+    L.draft = draft_logits;
+    L.dtype = dtype == SPV_F32 ? 0 : 1;
+    L.parent = parent;
+    L.tokens = tokens;
+    L.r = r;
+    L.keys = sample_keys;
+    L.B = B;
+    L.N = N;
+    L.V = V;
+    L.T = temperature;
+    L.accept_count = accept_count;
+    L.out_tokens = out_tokens;
+    L.out_nodes = out_nodes;
+    L.row_status = row_status;
+    L.ws = workspace;
+    const bool rows16 = (static_cast<size_t>(V) * elem_bytes(dtype)) % 16 == 0;
+    L.tma = rows16 && aligned16(target_logits) && (greedy || aligned16(draft_logits));
+    return cuda_status(spv::launch_tree(L, static_cast<cudaStream_t>(stream)));
+}
+
 size_t spv_filtered_workspace_bytes(int B, int gamma, int V)
 {
     if (B < 1 || gamma < 1 || gamma > SPV_MAX_GAMMA || V < 2) return 0;

@@ -45,6 +45,7 @@ struct ChainParams {
     const float *r;
     const uint64_t *keys;
     int B, gamma, R;
+    int nt, nd;      // target / draft rows per sequence (chain: gamma + 1, gamma; tree: N, N)
     float invT, c2;  // 1/T and log2(e)/T
     int vec;         // rows 16-byte aligned: vector loads in finalize
     int32_t *accept_count, *out_tokens;
@@ -53,6 +54,8 @@ struct ChainParams {
     float2 *stats;   // [B*R*nb] (block max of z, sum exp((z - max)/T)); NaN max = bad block
     float *resid;    // [B*nb] residual block masses (direct draw / normaliser only)
     CacheLookup cache;
+    const int32_t *tree_parent;  // tree verify: [B, N] parents
+    int32_t *tree_nodes;         // tree verify: [B, N] accepted nodes out (optional)
     int sag;         // Saguaro sampling: the draft distribution at position i divides its
     float invC;      // cached candidates' (cache lists) probability by C (invC = 1/C)
 };
@@ -76,6 +79,7 @@ struct ChainSmem {
     float Z;
     uint64_t key;
     int sag_id[32][64];  // Saguaro: cached candidates of draft position i (-1: none / repeated)
+    int par[32];         // tree: parent of each node
 };
 
 // Barrier of the FWV warps of a chain finalize CTA.
@@ -115,11 +119,12 @@ template <int DT> struct ChainOp {
     using Smem = ChainSmem;
     static constexpr int EB = DType<DT>::BYTES;
 
+    // Row rho of sequence b: target rows 0 .. nt-1, then draft rows.
     __device__ static __forceinline__ const unsigned char *row_of(const Params &P, int b, int rho)
     {
-        if (rho <= P.gamma)
-            return P.target + (static_cast<size_t>(b) * (P.gamma + 1) + rho) * static_cast<size_t>(P.V) * EB;
-        return P.draft + (static_cast<size_t>(b) * P.gamma + (rho - P.gamma - 1)) * static_cast<size_t>(P.V) * EB;
+        if (rho < P.nt)
+            return P.target + (static_cast<size_t>(b) * P.nt + rho) * static_cast<size_t>(P.V) * EB;
+        return P.draft + (static_cast<size_t>(b) * P.nd + (rho - P.nt)) * static_cast<size_t>(P.V) * EB;
     }
     __device__ static __forceinline__ const void *row_ptr(const Params &P, long long row)
     {
@@ -349,12 +354,78 @@ template <int DT> struct ChainOp {
         return xi;
     }
 
+    // Row statistics of sequence b from its block statistics: one half-warp
+    // per row, all rows at once, up to 16 loads per lane in flight together:
+    // sm.M / sm.S = row max / sum exp((z - max) / T).  Target rows rho <
+    // ncache keep (m_beta, race factor) in sm.st for the draws (when they
+    // fit).  A bad row (NaN / +inf, no finite logit) gets S = NaN; with
+    // flag_all it also sets sm.bad.  FWV warps.
+    template <int FWV>
+    __device__ static void merge_stats(const Params &P, int b, Smem &sm, int ncache, bool flag_all, int warp, int lane)
+    {
+        const int R = P.R, nb = P.nb;
+        const int half = lane >> 4, hl = lane & 15;
+        for (int rho0 = 0; rho0 < R; rho0 += 2 * FWV) {
+            const int rho = rho0 + 2 * warp + half;
+            const bool active = rho < R;
+            const float2 *st = P.stats + (static_cast<long long>(b) * R + (active ? rho : 0)) * nb;
+            const bool keep = active && rho < ncache && sm.cached;
+            float m = -INFINITY, s = 0.f;
+            bool bad = false;
+            for (int base = 0; base < nb; base += 16 * 16) {
+                float2 v[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int beta = base + 16 * u + hl;
+                    v[u] = (active && beta < nb) ? __ldcg(&st[beta]) : make_float2(-INFINITY, 0.f);
+                }
+                float cm = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    const int beta = base + 16 * u + hl;
+                    if (isnan(v[u].x)) bad = true;
+                    else cm = fmaxf(cm, v[u].x);
+                    if (keep && beta < nb) sm.st[rho * nb + beta] = v[u];
+                }
+                const float nm = fmaxf(m, cm);
+                if (nm != -INFINITY) {
+                    float acc = s > 0.f ? s * expf((m - nm) * P.invT) : 0.f;
+#pragma unroll
+                    for (int u = 0; u < 16; ++u)
+                        if (v[u].y > 0.f) acc += v[u].y * expf((v[u].x - nm) * P.invT);
+                    s = acc;
+                    m = nm;
+                }
+            }
+            float mw = m;
+#pragma unroll
+            for (int o = 8; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+            s = (s > 0.f) ? s * expf((m - mw) * P.invT) : 0.f;
+#pragma unroll
+            for (int o = 8; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            const unsigned badm = __ballot_sync(0xffffffffu, bad);
+            const bool rowbad = ((badm >> (16 * half)) & 0xffffu) != 0 || !(s > 0.f);
+            if (active && hl == 0) {
+                sm.M[rho] = mw;
+                sm.S[rho] = rowbad ? __int_as_float(0x7fffffff) : s;
+                if (rowbad && flag_all) atomicOr(&sm.bad, 1);
+            }
+            if (keep && !rowbad && mw != -INFINITY) {
+                // entry beta was staged by this lane (beta = hl mod 16): no warp barrier needed
+                for (int beta = hl; beta < nb; beta += 16) {
+                    const float2 v = sm.st[rho * nb + beta];
+                    sm.st[rho * nb + beta].y = v.y > 0.f ? fast_exp2((mw - v.x) * P.c2) / v.y : -1.f;
+                }
+            }
+        }
+    }
+
     // Direct race over the residual w = max(0, p - q) (after the rejection
     // trials all failed): block masses from residual_pass, then sub-blocks
     // and ids of the winning block (target and draft logits in tb / db).
     __device__ static int race_resid(const Params &P, int b, const unsigned char *tp, const unsigned char *dp, float Mt,
                                      float St, float Md, float Sd, uint64_t key, uint32_t pos, float *tb, float *db,
-                                     const int *sids, int lane)
+                                     const int *sids, float qs, int lane)
     {
         float best = INFINITY;
         int bi = INT_MAX;
@@ -395,7 +466,7 @@ template <int DT> struct ChainOp {
         float ws = 0.f;
         for (int i = 0; i < SUB; ++i) {
             const int e = (i + lane) & (SUB - 1), o = SUB * lane + e;
-            ws += resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((smask >> e) & 1u) ? P.invC : 1.f);
+            ws += resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((smask >> e) & 1u) ? P.invC * qs : qs);
         }
         const uint32_t n = static_cast<uint32_t>(base / SUB + lane);
         uint32_t w[4];
@@ -407,7 +478,8 @@ template <int DT> struct ChainOp {
         const int o = SUB * si + lane;
         const uint32_t wmask = __shfl_sync(0xffffffffu, smask, si);
         const float wx =
-            x < P.V ? resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((wmask >> lane) & 1u) ? P.invC : 1.f) : 0.f;
+            x < P.V ? resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((wmask >> lane) & 1u) ? P.invC * qs : qs)
+                    : 0.f;
         philox_group(w, key, STREAM_FB_TOKEN, 0, pos, static_cast<uint32_t>(x) >> 2);
         float Ax = wx > 0.f ? arrival(expo(w[x & 3]), 1.f / wx) : INFINITY;
         int xi = x;
@@ -434,14 +506,14 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
     // P.resid; returns Z = sum w in sm.Z.  All consumer warps.
     __device__ static void residual_pass(const Params &P, int b, const unsigned char *tp, const unsigned char *dp,
                                          float Mt, float St, float Md, float Sd, Smem &sm, int warp, int lane, float *tb,
-                                         int k)
+                                         int k, float qs = 1.f)
     {
         const float it = 1.f / St, id = 1.f / Sd;
         for (int beta = warp; beta < P.nb; beta += FWV) {
             float part = 0.f;
             const int hi = min(P.V, (beta + 1) * G);
             for (int x = beta * G + lane; x < hi; x += 32)
-                part += resid_mass(DType<DT>::load(tp, x), DType<DT>::load(dp, x), Mt, it, Md, id, P.invT);
+                part += resid_mass_w(DType<DT>::load(tp, x), DType<DT>::load(dp, x), Mt, it, Md, id, P.invT, qs);
             part = warp_sum(part);
             if (lane == 0) P.resid[static_cast<size_t>(b) * P.nb + beta] = part;
         }
@@ -571,63 +643,8 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
-        // B. Row statistics from the block statistics: one half-warp per row,
-        //    all rows at once, up to 16 loads per lane in flight together.  Target
-        //    rows keep (m_beta, race factor) in shared memory for the draw.
-        const int half = lane >> 4, hl = lane & 15;
-        for (int rho0 = 0; rho0 < R; rho0 += 2 * FWV) {
-            const int rho = rho0 + 2 * warp + half;
-            const bool active = rho < R;
-            const float2 *st = P.stats + (static_cast<long long>(b) * R + (active ? rho : 0)) * nb;
-            const bool keep = active && rho <= g && sm.cached;
-            float m = -INFINITY, s = 0.f;
-            bool bad = false;
-            for (int base = 0; base < nb; base += 16 * 16) {
-                float2 v[16];
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int beta = base + 16 * u + hl;
-                    v[u] = (active && beta < nb) ? __ldcg(&st[beta]) : make_float2(-INFINITY, 0.f);
-                }
-                float cm = -INFINITY;
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int beta = base + 16 * u + hl;
-                    if (isnan(v[u].x)) bad = true;
-                    else cm = fmaxf(cm, v[u].x);
-                    if (keep && beta < nb) sm.st[rho * nb + beta] = v[u];
-                }
-                const float nm = fmaxf(m, cm);
-                if (nm != -INFINITY) {
-                    float acc = s > 0.f ? s * expf((m - nm) * P.invT) : 0.f;
-#pragma unroll
-                    for (int u = 0; u < 16; ++u)
-                        if (v[u].y > 0.f) acc += v[u].y * expf((v[u].x - nm) * P.invT);
-                    s = acc;
-                    m = nm;
-                }
-            }
-            float mw = m;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-            s = (s > 0.f) ? s * expf((m - mw) * P.invT) : 0.f;
-#pragma unroll
-            for (int o = 8; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            const unsigned badm = __ballot_sync(0xffffffffu, bad);
-            const bool rowbad = ((badm >> (16 * half)) & 0xffffu) != 0;
-            if (active && hl == 0) {
-                sm.M[rho] = mw;
-                sm.S[rho] = s;
-                if (rowbad || !(s > 0.f)) atomicOr(&sm.bad, 1);
-            }
-            if (keep && !rowbad && mw != -INFINITY) {
-                // entry beta was staged by this lane (beta = hl mod 16): no warp barrier needed
-                for (int beta = hl; beta < nb; beta += 16) {
-                    const float2 v = sm.st[rho * nb + beta];
-                    sm.st[rho * nb + beta].y = v.y > 0.f ? fast_exp2((mw - v.x) * P.c2) / v.y : -1.f;
-                }
-            }
-        }
+        // B. Row statistics from the block statistics (all rows at once).
+        Base::template merge_stats<FWV>(P, b, sm, g + 1, true, warp, lane);
         fin_sync<FWV>();
         if (sm.bad) {
             write_bad_row(P, b, warp, lane);
@@ -727,7 +744,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 if (fallback) {
                     if (warp == 0) {
                         const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(k), tb, db,
-                                                 P.sag ? sm.sag_id[k] : nullptr, lane);
+                                                 P.sag ? sm.sag_id[k] : nullptr, 1.f, lane);
                         if (lane == 0) sm.result = x;
                     }
                     fin_sync<FWV>();
@@ -757,6 +774,209 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
 };
 
 // =====================================================================================
+// Tree verify, T > 0 (multi-round speculative sampling over a token tree)
+// =====================================================================================
+// Rows per sequence: target rows 0..N-1 (p at node v), draft rows N..2N-1 (q
+// at node v, from which v's children were drawn).  The finalize walks the
+// tree from the root: the children c of node u are tested in index order
+// against P_m = max(0, p_u - s_m q_u) / N_m (s_0 = 0, N_0 = 1, s_{m+1} = s_m +
+// N_m, N_m = sum max(0, p_u - s_m q_u): a residual pass of the whole CTA);
+// the first accepted child is descended into; when all are rejected one
+// token is drawn from P_m (rejection trials from p_u with q scaled by s_m,
+// then the direct residual race), at a leaf the bonus from p_u.
+struct TreeIO {
+    const int32_t *parent;  // [B, N]
+    int32_t *out_nodes;     // [B, N] accepted nodes, then -1 (optional)
+};
+
+template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
+    using Fin = ChainFin<DT, FWV>;
+    using Base = ChainOp<DT>;
+    using Params = ChainParams;
+    using Smem = ChainSmem;
+    static constexpr int FIN_WARPS = FWV;
+    static constexpr int FIN_BUF_FLOATS = 2 * FWV * G;
+
+    __device__ static void write_bad_tree(const Params &P, const TreeIO &T, int b, int lane)
+    {
+        const int N = P.nt;
+        if (threadIdx.x < 32) {
+            for (int i = lane; i < N; i += 32) {
+                P.out_tokens[static_cast<size_t>(b) * N + i] = -1;
+                if (T.out_nodes) T.out_nodes[static_cast<size_t>(b) * N + i] = -1;
+            }
+            if (lane == 0) {
+                P.accept_count[b] = -1;
+                if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
+            }
+        }
+    }
+
+    __device__ static void finalize(const Params &P, int b, Smem &sm, float *buf, int warp, int lane)
+    {
+        finalize_tree(P, TreeIO{P.tree_parent, P.tree_nodes}, b, sm, buf, warp, lane);
+    }
+
+    __device__ static void finalize_tree(const Params &P, const TreeIO &T, int b, Smem &sm, float *buf, int warp,
+                                         int lane)
+    {
+        const int N = P.nt, nb = P.nb;
+        float *tb = buf + warp * 2 * G, *db = tb + G;
+        // A. Inputs: parents, tokens, uniforms, and each node's token logit
+        //    in its parent's target and draft rows (before the dependent wait).
+        if (threadIdx.x == 0) {
+            sm.bad = 0;
+            sm.key = P.keys[b];
+            sm.cached = (N * nb <= STAT_CACHE) ? 1 : 0;
+        }
+        if (warp == 0 && lane < N) {
+            const int v = lane;
+            const int pv = T.parent[static_cast<size_t>(b) * N + v];
+            const int x = P.tokens[static_cast<size_t>(b) * N + v];
+            sm.par[v] = pv;
+            sm.x[v] = x;
+            sm.rr[v] = P.r[static_cast<size_t>(b) * N + v];
+            const bool ok = (v == 0) ? (pv == -1) : (pv >= 0 && pv < v && x >= 0 && x < P.V);
+            sm.zt[v] = sm.zd[v] = 0.f;
+            if (v > 0 && ok) {
+                sm.zt[v] = DType<DT>::load(Base::row_of(P, b, pv), x);
+                sm.zd[v] = DType<DT>::load(Base::row_of(P, b, N + pv), x);
+            }
+            if (!ok) atomicOr(&sm.bad, 1);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        fin_sync<FWV>();
+        // B. Row statistics; a bad target row, or a bad draft row of a node
+        //    with children, makes the sequence bad.
+        Base::template merge_stats<FWV>(P, b, sm, N, false, warp, lane);
+        fin_sync<FWV>();
+        if (warp == 0 && !sm.bad) {
+            bool bad = lane < N && !(sm.S[lane] > 0.f);
+            // the draft row of u matters iff some node has parent u
+            for (int v = 1; v < N; ++v)
+                if (lane == sm.par[v] && !(sm.S[N + lane] > 0.f)) bad = true;
+            if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&sm.bad, 1);
+        }
+        fin_sync<FWV>();
+        if (sm.bad) {
+            write_bad_tree(P, T, b, lane);
+            return;
+        }
+        // C. The walk.  Every thread follows the same decisions (from shared
+        //    values); residual passes and draws use the CTA.
+        const uint64_t key = sm.key;
+        int u = 0, k = 0, res = -1;
+        for (;;) {
+            const unsigned kids = __ballot_sync(0xffffffffu, lane < N && lane > u && sm.par[lane] == u);
+            const float Mt = sm.M[u], St = sm.S[u];
+            const unsigned char *tp = Base::row_of(P, b, u);
+            if (kids == 0u) {
+                // leaf: the bonus token from p_u (warp 0)
+                if (warp == 0) {
+                    const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, 0u, static_cast<uint32_t>(u), lane);
+                    Base::load_block(P, tp, beta, tb, lane);
+                    const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), key, STREAM_SUB,
+                                                        STREAM_TOKEN, 0u, static_cast<uint32_t>(u), lane);
+                    if (lane == 0) sm.result = x;
+                }
+                fin_sync<FWV>();
+                res = sm.result;
+                break;
+            }
+            const float Md = sm.M[N + u], Sd = sm.S[N + u];
+            const unsigned char *dp = Base::row_of(P, b, N + u);
+            float sres = 0.f, Nm = 1.f;
+            int next = -1;
+            for (unsigned m = kids; m; m &= m - 1u) {
+                const int c = __ffs(m) - 1;
+                const float px = expf((sm.zt[c] - Mt) * P.invT) / St;
+                const float qx = expf((sm.zd[c] - Md) * P.invT) / Sd;
+                float Pm = px;
+                if (sres > 0.f) {
+                    const float d = __fsub_rn(px, __fmul_rn(sres, qx));
+                    Pm = d > 0.f ? d / Nm : 0.f;
+                }
+                if (Pm > 0.f && sm.rr[c] * qx <= Pm) {
+                    next = c;
+                    break;
+                }
+                // rejected: the next residual and its mass N_m
+                sres += Nm;
+                Fin::residual_pass(P, b, tp, dp, Mt, St, Md, Sd, sm, warp, lane, tb, 0, sres);
+                Nm = sm.Z;
+                if (!(Nm > 0.f)) {  // no residual mass (a token outside q's support)
+                    write_bad_tree(P, T, b, lane);
+                    return;
+                }
+            }
+            if (next >= 0) {
+                if (threadIdx.x == 0) {
+                    P.out_tokens[static_cast<size_t>(b) * N + k] = sm.x[next];
+                    if (T.out_nodes) T.out_nodes[static_cast<size_t>(b) * N + k] = next;
+                }
+                ++k;
+                u = next;
+                continue;
+            }
+            // every child rejected: one draw from max(0, p_u - s q_u), FWV trials per round
+            if (threadIdx.x == 0) sm.result = -1;
+            fin_sync<FWV>();
+            for (int round = 0; round < MAX_TRIALS / FWV; ++round) {
+                const uint32_t t = static_cast<uint32_t>(round * FWV + warp);
+                const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, t, static_cast<uint32_t>(u), lane);
+                Base::load_block(P, tp, beta, tb, lane);
+                Base::load_block(P, dp, beta, db, lane);
+                uint32_t aw = 0;
+                const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), key, STREAM_SUB,
+                                                    STREAM_TOKEN, t, static_cast<uint32_t>(u), lane, STREAM_ACCEPT, &aw);
+                if (lane == 0) {
+                    const float v = uniform24(aw);
+                    const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
+                    const float q = __fmul_rn(expf((db[x - beta * G] - Md) * P.invT) / Sd, sres);
+                    sm.trial_x[warp] = x;
+                    sm.trial_acc[warp] = (q <= (1.0f - v) * p) ? 1 : 0;
+                }
+                fin_sync<FWV>();
+                if (threadIdx.x == 0) {
+                    for (int w = 0; w < FWV; ++w)
+                        if (sm.trial_acc[w]) {
+                            sm.result = sm.trial_x[w];
+                            break;
+                        }
+                }
+                fin_sync<FWV>();
+                if (sm.result >= 0) break;
+            }
+            if (sm.result < 0) {
+                // the block masses of max(0, p - s q) are those of the last residual pass
+                if (warp == 0) {
+                    const int x = Base::race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(u), tb, db,
+                                                   nullptr, sres, lane);
+                    if (lane == 0) sm.result = x;
+                }
+                fin_sync<FWV>();
+            }
+            res = sm.result;
+            break;
+        }
+        if (res < 0) {
+            write_bad_tree(P, T, b, lane);
+            return;
+        }
+        if (threadIdx.x < 32) {
+            for (int i = k + lane; i < N; i += 32) {
+                P.out_tokens[static_cast<size_t>(b) * N + i] = (i == k) ? res : -1;
+                if (T.out_nodes) T.out_nodes[static_cast<size_t>(b) * N + i] = -1;
+            }
+            if (lane == 0) {
+                P.accept_count[b] = k;
+                if (P.row_status) P.row_status[b] = 0;
+            }
+        }
+    }
+};
+
+// =====================================================================================
 // Greedy verify, T = 0
 // =====================================================================================
 struct GreedyParams {
@@ -769,11 +989,14 @@ struct GreedyParams {
     int32_t *accept_count, *out_tokens, *row_status;
     int2 *best;  // [B*R*nb] (max value bits, argmax id); id -2 marks a bad block
     CacheLookup cache;
+    const int32_t *tree_parent;  // greedy tree verify: [B, N] parents (R = N)
+    int32_t *tree_nodes;
 };
 
 struct GreedySmem {
     int a[33];
     int x[32];
+    int par[32];
     int bad;
 };
 
@@ -907,6 +1130,88 @@ template <int DT> struct GreedyOp {
     }
 };
 
+// Greedy tree verify (T = 0): descend into the first child whose token is
+// the argmax of p_u (lowest id on ties); emit the argmax of the last node.
+template <int DT> struct GreedyTreeFin : GreedyOp<DT> {
+    using Params = GreedyParams;
+    using Smem = GreedySmem;
+    static constexpr int FIN_WARPS = NCW;
+    static constexpr int FIN_BUF_FLOATS = 0;
+
+    __device__ static void finalize(const Params &P, int b, Smem &sm, float *, int warp, int lane)
+    {
+        const int N = P.R, nb = P.nb;
+        if (threadIdx.x == 0) sm.bad = 0;
+        if (warp == 0 && lane < N) {
+            const int pv = P.tree_parent[static_cast<size_t>(b) * N + lane];
+            const int x = P.tokens[static_cast<size_t>(b) * N + lane];
+            sm.par[lane] = pv;
+            sm.x[lane] = x;
+            const bool ok = (lane == 0) ? (pv == -1) : (pv >= 0 && pv < lane && x >= 0 && x < P.V);
+            if (!ok) atomicOr(&sm.bad, 1);
+        }
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        consumer_sync();
+        for (int rho = warp; rho < N; rho += NCW) {
+            const int2 *bb = P.best + (static_cast<long long>(b) * N + rho) * nb;
+            float bv = -INFINITY;
+            int bi = INT_MAX;
+            bool bad = false;
+            for (int beta = lane; beta < nb; beta += 32) {
+                const int2 o = __ldcg(&bb[beta]);
+                if (o.y == -2) {
+                    bad = true;
+                } else {
+                    const float v = __int_as_float(o.x);
+                    if (v > bv || (v == bv && o.y < bi)) {
+                        bv = v;
+                        bi = o.y;
+                    }
+                }
+            }
+            warp_argmax(bv, bi);
+            bad = __any_sync(0xffffffffu, bad);
+            if (lane == 0) {
+                sm.a[rho] = bi;
+                if (bad || bv == -INFINITY || bi == INT_MAX) atomicOr(&sm.bad, 1);
+            }
+        }
+        consumer_sync();
+        if (warp != 0) return;
+        if (sm.bad) {
+            for (int i = lane; i < N; i += 32) {
+                P.out_tokens[static_cast<size_t>(b) * N + i] = -1;
+                if (P.tree_nodes) P.tree_nodes[static_cast<size_t>(b) * N + i] = -1;
+            }
+            if (lane == 0) {
+                P.accept_count[b] = -1;
+                if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
+            }
+            return;
+        }
+        int u = 0, k = 0;
+        for (;;) {
+            const unsigned m = __ballot_sync(0xffffffffu, lane < N && lane > u && sm.par[lane] == u && sm.x[lane] == sm.a[u]);
+            if (!m) break;
+            const int c = __ffs(m) - 1;
+            if (lane == 0) {
+                P.out_tokens[static_cast<size_t>(b) * N + k] = sm.x[c];
+                if (P.tree_nodes) P.tree_nodes[static_cast<size_t>(b) * N + k] = c;
+            }
+            ++k;
+            u = c;
+        }
+        for (int i = k + lane; i < N; i += 32) {
+            P.out_tokens[static_cast<size_t>(b) * N + i] = (i == k) ? sm.a[u] : -1;
+            if (P.tree_nodes) P.tree_nodes[static_cast<size_t>(b) * N + i] = -1;
+        }
+        if (lane == 0) {
+            P.accept_count[b] = k;
+            if (P.row_status) P.row_status[b] = 0;
+        }
+    }
+};
+
 // =====================================================================================
 // Host launch
 // =====================================================================================
@@ -949,6 +1254,8 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
     P.B = L.B;
     P.gamma = L.gamma;
     P.R = 2 * L.gamma + 1;
+    P.nt = L.gamma + 1;
+    P.nd = L.gamma;
     P.total_items = static_cast<long long>(L.B) * P.R * P.nc;
     unsigned char *ws = static_cast<unsigned char *>(L.ws);
     P.err = reinterpret_cast<unsigned *>(ws);
@@ -1006,6 +1313,80 @@ cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st)
     fill_cache(P.cache, L);
     return L.dtype == 0 ? launch_stream_finalize<GreedyOp<0>, GreedyOp<0>, 0>(P, L.tma, L.B, st)
                         : launch_stream_finalize<GreedyOp<1>, GreedyOp<1>, 1>(P, L.tma, L.B, st);
+}
+
+size_t tree_ws_bytes(int B, int N, int V)
+{
+    const size_t nb = blocks_per_row(V), R = 2 * static_cast<size_t>(N);
+    size_t n = WS_HEADER;
+    n += align256(static_cast<size_t>(B) * R * nb * 8);  // block statistics
+    n += align256(static_cast<size_t>(B) * nb * 4);      // residual block masses
+    const size_t gr = WS_HEADER + align256(static_cast<size_t>(B) * N * nb * 8);
+    return n > gr ? n : gr;
+}
+
+cudaError_t launch_tree(const TreeLaunch &L, cudaStream_t st)
+{
+    unsigned char *ws = static_cast<unsigned char *>(L.ws);
+    if (L.T == 0.0f) {
+        GreedyParams P{};
+        P.V = L.V;
+        P.nb = blocks_per_row(L.V);
+        P.nc = chunks_per_row(L.V);
+        P.B = L.B;
+        P.gamma = L.N - 1;
+        P.R = L.N;
+        P.total_items = static_cast<long long>(L.B) * P.R * P.nc;
+        P.err = reinterpret_cast<unsigned *>(ws);
+        P.best = reinterpret_cast<int2 *>(ws + WS_HEADER);
+        P.target = static_cast<const unsigned char *>(L.target);
+        P.tokens = L.tokens;
+        P.accept_count = L.accept_count;
+        P.out_tokens = L.out_tokens;
+        P.row_status = L.row_status;
+        P.tree_parent = L.parent;
+        P.tree_nodes = L.out_nodes;
+        return L.dtype == 0 ? launch_stream_finalize<GreedyOp<0>, GreedyTreeFin<0>, 0>(P, L.tma, L.B, st)
+                            : launch_stream_finalize<GreedyOp<1>, GreedyTreeFin<1>, 1>(P, L.tma, L.B, st);
+    }
+    ChainParams P{};
+    P.V = L.V;
+    P.nb = blocks_per_row(L.V);
+    P.nc = chunks_per_row(L.V);
+    P.B = L.B;
+    P.gamma = L.N - 1;
+    P.nt = L.N;
+    P.nd = L.N;
+    P.R = 2 * L.N;
+    P.total_items = static_cast<long long>(L.B) * P.R * P.nc;
+    P.err = reinterpret_cast<unsigned *>(ws);
+    size_t off = WS_HEADER;
+    P.stats = reinterpret_cast<float2 *>(ws + off);
+    off += align256(static_cast<size_t>(L.B) * P.R * P.nb * 8);
+    P.resid = reinterpret_cast<float *>(ws + off);
+    P.target = static_cast<const unsigned char *>(L.target);
+    P.draft = static_cast<const unsigned char *>(L.draft);
+    P.tokens = L.tokens;
+    P.r = L.r;
+    P.keys = L.keys;
+    P.invT = 1.0f / L.T;
+    P.c2 = 1.4426950408889634f / L.T;
+    P.vec = L.tma ? 1 : 0;
+    P.accept_count = L.accept_count;
+    P.out_tokens = L.out_tokens;
+    P.row_status = L.row_status;
+    P.invC = 1.0f;
+    P.tree_parent = L.parent;
+    P.tree_nodes = L.out_nodes;
+    int sms = 0;
+    cudaError_t e = device_sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    const bool wide = L.B <= sms;
+    if (L.dtype == 0)
+        return wide ? launch_stream_finalize<ChainOp<0>, TreeFin<0, FW>, 0>(P, L.tma, L.B, st)
+                    : launch_stream_finalize<ChainOp<0>, TreeFin<0, NCW>, 0>(P, L.tma, L.B, st);
+    return wide ? launch_stream_finalize<ChainOp<1>, TreeFin<1, FW>, 1>(P, L.tma, L.B, st)
+                : launch_stream_finalize<ChainOp<1>, TreeFin<1, NCW>, 1>(P, L.tma, L.B, st);
 }
 
 }  // namespace spv

@@ -41,6 +41,19 @@ struct ChainLaunch {
     float sag_C;
 };
 
+struct TreeLaunch {
+    const void *target, *draft;
+    int dtype;
+    const int32_t *parent, *tokens;
+    const float *r;
+    const uint64_t *keys;
+    int B, N, V;
+    float T;
+    int32_t *accept_count, *out_tokens, *out_nodes, *row_status;
+    void *ws;
+    bool tma;
+};
+
 struct FanoutLaunch {
     const void *draft;
     int dtype;
@@ -58,10 +71,12 @@ size_t chain_ws_bytes(int B, int gamma, int V);
 size_t greedy_ws_bytes(int B, int gamma, int V);
 size_t fanout_ws_bytes(int B, int K1, int V, int Fmax);
 size_t filtered_ws_bytes(int B, int gamma, int V);
+size_t tree_ws_bytes(int B, int N, int V);
 
 cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st);
 cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st);
 cudaError_t launch_fanout(const FanoutLaunch &L, cudaStream_t st);
 cudaError_t launch_filtered(const ChainLaunch &L, cudaStream_t st);
+cudaError_t launch_tree(const TreeLaunch &L, cudaStream_t st);
 
 }  // namespace spv

@@ -33,6 +33,11 @@ import torch
 SEEDS = dict(tiny=(100, 101, 0, 1), spd=(200, 201, 0, 1), eagle=(300, 301, 2, 3), sweep=(200, 201, 0, 1))
 PEAK_SEED = 202
 FANOUT_SEEDS = (400, 4)
+TREE_SEEDS = (500, 501, 5, 6)
+# Draft-tree shapes: children per node, level by level.  "k21": the 21-node
+# tree (root, 4, 8, 8) of tree-style verification; "w4": width-4 tree drafting
+# (root with 4 children, each continued by a chain of 3).
+TREE_SHAPES = {"k21": [4, 2, 1], "w4": [4, 1, 1, 1], "path4": [1, 1, 1, 1]}
 BONUS_SEED_OFFSET = 7919  # seed of the bonus-position draft row = draft seed + this
 
 
@@ -197,3 +202,83 @@ def saguaro_tokens(w: ChainInputs, cache_ids: torch.Tensor, fanout, C: float, se
     probs = torch.softmax(logits.reshape(B * g, V), dim=1)
     gen = _gen(w.draft.device, seed)
     return torch.multinomial(probs, 1, generator=gen).to(torch.int32).reshape(B, g)
+
+
+@dataclass
+class TreeInputs:
+    name: str
+    target: torch.Tensor   # [B, N, V]: p at node v
+    draft: torch.Tensor    # [B, N, V]: q at node v (its children are drawn from it)
+    parent: torch.Tensor   # [B, N] int32, -1 at the root
+    tokens: torch.Tensor   # [B, N] int32, token of node v (0 at the root)
+    r: torch.Tensor        # [B, N] fp32 in (0, 1]
+    keys: torch.Tensor     # [B] int64
+    temperature: float
+
+    @property
+    def B(self):
+        return self.target.shape[0]
+
+    @property
+    def N(self):
+        return self.target.shape[1]
+
+    @property
+    def V(self):
+        return self.target.shape[2]
+
+
+def tree_parents(shape) -> list:
+    """Parents of a tree built level by level: every node of a level gets
+    shape[level] children; nodes are numbered breadth first."""
+    parent, level = [-1], [0]
+    for width in shape:
+        nxt = []
+        for u in level:
+            for _ in range(width):
+                parent.append(u)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return parent
+
+
+def tree(B=64, shape="k21", V=151936, dtype=torch.bfloat16, temperature=1.0, device="cpu", z_std=3.0, d_std=1.0,
+         peaks=20) -> TreeInputs:
+    """Draft trees on the spd distributions: z ~ N(0, z_std^2) per node (+8
+    on `peaks` ids), d = z + N(0, d_std^2); at T > 0 the children of u are
+    drawn i.i.d. from softmax(d_u / T), at T = 0 they are the top draft ids
+    of u in rank order (distinct)."""
+    par = tree_parents(TREE_SHAPES[shape])
+    N = len(par)
+    s_z, s_d, s_tok, s_u = TREE_SEEDS
+    z = torch.randn(B, N, V, generator=_gen(device, s_z), device=device) * z_std
+    if peaks:
+        score = torch.rand(B, N, V, generator=_gen(device, PEAK_SEED), device=device)
+        idx = score.topk(peaks, dim=2).indices
+        z.scatter_add_(2, idx, torch.full(idx.shape, 8.0, device=device))
+        del score, idx
+    d = torch.randn(B, N, V, generator=_gen(device, s_d), device=device) * d_std
+    d.add_(z)
+    target, draft = z.to(dtype), d.to(dtype)
+    del z, d
+    tok = torch.zeros(B, N, dtype=torch.int32, device=device)
+    gen = _gen(device, s_tok)
+    kids = {}
+    for v in range(1, N):
+        kids.setdefault(par[v], []).append(v)
+    for u, cs in kids.items():
+        du = draft[:, u].float()
+        if temperature == 0:
+            top = du.topk(len(cs), dim=1).indices
+            for j, c in enumerate(cs):
+                tok[:, c] = top[:, j].to(torch.int32)
+        else:
+            probs = torch.softmax(du / temperature, dim=1)
+            pick = torch.multinomial(probs, len(cs), replacement=True, generator=gen)
+            for j, c in enumerate(cs):
+                tok[:, c] = pick[:, j].to(torch.int32)
+    g2 = _gen(device, s_u)
+    r = 1.0 - torch.rand(B, N, generator=g2, device=device, dtype=torch.float32)
+    keys = torch.randint(-(2 ** 63), 2 ** 63 - 1, (B,), generator=g2, device=device, dtype=torch.int64)
+    parent = torch.tensor(par, dtype=torch.int32, device=device).repeat(B, 1)
+    return TreeInputs(f"tree_{shape}", target, draft, parent, tok, r, keys, float(temperature))

@@ -49,6 +49,15 @@ def chain_bytes(B, gamma, V, elem_bytes, T):
     return B * (2 * gamma + 1) * V * elem_bytes + B * gamma * 8 + B * 8 + B * (gamma + 2) * 4
 
 
+def tree_bytes(B, N, internal, V, elem_bytes, T):
+    """Tree verify: every target row once, the draft rows of the nodes with
+    children once (a leaf's draft row is not read), parents and tokens, and
+    at T > 0 r and keys; outputs: accept count, N ids and N nodes."""
+    rows = N if T == 0 else N + internal
+    extra = 0 if T == 0 else B * N * 4 + B * 8
+    return B * rows * V * elem_bytes + B * N * 8 + extra + B * (2 * N + 1) * 4
+
+
 def fanout_bytes(B, K1, V, elem_bytes, sumF):
     return B * K1 * V * elem_bytes + B * K1 * 4 + B * sumF * 4
 
@@ -503,6 +512,21 @@ def run_variants(spv, dev, stream, args):
         res[-1]["mean_accepted"] = round(acc / n, 4)
         res[-1]["sample"] = f"{n} verify outcomes"
     del w, ws, lists
+    # Tree verify (multi-round speculative sampling over a draft tree per
+    # sequence): the 21-node tree and the width-4 tree on the spd rows.
+    tcases = [("k21", 1.0, torch.bfloat16), ("k21", 0.0, torch.bfloat16), ("w4", 1.0, torch.bfloat16),
+              ("k21", 1.0, torch.float32)]
+    for shape, T, dt in tcases:
+        w = workloads.tree(B=64, shape=shape, dtype=dt, temperature=T, device=dev)
+        ws = spv.new_workspace(spv.spv_tree_workspace_bytes(w.B, w.N, w.V), dev)
+        o = spv.spv_verify_tree(w.target, w.draft, w.parent, w.tokens, w.r, w.keys, T, workspace=ws)
+        ms = time_graph(lambda: spv.spv_verify_tree(w.target, w.draft, w.parent, w.tokens, w.r, w.keys, T,
+                                                    workspace=ws, out=o))
+        internal = len(set(workloads.tree_parents(workloads.TREE_SHAPES[shape])[1:]))
+        add(f"tree verify {shape} (N={w.N}) B=64 {str(dt).replace('torch.', '')} T={T:g}", ms,
+            tree_bytes(w.B, w.N, internal, w.V, w.target.element_size(), T), w.B * w.N)
+        res[-1]["mean_accepted"] = round(float(o["accept_count"].float().mean()), 4)
+        del w, ws, o
     torch.cuda.synchronize()
     return res
 

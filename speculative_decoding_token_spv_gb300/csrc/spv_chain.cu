@@ -56,6 +56,8 @@ struct ChainParams {
     CacheLookup cache;
     const int32_t *tree_parent;  // tree verify: [B, N] parents
     int32_t *tree_nodes;         // tree verify: [B, N] accepted nodes out (optional)
+    int cs;                      // tree verify: finalize CTAs per sequence (one cluster)
+    unsigned *tree_bar;          // tree verify: [B][2] barrier of a sequence's CTAs
     int sag;         // Saguaro sampling: the draft distribution at position i divides its
     float invC;      // cached candidates' (cache lists) probability by C (invC = 1/C)
 };
@@ -76,6 +78,7 @@ struct ChainSmem {
     int trial_x[FW];
     int trial_acc[FW];
     int result;
+    int gflag;              // tree: outcome of the last barrier of the sequence's CTAs
     float Z;
     uint64_t key;
     int sag_id[32][64];  // Saguaro: cached candidates of draft position i (-1: none / repeated)
@@ -425,8 +428,9 @@ template <int DT> struct ChainOp {
     // and ids of the winning block (target and draft logits in tb / db).
     __device__ static int race_resid(const Params &P, int b, const unsigned char *tp, const unsigned char *dp, float Mt,
                                      float St, float Md, float Sd, uint64_t key, uint32_t pos, float *tb, float *db,
-                                     const int *sids, float qs, int lane)
+                                     const int *sids, float qs, int lane, const float *rb = nullptr)
     {
+        if (!rb) rb = P.resid + static_cast<size_t>(b) * P.nb;  // the block masses of the residual
         float best = INFINITY;
         int bi = INT_MAX;
         for (int g = lane; 4 * g < P.nb; g += 32) {
@@ -434,7 +438,7 @@ template <int DT> struct ChainOp {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int beta = 4 * g + e;
-                W[e] = beta < P.nb ? __ldcg(&P.resid[static_cast<size_t>(b) * P.nb + beta]) : 0.f;
+                W[e] = beta < P.nb ? __ldcg(&rb[beta]) : 0.f;
             }
             uint32_t w[4];
             philox_group(w, key, STREAM_FB_BLOCK, 0, pos, static_cast<uint32_t>(g));
@@ -581,7 +585,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
 
     __device__ static void finalize(const Params &P, int b, Smem &sm, float *buf, int warp, int lane)
     {
-        const int R = P.R, g = P.gamma, nb = P.nb;
+        const int g = P.gamma, nb = P.nb;
         constexpr int NT = FWV * 32;
         float *tb = buf + warp * 2 * G, *db = tb + G;  // this warp's block buffers
         // A. Inputs that do not depend on the streaming grid: tokens, r, key
@@ -784,9 +788,35 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
 // the first accepted child is descended into; when all are rejected one
 // token is drawn from P_m (rejection trials from p_u with q scaled by s_m,
 // then the direct residual race), at a leaf the bonus from p_u.
-struct TreeIO {
-    const int32_t *parent;  // [B, N]
-    int32_t *out_nodes;     // [B, N] accepted nodes, then -1 (optional)
+// The tree's streaming pass: the chain's, except that the draft row of a
+// leaf (a node no other node hangs from) is neither loaded nor reduced.
+template <int DT> struct TreeOp : ChainOp<DT> {
+    static constexpr bool SKIPS = true;
+
+    // Draft rows: lane v holds the parent of node v.  Target rows: no load.
+    __device__ static __forceinline__ int skip_key(const ChainParams &P, long long row, int lane)
+    {
+        const long long b = row / P.R;
+        const int rho = static_cast<int>(row - b * P.R);
+        if (rho < P.nt || lane >= P.nt) return -1;
+        return __ldg(&P.tree_parent[b * P.nt + lane]);
+    }
+
+    __device__ static __forceinline__ bool skip(const ChainParams &P, long long row, int key, int)
+    {
+        const long long b = row / P.R;
+        const int u = static_cast<int>(row - b * P.R) - P.nt;
+        if (u < 0) return false;
+        return __ballot_sync(0xffffffffu, key == u) == 0u;
+    }
+
+    // Before the finalize grid (which waits for this grid) meets in its
+    // barriers: every sequence's barrier count and generation start at 0.
+    __device__ static __forceinline__ void reset(const ChainParams &P)
+    {
+        if (blockIdx.x == 0 && P.tree_bar)
+            for (int i = threadIdx.x; i < 2 * P.B; i += blockDim.x) P.tree_bar[i] = 0u;
+    }
 };
 
 template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
@@ -797,13 +827,13 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
     static constexpr int FIN_WARPS = FWV;
     static constexpr int FIN_BUF_FLOATS = 2 * FWV * G;
 
-    __device__ static void write_bad_tree(const Params &P, const TreeIO &T, int b, int lane)
+    __device__ static void write_bad_tree(const Params &P, int b, int rank, int lane)
     {
         const int N = P.nt;
-        if (threadIdx.x < 32) {
+        if (rank == 0 && threadIdx.x < 32) {
             for (int i = lane; i < N; i += 32) {
                 P.out_tokens[static_cast<size_t>(b) * N + i] = -1;
-                if (T.out_nodes) T.out_nodes[static_cast<size_t>(b) * N + i] = -1;
+                if (P.tree_nodes) P.tree_nodes[static_cast<size_t>(b) * N + i] = -1;
             }
             if (lane == 0) {
                 P.accept_count[b] = -1;
@@ -812,14 +842,138 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
         }
     }
 
-    __device__ static void finalize(const Params &P, int b, Smem &sm, float *buf, int warp, int lane)
+    // Coefficients of one residual pass: p(x) = ex2(z c2 - mt) ps and
+    // q(x) = ex2(z' c2 - md) qs, with mt = Mt c2 rounded and its rounding
+    // (delta = Mt c2 - mt, exact by FMA) folded into ps as 2^-delta, likewise
+    // for the draft row, whose scale also carries the weight s.  One FFMA and
+    // one ex2 per probability; identical target and draft rows still give
+    // exactly p = q at s = 1.
+    struct ResidCoef {
+        float c2, mt, md, ps, qs;
+    };
+
+    __device__ static __forceinline__ ResidCoef resid_coef(const Params &P, float Mt, float St, float Md, float Sd,
+                                                           float s)
     {
-        finalize_tree(P, TreeIO{P.tree_parent, P.tree_nodes}, b, sm, buf, warp, lane);
+        constexpr float LN2 = 0.6931471805599453f;
+        ResidCoef c;
+        c.c2 = P.c2;
+        c.mt = Mt * P.c2;
+        c.md = Md * P.c2;
+        const float dt = fmaf(Mt, P.c2, -c.mt), dd = fmaf(Md, P.c2, -c.md);
+        c.ps = __fmul_rn(1.f / St, fmaf(-dt, LN2, 1.f));
+        c.qs = __fmul_rn(__fmul_rn(1.f / Sd, fmaf(-dd, LN2, 1.f)), s);
+        return c;
     }
 
-    __device__ static void finalize_tree(const Params &P, const TreeIO &T, int b, Smem &sm, float *buf, int warp,
-                                         int lane)
+    __device__ static __forceinline__ float rterm(float zt, float zd, const ResidCoef &c)
     {
+        const float p = __fmul_rn(fast_exp2(fmaf(zt, c.c2, -c.mt)), c.ps);
+        const float q = __fmul_rn(fast_exp2(fmaf(zd, c.c2, -c.md)), c.qs);
+        return fmaxf(__fsub_rn(p, q), 0.f);
+    }
+
+    // Residual mass of block beta, sum over x of max(0, p(x) - s q(x)) (this
+    // lane's share); 16-byte loads when the rows are 16-byte aligned, the
+    // ragged tail padded with -inf logits (mass 0).
+    __device__ static __forceinline__ float block_resid(const Params &P, const unsigned char *tp,
+                                                        const unsigned char *dp, int beta, const ResidCoef &rc,
+                                                        int lane)
+    {
+        const int lo = beta * G, hi = min(P.V, lo + G);
+        float pa[4] = {0.f, 0.f, 0.f, 0.f};
+        if (P.vec) {
+            if constexpr (DT == 0) {
+                const float4 *t4 = reinterpret_cast<const float4 *>(tp) + lo / 4;
+                const float4 *d4 = reinterpret_cast<const float4 *>(dp) + lo / 4;
+                const int n4 = (hi - lo) >> 2;
+#pragma unroll
+                for (int h = 0; h < G / 512; ++h) {
+                    float4 a[4], c[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int i = lane + 32 * (4 * h + j);
+                        if (i < n4) {
+                            a[j] = __ldcg(t4 + i);
+                            c[j] = __ldcg(d4 + i);
+                        } else {
+                            a[j] = c[j] = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        pa[0] += rterm(a[j].x, c[j].x, rc);
+                        pa[1] += rterm(a[j].y, c[j].y, rc);
+                        pa[2] += rterm(a[j].z, c[j].z, rc);
+                        pa[3] += rterm(a[j].w, c[j].w, rc);
+                    }
+                }
+            } else {
+                const uint4 *t8 = reinterpret_cast<const uint4 *>(tp) + lo / 8;
+                const uint4 *d8 = reinterpret_cast<const uint4 *>(dp) + lo / 8;
+                const int n8 = (hi - lo) >> 3;
+                constexpr unsigned NEG = 0xff80ff80u;  // two bf16 -inf
+                uint4 a[G / 256], c[G / 256];
+#pragma unroll
+                for (int j = 0; j < G / 256; ++j) {
+                    const int i = lane + 32 * j;
+                    if (i < n8) {
+                        a[j] = __ldcg(t8 + i);
+                        c[j] = __ldcg(d8 + i);
+                    } else {
+                        a[j] = c[j] = make_uint4(NEG, NEG, NEG, NEG);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < G / 256; ++j) {
+                    const unsigned wa[4] = {a[j].x, a[j].y, a[j].z, a[j].w}, wc[4] = {c[j].x, c[j].y, c[j].z, c[j].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        pa[e] += rterm(__uint_as_float(wa[e] << 16), __uint_as_float(wc[e] << 16), rc);
+                        pa[e] += rterm(__uint_as_float(wa[e] & 0xffff0000u), __uint_as_float(wc[e] & 0xffff0000u), rc);
+                    }
+                }
+            }
+        } else {
+            for (int x = lo + lane; x < hi; x += 32)
+                pa[0] += rterm(DType<DT>::load(tp, x), DType<DT>::load(dp, x), rc);
+        }
+        return (pa[0] + pa[1]) + (pa[2] + pa[3]);
+    }
+
+    // Residual pass j of sequence b: the block masses of max(0, p_u - s q_u),
+    // the blocks split over the sequence's cs CTAs (buffer j % 2, so a pass
+    // never overwrites masses another CTA may still be summing), then in
+    // every CTA N = their sum in one fixed order (identical in all of them).
+    __device__ static bool tree_pass(const Params &P, int b, int rank, int j, const unsigned char *tp,
+                                     const unsigned char *dp, float Mt, float St, float Md, float Sd, float s, Smem &sm,
+                                     int warp, int lane)
+    {
+        float *rb = P.resid + (static_cast<size_t>(b) * 2 + (j & 1)) * P.nb;
+        const ResidCoef rc = resid_coef(P, Mt, St, Md, Sd, s);
+        for (int beta = rank * FWV + warp; beta < P.nb; beta += P.cs * FWV) {
+            const float part = warp_sum(block_resid(P, tp, dp, beta, rc, lane));
+            if (lane == 0) rb[beta] = part;
+        }
+        bool ok = true;
+        if (P.cs > 1) ok = group_barrier<FWV * 32>(P.tree_bar + 2 * b, static_cast<unsigned>(P.cs), P.err, &sm.gflag);
+        else fin_sync<FWV>();
+        if (warp == 0) {
+            float z = 0.f;
+            for (int beta = lane; beta < P.nb; beta += 32) z += __ldcg(&rb[beta]);
+            z = warp_sum(z);
+            if (lane == 0) sm.Z = z;
+        }
+        fin_sync<FWV>();
+        return ok;
+    }
+
+    // Group g = b * cs + rank: CTA `rank` of sequence b.  Every CTA of the
+    // sequence walks the tree and takes the same decisions from the same
+    // values; rank 0 writes the outputs.
+    __device__ static void finalize(const Params &P, int g, Smem &sm, float *buf, int warp, int lane)
+    {
+        const int b = g / P.cs, rank = g - b * P.cs;
         const int N = P.nt, nb = P.nb;
         float *tb = buf + warp * 2 * G, *db = tb + G;
         // A. Inputs: parents, tokens, uniforms, and each node's token logit
@@ -831,7 +985,7 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
         }
         if (warp == 0 && lane < N) {
             const int v = lane;
-            const int pv = T.parent[static_cast<size_t>(b) * N + v];
+            const int pv = P.tree_parent[static_cast<size_t>(b) * N + v];
             const int x = P.tokens[static_cast<size_t>(b) * N + v];
             sm.par[v] = pv;
             sm.x[v] = x;
@@ -847,25 +1001,24 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
         // B. Row statistics; a bad target row, or a bad draft row of a node
-        //    with children, makes the sequence bad.
+        //    with children, makes the sequence bad (a leaf's draft row was
+        //    not streamed and is not looked at).
         Base::template merge_stats<FWV>(P, b, sm, N, false, warp, lane);
         fin_sync<FWV>();
         if (warp == 0 && !sm.bad) {
             bool bad = lane < N && !(sm.S[lane] > 0.f);
-            // the draft row of u matters iff some node has parent u
             for (int v = 1; v < N; ++v)
                 if (lane == sm.par[v] && !(sm.S[N + lane] > 0.f)) bad = true;
             if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&sm.bad, 1);
         }
         fin_sync<FWV>();
         if (sm.bad) {
-            write_bad_tree(P, T, b, lane);
+            write_bad_tree(P, b, rank, lane);
             return;
         }
-        // C. The walk.  Every thread follows the same decisions (from shared
-        //    values); residual passes and draws use the CTA.
+        // C. The walk.
         const uint64_t key = sm.key;
-        int u = 0, k = 0, res = -1;
+        int u = 0, k = 0, res = -1, pass = 0;
         for (;;) {
             const unsigned kids = __ballot_sync(0xffffffffu, lane < N && lane > u && sm.par[lane] == u);
             const float Mt = sm.M[u], St = sm.S[u];
@@ -900,19 +1053,25 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
                     next = c;
                     break;
                 }
-                // rejected: the next residual and its mass N_m
+                // rejected: the next residual.  Its mass N_m is needed for the
+                // next child's test; after the last child the draw below
+                // needs only s (the pass runs there if the trials all fail).
                 sres += Nm;
-                Fin::residual_pass(P, b, tp, dp, Mt, St, Md, Sd, sm, warp, lane, tb, 0, sres);
+                if ((m & (m - 1u)) == 0u) break;
+                if (!tree_pass(P, b, rank, pass++, tp, dp, Mt, St, Md, Sd, sres, sm, warp, lane)) {
+                    write_bad_tree(P, b, rank, lane);  // a CTA of the sequence did not arrive (error flag set)
+                    return;
+                }
                 Nm = sm.Z;
                 if (!(Nm > 0.f)) {  // no residual mass (a token outside q's support)
-                    write_bad_tree(P, T, b, lane);
+                    write_bad_tree(P, b, rank, lane);
                     return;
                 }
             }
             if (next >= 0) {
-                if (threadIdx.x == 0) {
+                if (rank == 0 && threadIdx.x == 0) {
                     P.out_tokens[static_cast<size_t>(b) * N + k] = sm.x[next];
-                    if (T.out_nodes) T.out_nodes[static_cast<size_t>(b) * N + k] = next;
+                    if (P.tree_nodes) P.tree_nodes[static_cast<size_t>(b) * N + k] = next;
                 }
                 ++k;
                 u = next;
@@ -948,10 +1107,16 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
                 if (sm.result >= 0) break;
             }
             if (sm.result < 0) {
-                // the block masses of max(0, p - s q) are those of the last residual pass
+                // the direct draw: block masses of max(0, p_u - s q_u) (no
+                // mass at all leaves nothing to draw: bad row, below)
+                if (!tree_pass(P, b, rank, pass++, tp, dp, Mt, St, Md, Sd, sres, sm, warp, lane)) {
+                    write_bad_tree(P, b, rank, lane);
+                    return;
+                }
                 if (warp == 0) {
+                    const float *rb = P.resid + (static_cast<size_t>(b) * 2 + ((pass - 1) & 1)) * nb;
                     const int x = Base::race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(u), tb, db,
-                                                   nullptr, sres, lane);
+                                                   nullptr, sres, lane, rb);
                     if (lane == 0) sm.result = x;
                 }
                 fin_sync<FWV>();
@@ -960,13 +1125,13 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
             break;
         }
         if (res < 0) {
-            write_bad_tree(P, T, b, lane);
+            write_bad_tree(P, b, rank, lane);
             return;
         }
-        if (threadIdx.x < 32) {
+        if (rank == 0 && threadIdx.x < 32) {
             for (int i = k + lane; i < N; i += 32) {
                 P.out_tokens[static_cast<size_t>(b) * N + i] = (i == k) ? res : -1;
-                if (T.out_nodes) T.out_nodes[static_cast<size_t>(b) * N + i] = -1;
+                if (P.tree_nodes) P.tree_nodes[static_cast<size_t>(b) * N + i] = -1;
             }
             if (lane == 0) {
                 P.accept_count[b] = k;
@@ -1320,7 +1485,8 @@ size_t tree_ws_bytes(int B, int N, int V)
     const size_t nb = blocks_per_row(V), R = 2 * static_cast<size_t>(N);
     size_t n = WS_HEADER;
     n += align256(static_cast<size_t>(B) * R * nb * 8);  // block statistics
-    n += align256(static_cast<size_t>(B) * nb * 4);      // residual block masses
+    n += align256(static_cast<size_t>(B) * 2 * nb * 4);  // residual block masses, two buffers
+    n += align256(static_cast<size_t>(B) * 2 * 4);       // barrier of each sequence's finalize CTAs
     const size_t gr = WS_HEADER + align256(static_cast<size_t>(B) * N * nb * 8);
     return n > gr ? n : gr;
 }
@@ -1364,6 +1530,8 @@ cudaError_t launch_tree(const TreeLaunch &L, cudaStream_t st)
     P.stats = reinterpret_cast<float2 *>(ws + off);
     off += align256(static_cast<size_t>(L.B) * P.R * P.nb * 8);
     P.resid = reinterpret_cast<float *>(ws + off);
+    off += align256(static_cast<size_t>(L.B) * 2 * P.nb * 4);
+    P.tree_bar = reinterpret_cast<unsigned *>(ws + off);
     P.target = static_cast<const unsigned char *>(L.target);
     P.draft = static_cast<const unsigned char *>(L.draft);
     P.tokens = L.tokens;
@@ -1381,12 +1549,17 @@ cudaError_t launch_tree(const TreeLaunch &L, cudaStream_t st)
     int sms = 0;
     cudaError_t e = device_sm_count(&sms);
     if (e != cudaSuccess) return e;
+    // The walk's residual passes (one per rejected child) are split over a
+    // cluster of cs CTAs per sequence, as many as the idle SMs allow (<= 8).
+    int cs = 1;
+    while (cs < 8 && L.B * cs * 2 <= sms) cs *= 2;
+    P.cs = cs;
     const bool wide = L.B <= sms;
     if (L.dtype == 0)
-        return wide ? launch_stream_finalize<ChainOp<0>, TreeFin<0, FW>, 0>(P, L.tma, L.B, st)
-                    : launch_stream_finalize<ChainOp<0>, TreeFin<0, NCW>, 0>(P, L.tma, L.B, st);
-    return wide ? launch_stream_finalize<ChainOp<1>, TreeFin<1, FW>, 1>(P, L.tma, L.B, st)
-                : launch_stream_finalize<ChainOp<1>, TreeFin<1, NCW>, 1>(P, L.tma, L.B, st);
+        return wide ? launch_stream_finalize<TreeOp<0>, TreeFin<0, FW>, 0>(P, L.tma, L.B * cs, st, cs)
+                    : launch_stream_finalize<TreeOp<0>, TreeFin<0, NCW>, 0>(P, L.tma, L.B, st);
+    return wide ? launch_stream_finalize<TreeOp<1>, TreeFin<1, FW>, 1>(P, L.tma, L.B * cs, st, cs)
+                : launch_stream_finalize<TreeOp<1>, TreeFin<1, NCW>, 1>(P, L.tma, L.B, st);
 }
 
 }  // namespace spv

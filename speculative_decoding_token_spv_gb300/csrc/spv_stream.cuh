@@ -19,6 +19,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 namespace spv {
 
 constexpr int G = 1024;                       // sampler block: tokens per block
@@ -148,6 +150,49 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity)
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
+{
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Barrier of the n CTAs of one thread-block cluster (co-scheduled, so every
+// one of them arrives) through global memory: bar[0] counts arrivals and is
+// reset by the last one, which then advances the generation bar[1].  Called
+// by all `threads` threads of each CTA (named barrier 1); global writes made
+// before it are visible to every CTA after it.  The wait is bounded: false
+// (and STATUS_TIMEOUT in *err) if it gave up.
+template <int THREADS_> __device__ __forceinline__ bool group_barrier(unsigned *bar, unsigned n, unsigned *err,
+                                                                      int *sh_flag)
+{
+    __threadfence();
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS_) : "memory");
+    if (threadIdx.x == 0) {
+        int ok = 1;
+        const unsigned g0 = ld_acquire_gpu(bar + 1);
+        __threadfence();
+        if (atomicAdd(bar, 1u) == n - 1u) {
+            atomicExch(bar, 0u);
+            __threadfence();
+            atomicAdd(bar + 1, 1u);
+        } else {
+            for (uint32_t i = 0; ld_acquire_gpu(bar + 1) == g0; ++i) {
+                if (i == WAIT_LIMIT) {
+                    atomicExch(err, STATUS_TIMEOUT);
+                    ok = 0;
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __threadfence();
+        *sh_flag = ok;
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS_) : "memory");
+    return *reinterpret_cast<volatile int *>(sh_flag) != 0;
 }
 
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
@@ -369,6 +414,20 @@ __device__ __forceinline__ void load_block_global(float v[32], const void *blk, 
 //   finalize(P, g, sm, warp, lane)       merge + outputs of group g (run by
 //                                        finalize_kernel, one CTA per group);
 //   struct Smem                          shared scratch of finalize.
+// and optionally (SKIPS = true) rows it does not read at all:
+//   skip_key(P, row, lane)               a per-lane input of skip(), read
+//                                        from global memory one item ahead;
+//   skip(P, row, key, lane)              warp-uniform: the row is skipped;
+//   reset(P)                             run by every thread at the start.
+// Producer and consumers take the same decisions, so a skipped item uses
+// no ring stage.
+template <class Op, class = void> struct OpSkips {
+    static constexpr bool value = false;
+};
+template <class Op> struct OpSkips<Op, std::void_t<decltype(Op::SKIPS)>> {
+    static constexpr bool value = Op::SKIPS;
+};
+
 template <class Op, int DT, bool TMA>
 __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const typename Op::Params P)
 {
@@ -396,8 +455,50 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
 
     const long long total = P.total_items;
     const int nc = P.nc;
+    if constexpr (OpSkips<Op>::value) Op::reset(P);
 
+    constexpr bool SK = OpSkips<Op>::value;
     if (warp == NCW) {  // ---------------- producer
+        if constexpr (SK) {
+            if (TMA) {  // the whole warp walks the items (skip() is a warp vote); lane 0 copies
+                const uint64_t pol = l2_evict_first_policy();
+                int i = 0;
+                long long it = blockIdx.x;
+                int key = it < total ? Op::skip_key(P, it / nc, lane) : 0;
+                for (; it < total; it += gridDim.x) {
+                    const long long row = it / nc;
+                    const long long nx = it + gridDim.x;
+                    const int nkey = nx < total ? Op::skip_key(P, nx / nc, lane) : 0;
+                    const bool skip = Op::skip(P, row, key, lane);
+                    key = nkey;
+                    if (skip) continue;
+                    const int s = i % S;
+                    const uint32_t ph = (i / S) & 1;
+                    int stop = 0;
+                    if (lane == 0) {
+                        if (!mbar_wait(&empty_bar[s], ph ^ 1u)) {
+                            atomicExch(P.err, STATUS_TIMEOUT);
+                            sh_abort = 1;
+                            stop = 1;
+                        } else if (sh_abort) {
+                            stop = 1;
+                        } else {
+                            const int c = static_cast<int>(it - row * nc);
+                            const int n = min(CHUNK, P.V - c * CHUNK);
+                            const unsigned char *src = reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) +
+                                                       static_cast<size_t>(c) * CHUNK_BYTES;
+                            mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(n * EB));
+                            bulk_g2s(ring + s * CHUNK_BYTES, src, static_cast<uint32_t>(n * EB), &full_bar[s], pol);
+                        }
+                    }
+                    if (__shfl_sync(0xffffffffu, stop, 0)) break;
+                    ++i;
+                }
+                if (lane == 0)
+                    for (int k = max(0, i - S); k < i; ++k) mbar_wait(&full_bar[k % S], (k / S) & 1);
+            }
+            return;
+        }
         if (TMA && lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
             int i = 0;
@@ -426,7 +527,16 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
 
     // ---------------- consumers
     int i = 0;
-    for (long long it = blockIdx.x; it < total; it += gridDim.x, ++i) {
+    int key = 0;
+    if constexpr (SK) key = blockIdx.x < total ? Op::skip_key(P, blockIdx.x / nc, lane) : 0;
+    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+        if constexpr (SK) {
+            const long long nx = it + gridDim.x;
+            const int nkey = nx < total ? Op::skip_key(P, nx / nc, lane) : 0;
+            const bool skip = Op::skip(P, it / nc, key, lane);
+            key = nkey;
+            if (skip) continue;
+        }
         const int s = i % S;
         const uint32_t ph = (i / S) & 1;
         bool ok = true;
@@ -458,6 +568,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
             // A timed-out wait anywhere stops every consumer warp together.
             if (__any_sync(0xffffffffu, sh_abort != 0)) break;
         }
+        ++i;
     }
 }
 
@@ -496,7 +607,8 @@ static inline cudaError_t device_sm_count(int *out)
 // by the item count) and then the finalize grid of Fin, `groups` CTAs, as a
 // programmatic dependent launch on the same stream.
 template <class Op, class Fin, int DT>
-static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma, int groups, cudaStream_t st)
+static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma, int groups, cudaStream_t st,
+                                          int cluster = 1)
 {
     void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
     const int smem = tma ? stages<DT>(Op::CTAS_PER_SM) * CHUNK * DType<DT>::BYTES : 0;
@@ -533,11 +645,18 @@ static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma
     cfg.blockDim = dim3(Fin::FIN_WARPS * 32);
     cfg.dynamicSmemBytes = Fin::FIN_BUF_FLOATS * 4;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    if (cluster > 1) {  // finalize CTAs g*cluster .. g*cluster+cluster-1 co-scheduled as one cluster
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
     return cudaLaunchKernelEx(&cfg, finalize_kernel<Fin, DT>, P);
 }
 

@@ -186,3 +186,13 @@ def test_invalid_arguments(spv):
     with pytest.raises(spv.SpvError):
         spv.spv_verify_tree(big, big, par, torch.zeros_like(par), torch.ones(1, 33, device="cuda"),
                             torch.zeros(1, dtype=torch.int64, device="cuda"), 1.0)
+
+
+@pytest.mark.parametrize("B", [8, 40, 80, 200])
+def test_finalize_split_over_clusters(spv, B):
+    """The walk's residual passes run on a cluster of CTAs per sequence, as
+    many as the idle SMs allow (8 at B = 8, 2 at B = 40, 1 at B = 80, and
+    the narrow finalize at B = 200): the same outcomes as the oracle."""
+    w = workloads.tree(B=B, shape="w4", V=30000, dtype=torch.float32, device="cuda", d_std=2.0)
+    got, ref = check_tree(spv, w)
+    assert (ref["accept_count"] == 0).any()

@@ -84,6 +84,17 @@ MUTANTS = {
     "tree_shift_by_one": ("            s += Nm;\n", "            s += 1.0;\n", ["test_tree_root_acceptance_closed_form"]),
     "tree_residual_unnormalised": ("(px - s * qx) / Nm : 0.0);", "(px - s * qx) : 0.0);",
                                    ["test_tree_root_acceptance_closed_form"]),
+    "tree_greedy_last_child": ("if (parent[c] == u && tok[c] == a) { next = c; break; }",
+                               "if (parent[c] == u && tok[c] == a) { next = c; }",
+                               ["test_tree_greedy_walk"]),
+    "tree_bonus_position": ("emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,\n"
+                            "                                  (uint32_t)u, &margin);",
+                            "emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,\n"
+                            "                                  (uint32_t)0, &margin);",
+                            ["test_tree_path_is_the_chain"]),
+    "tree_draw_ignores_shift": ("emitted = tree_trials(w, du, V, T, Md, Sd, s, seq_key,",
+                                "emitted = tree_trials(w, du, V, T, Md, Sd, 1.0, seq_key,",
+                                ["test_tree_first_token_is_exact"]),
     "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
                        ["test_fanout_sizes_golden"]),
 }
@@ -99,6 +110,8 @@ def _calls(name):
         return [lambda: fn(1.0)]
     if name == "test_tree_root_acceptance_closed_form":
         return [lambda: fn(2), lambda: fn(4)]
+    if name == "test_tree_first_token_is_exact":
+        return [lambda: fn(3), lambda: fn(4)]
     if name == "test_saguaro_draft_probabilities":
         return [lambda: fn(2.0), lambda: fn(8.0)]
     if name == "test_filtered_acceptance_rate_is_one_minus_tvd":

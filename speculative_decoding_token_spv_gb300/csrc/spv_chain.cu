@@ -135,7 +135,7 @@ template <int DT> struct ChainOp {
         return row_of(P, b, static_cast<int>(row - static_cast<long long>(b) * P.R));
     }
 
-    static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 3;
+    static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 4;
 
     // From the staged block.  bf16 stays packed for the max (bf16x2 max,
     // NaN ignored like fmaxf) and is widened only for the exponentials.
@@ -1175,15 +1175,73 @@ template <int DT> struct GreedyOp {
         return P.target + static_cast<size_t>(row) * static_cast<size_t>(P.V) * EB;
     }
 
-    static constexpr int CTAS_PER_SM = 2;
+    static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 4;
 
     __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta,
                                                       const unsigned char *blk, int valid, int lane)
     {
-        float v[32];
-        load_block_smem<DT>(v, blk, lane);
-        mask_tail<DT>(v, valid, lane);
-        block(P, row, beta, v, valid, lane);
+        if constexpr (DT == 0) {
+            float v[32];
+            load_block_smem<DT>(v, blk, lane);
+            mask_tail<DT>(v, valid, lane);
+            block(P, row, beta, v, valid, lane);
+        } else {
+            block_bf16(P, row, beta, blk, valid, lane);
+        }
+    }
+
+    // bf16 from the staged block, packed: the block max by bf16x2 max with
+    // NaN propagation, then the first id holding it (ids rise with the word
+    // index within a lane, so the first match is the smallest; -0.0 == +0.0).
+    __device__ static __forceinline__ void block_bf16(const Params &P, long long row, int beta,
+                                                      const unsigned char *blk, int valid, int lane)
+    {
+        uint32_t w[16];
+        const uint4 *p = reinterpret_cast<const uint4 *>(blk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 t = p[j * 32 + lane];
+            w[4 * j] = t.x;
+            w[4 * j + 1] = t.y;
+            w[4 * j + 2] = t.z;
+            w[4 * j + 3] = t.w;
+        }
+        if (valid < G) {  // element 2h / 2h+1 of word h of vector j: j*256 + lane*8 + 2h (+1)
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int e0 = (q >> 2) * 256 + lane * 8 + 2 * (q & 3);
+                if (e0 >= valid) w[q] = (w[q] & 0xffff0000u) | 0xff80u;
+                if (e0 + 1 >= valid) w[q] = (w[q] & 0x0000ffffu) | 0xff800000u;
+            }
+        }
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(w);
+        __nv_bfloat162 mx[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx[a] = __hmax2_nan(h[a], h[a + 8]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) mx[a] = __hmax2_nan(mx[a], mx[a + 4]);
+        mx[0] = __hmax2_nan(__hmax2_nan(mx[0], mx[1]), __hmax2_nan(mx[2], mx[3]));
+        const float lo = __low2float(mx[0]), hi = __high2float(mx[0]);
+        const bool nan = __any_sync(0xffffffffu, isnan(lo) || isnan(hi));
+        const float m = warp_max(fmaxf(lo, hi));
+        int i = INT_MAX;
+        if (!nan && m != -INFINITY && m != INFINITY) {
+            const __nv_bfloat162 mm = __float2bfloat162_rn(m);  // exact: m is one of the bf16 values
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const unsigned e = __heq2_mask(h[q], mm);
+                const int id0 = (q >> 2) * 256 + lane * 8 + 2 * (q & 3);
+                const int c = (e & 0xffffu) ? id0 : ((e >> 16) ? id0 + 1 : INT_MAX);
+                i = min(i, c);
+            }
+            i = static_cast<int>(__reduce_min_sync(0xffffffffu, static_cast<unsigned>(i)));
+        }
+        if (lane == 0) {
+            int2 o;
+            if (nan || m == INFINITY) o = make_int2(0x7fc00000, -2);
+            else o = make_int2(__float_as_int(m), i == INT_MAX ? INT_MAX : beta * G + i);
+            P.best[row * P.nb + beta] = o;
+        }
     }
 
     // Per-block (max, first argmax): four independent accumulators over the

@@ -247,7 +247,7 @@ __device__ __forceinline__ float max_nan(float a, float b)
 template <int DT> struct FiltOp {
     using Params = FiltParams;
     static constexpr int EB = DType<DT>::BYTES;
-    static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 3;
+    static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 4;
 
     __device__ static __forceinline__ const void *row_ptr(const Params &P, long long row)
     {

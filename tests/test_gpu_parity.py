@@ -282,3 +282,32 @@ def test_zero_residual_mass_is_a_bad_row(spv, dtype):
     w = _to(w, "cuda")
     got, ref = check_chain(spv, w, want_Z=True, expect_bad=[0, 1])
     assert list(_np(got["accept_count"])) == [-1, -1, 2]
+
+
+@pytest.mark.parametrize("V", [1032, 5000, 1001])
+def test_greedy_bf16_edges(spv, V):
+    """Greedy on bf16 rows (packed max with NaN propagation, then the first id
+    holding it): a maximum of zero reached by -0.0 before +0.0, NaN, +inf, an
+    all -inf row, a single finite logit, the maximum in the ragged tail, and
+    the maximum tied across blocks.  V = 1001 takes the plain-load path."""
+    gen = torch.Generator(device="cpu").manual_seed(61 + V)
+    B, g = 8, 2
+    z = torch.randint(-3, 3, (B, g + 1, V), generator=gen).float()
+    z[0] = -torch.randint(0, 3, (g + 1, V), generator=gen).float()   # max 0
+    z[0, :, 3] = -0.0
+    z[0, :, 9] = 0.0
+    z[1, 1, V // 2] = float("nan")
+    z[2, 0, 17] = float("inf")
+    z[3, 2] = float("-inf")
+    z[4] = float("-inf")
+    z[4, :, V - 5] = -1.0
+    z[5, :, V - 1] = 9.0
+    z[6, :, 40] = 7.0
+    z[6, :, min(V - 1, 3 * 1024 + 5)] = 7.0
+    a = z.nan_to_num(nan=0.0).argmax(dim=2)
+    tok = a[:, :g].to(torch.int32).clone()
+    w = workloads.ChainInputs("bf16_edges", z.to(torch.bfloat16).cuda(), z[:, :g].to(torch.bfloat16).cuda(),
+                              tok.cuda(), None, None, 0.0)
+    got, ref = check_chain(spv, w, expect_bad=[1, 2, 3])
+    ok = ref["status"] == 0
+    assert (ref["accept_count"][ok] == g).all()

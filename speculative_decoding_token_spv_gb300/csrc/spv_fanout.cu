@@ -68,8 +68,8 @@ template <int DT> struct FanoutOp {
     // Top-F of a block staged in shared memory.  The F-th largest of the 32
     // lane maxima bounds the block's F-th largest key from below (F distinct
     // elements reach it), so only elements at or above it can be in the
-    // top F; the F rounds then visit only those (keys re-read from the
-    // staged block).  F > 32 visits every element.
+    // top F (keys re-read from the staged block).  F > 32 visits every
+    // element.
     __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta,
                                                       const unsigned char *blk, int valid, int lane)
     {
@@ -116,6 +116,54 @@ template <int DT> struct FanoutOp {
         uint32_t mask = 0;
 #pragma unroll
         for (int e = 0; e < 32; ++e) mask |= (key[e] >= thr ? 1u : 0u) << e;
+        // Usually few elements reach the threshold: compact them (<= 64) into
+        // the warp's shared slots, sort the 64-bit keys once (bitonic, two per
+        // lane, descending) and keep the first F.  Otherwise F rounds of a
+        // warp max over the candidates.
+        __shared__ uint64_t slots[NCW][64];
+        const int n = __popc(mask);
+        int pre = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, pre, o);
+            if (lane >= o) pre += y;
+        }
+        const int total = __shfl_sync(0xffffffffu, pre, 31);
+        if (F <= 32 && total <= 64) {
+            const int warp = threadIdx.x >> 5;
+            uint64_t *sl = slots[warp];
+            int pos = pre - n;
+            for (uint32_t m = mask; m; m &= m - 1) {
+                const int e = __ffs(m) - 1;
+                sl[pos++] = cand_key(smem_key(blk, lane, e, valid, base, ex), base + lane_index<DT>(lane, e));
+            }
+            __syncwarp();
+            uint64_t a = lane < total ? sl[lane] : 0ull, c = lane + 32 < total ? sl[lane + 32] : 0ull;
+            __syncwarp();
+            // element i = lane (a) and i = lane + 32 (c); descending bitonic network over 64
+#pragma unroll
+            for (int kk = 2; kk <= 64; kk <<= 1) {
+#pragma unroll
+                for (int j = kk >> 1; j > 0; j >>= 1) {
+                    if (j == 32) {
+                        // partner of i is i + 32 (same lane): i = lane < 32 is the lower one
+                        const bool desc = (lane & kk) == 0;  // kk == 64: whole sequence descending
+                        const uint64_t hi = a > c ? a : c, lo = a > c ? c : a;
+                        a = desc ? hi : lo;
+                        c = desc ? lo : hi;
+                    } else {
+                        const uint64_t oa = __shfl_xor_sync(0xffffffffu, a, j);
+                        const uint64_t oc = __shfl_xor_sync(0xffffffffu, c, j);
+                        const bool lower = (lane & j) == 0;
+                        const bool da = ((lane & kk) == 0), dc = (((lane + 32) & kk) == 0);
+                        a = (lower == da) ? (a > oa ? a : oa) : (a < oa ? a : oa);
+                        c = (lower == dc) ? (c > oc ? c : oc) : (c < oc ? c : oc);
+                    }
+                }
+            }
+            if (lane < F) out[lane] = a;
+            return;
+        }
         uint64_t prev = ~0ull;
         for (int t = 0; t < F; ++t) {
             uint64_t best = 0;

@@ -613,6 +613,11 @@ def profile_case(args):
         ws = spv.new_workspace(spv.spv_fanout_workspace_bytes(fw.draft.shape[0], 4, fw.draft.shape[2], 8), dev)
         for _ in range(args.iters):
             spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws)
+    elif name.startswith("tree"):
+        w = workloads.tree(B=B, shape=name[5:] or "k21", dtype=dt, temperature=T, device=dev)
+        ws = spv.new_workspace(spv.spv_tree_workspace_bytes(w.B, w.N, w.V), dev)
+        for _ in range(args.iters):
+            spv.spv_verify_tree(w.target, w.draft, w.parent, w.tokens, w.r, w.keys, T, workspace=ws)
     else:
         fk = dict(top_k=args.top_k, top_p=args.top_p) if args.top_k else {}
         if name == "sweep":
@@ -642,7 +647,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="spv", choices=["spv", "reference"])
     ap.add_argument("--no-variants", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-case", default=None, help="sweep | spd | eagle7 | eagle15 | fanout")
+    ap.add_argument("--profile-case", default=None, help="sweep | spd | eagle7 | eagle15 | fanout | tree_k21 | tree_w4")
     ap.add_argument("--dtype", default="float32")
     ap.add_argument("--B", type=int, default=64)
     ap.add_argument("--T", type=float, default=1.0)

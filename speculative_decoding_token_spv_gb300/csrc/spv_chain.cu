@@ -180,12 +180,18 @@ template <int DT> struct ChainOp {
         const float mu = (m == -INFINITY) ? 0.f : m;
         const float mc = mu * P.c2;
         const float delta = fmaf(mu, P.c2, -mc);
-        float sa[4] = {0.f, 0.f, 0.f, 0.f};
+        // z c2 - mc and the running sums on packed pairs (elements 2h, 2h + 1 of a word)
+        const unsigned long long c2x2 = pack2(P.c2, P.c2), nmc2 = pack2(-mc, -mc);
+        unsigned long long acc[2] = {0ull, 0ull};
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
-            sa[(2 * q) & 3] += fast_exp2(fmaf(__uint_as_float(w[q] << 16), P.c2, -mc));
-            sa[(2 * q + 1) & 3] += fast_exp2(fmaf(__uint_as_float(w[q] & 0xffff0000u), P.c2, -mc));
+            float a0, a1;
+            unpack2(ffma2(pack2(__uint_as_float(w[q] << 16), __uint_as_float(w[q] & 0xffff0000u)), c2x2, nmc2), a0, a1);
+            acc[q & 1] = fadd2(acc[q & 1], pack2(fast_exp2(a0), fast_exp2(a1)));
         }
+        float sa[4];
+        unpack2(acc[0], sa[0], sa[1]);
+        unpack2(acc[1], sa[2], sa[3]);
         float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
         s = warp_sum(s);
         if (lane == 0) {
@@ -209,9 +215,17 @@ template <int DT> struct ChainOp {
         const float mu = (m == -INFINITY) ? 0.f : m;
         const float mc = mu * P.c2;
         const float delta = fmaf(mu, P.c2, -mc);
-        float sa[4] = {0.f, 0.f, 0.f, 0.f};
+        const unsigned long long c2x2 = pack2(P.c2, P.c2), nmc2 = pack2(-mc, -mc);
+        unsigned long long acc[2] = {0ull, 0ull};
 #pragma unroll
-        for (int e = 0; e < 32; ++e) sa[e & 3] += fast_exp2(fmaf(v[e], P.c2, -mc));
+        for (int e = 0; e < 32; e += 2) {
+            float a0, a1;
+            unpack2(ffma2(pack2(v[e], v[e + 1]), c2x2, nmc2), a0, a1);
+            acc[(e >> 1) & 1] = fadd2(acc[(e >> 1) & 1], pack2(fast_exp2(a0), fast_exp2(a1)));
+        }
+        float sa[4];
+        unpack2(acc[0], sa[0], sa[1]);
+        unpack2(acc[1], sa[2], sa[3]);
         float s = (sa[0] + sa[1]) + (sa[2] + sa[3]);
         s = warp_sum(s);
         if (lane == 0) {
@@ -868,8 +882,11 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
 
     __device__ static __forceinline__ float rterm(float zt, float zd, const ResidCoef &c)
     {
-        const float p = __fmul_rn(fast_exp2(fmaf(zt, c.c2, -c.mt)), c.ps);
-        const float q = __fmul_rn(fast_exp2(fmaf(zd, c.c2, -c.md)), c.qs);
+        // (zt, zd) as a packed pair: one FMA for both exponent arguments and
+        // one multiply for both scales, each element rounded as alone
+        float at, ad, p, q;
+        unpack2(ffma2(pack2(zt, zd), pack2(c.c2, c.c2), pack2(-c.mt, -c.md)), at, ad);
+        unpack2(mul2(pack2(fast_exp2(at), fast_exp2(ad)), pack2(c.ps, c.qs)), p, q);
         return fmaxf(__fsub_rn(p, q), 0.f);
     }
 

@@ -263,10 +263,74 @@ template <int DT> struct FiltOp {
     __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta, const unsigned char *blk,
                                                       int valid, int lane)
     {
+        if constexpr (DT == 1) {
+            const float tau = __ldcg(&P.tau[row]);
+            if (__bfloat162float(__float2bfloat16_rn(tau)) == tau) {  // tau is a bf16 value: compare packed
+                scan_bf16(P, row, beta, blk, valid, lane, tau);
+                return;
+            }
+        }
         float v[32];
         load_block_smem<DT>(v, blk, lane);
         mask_tail<DT>(v, valid, lane);
         scan(P, row, beta, v, blk, valid, lane);
+    }
+
+    // bf16, packed: the lane's maximum by bf16x2 max with NaN propagation and
+    // the elements reaching tau by bf16x2 >= masks (word q holds elements
+    // 2q and 2q + 1 of the lane, as in the float copy); otherwise as scan.
+    __device__ static __forceinline__ void scan_bf16(const Params &P, long long row, int beta, const unsigned char *blk,
+                                                     int valid, int lane, float tau)
+    {
+        uint32_t w[16];
+        const uint4 *p = reinterpret_cast<const uint4 *>(blk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 t = p[j * 32 + lane];
+            w[4 * j] = t.x;
+            w[4 * j + 1] = t.y;
+            w[4 * j + 2] = t.z;
+            w[4 * j + 3] = t.w;
+        }
+        if (valid < G) {  // -inf past the row's end
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const int e0 = (q >> 2) * 256 + lane * 8 + 2 * (q & 3);
+                if (e0 >= valid) w[q] = (w[q] & 0xffff0000u) | 0xff80u;
+                if (e0 + 1 >= valid) w[q] = (w[q] & 0x0000ffffu) | 0xff800000u;
+            }
+        }
+        const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(w);
+        __nv_bfloat162 mx2[8];
+#pragma unroll
+        for (int a = 0; a < 8; ++a) mx2[a] = __hmax2_nan(h[a], h[a + 8]);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) mx2[a] = __hmax2_nan(mx2[a], mx2[a + 4]);
+        mx2[0] = __hmax2_nan(__hmax2_nan(mx2[0], mx2[1]), __hmax2_nan(mx2[2], mx2[3]));
+        const float mx = max_nan(__low2float(mx2[0]), __high2float(mx2[0]));
+        const size_t slot = static_cast<size_t>(row) * P.nb + beta;
+        const bool bad = !(mx < INFINITY);  // NaN or +inf in the lane's logits
+        if (__any_sync(0xffffffffu, bad) && lane == 0) atomicExch(&P.rbad[row], 1);
+        const bool hit = !bad && mx >= tau;
+        if (!__any_sync(0xffffffffu, hit)) {
+            if (lane == 0) P.bcnt[slot] = 0;
+            return;
+        }
+        uint32_t mask = 0;
+        if (hit) {
+            const __nv_bfloat162 t2 = __float2bfloat162_rn(tau);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const unsigned m2 = __hge2_mask(h[q], t2);
+                mask |= ((m2 & 1u) | ((m2 >> 15) & 2u)) << (2 * q);
+            }
+            if (valid < G) {  // the -inf padding is no candidate, even for tau = -inf
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    if (lane_index<DT>(lane, e) >= valid) mask &= ~(1u << e);
+            }
+        }
+        emit(P, slot, beta, blk, mask, lane);
     }
 
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int valid,
@@ -302,6 +366,14 @@ template <int DT> struct FiltOp {
                     if (lane_index<DT>(lane, e) >= valid) mask &= ~(1u << e);
             }
         }
+        emit(P, slot, beta, blk, mask, lane);
+    }
+
+    // The block's count of elements at or above tau and the keys of the first
+    // CPB (lane order, then element order within the lane).
+    __device__ static __forceinline__ void emit(const Params &P, size_t slot, int beta, const unsigned char *blk,
+                                                uint32_t mask, int lane)
+    {
         const int c = __popc(mask);
         int off = c;
 #pragma unroll

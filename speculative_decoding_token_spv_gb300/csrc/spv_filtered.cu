@@ -167,6 +167,9 @@ template <int DT>
 __global__ void __launch_bounds__(SAMPLE_BLOCKS * 32) filt_sample_kernel(const FiltParams P)
 {
     __shared__ float sv[SAMPLE_BLOCKS][64];
+    // The streaming grid may be scheduled now: its copies do not depend on
+    // this grid; its consumers wait for it (griddepcontrol.wait).
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = blockIdx.x;
     constexpr int EB = DType<DT>::BYTES;
@@ -248,6 +251,7 @@ template <int DT> struct FiltOp {
     using Params = FiltParams;
     static constexpr int EB = DType<DT>::BYTES;
     static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 4;
+    static constexpr bool WAITS_PRIOR = true;  // tau0 and the cleared flags come from filt_sample_kernel
 
     __device__ static __forceinline__ const void *row_ptr(const Params &P, long long row)
     {

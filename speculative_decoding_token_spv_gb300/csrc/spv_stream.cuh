@@ -453,6 +453,16 @@ __device__ __forceinline__ void load_block_global(float v[32], const void *blk, 
 //   reset(P)                             run by every thread at the start.
 // Producer and consumers take the same decisions, so a skipped item uses
 // no ring stage.
+// and optionally (WAITS_PRIOR = true) the consumers wait for the grid
+// launched before this one (programmatic dependent launch): the producer's
+// copies start while that grid finishes.
+template <class Op, class = void> struct OpWaitsPrior {
+    static constexpr bool value = false;
+};
+template <class Op> struct OpWaitsPrior<Op, std::void_t<decltype(Op::WAITS_PRIOR)>> {
+    static constexpr bool value = Op::WAITS_PRIOR;
+};
+
 template <class Op, class = void> struct OpSkips {
     static constexpr bool value = false;
 };
@@ -558,6 +568,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
     }
 
     // ---------------- consumers
+    if constexpr (OpWaitsPrior<Op>::value) asm volatile("griddepcontrol.wait;" ::: "memory");
     int i = 0;
     int key = 0;
     if constexpr (SK) key = blockIdx.x < total ? Op::skip_key(P, blockIdx.x / nc, lane) : 0;
@@ -642,6 +653,7 @@ template <class Op, class Fin, int DT>
 static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma, int groups, cudaStream_t st,
                                           int cluster = 1)
 {
+    constexpr bool PRIOR = OpWaitsPrior<Op>::value;
     void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
     const int smem = tma ? stages<DT>(Op::CTAS_PER_SM) * CHUNK * DType<DT>::BYTES : 0;
     // Per device and kernel variant: the shared-memory attributes and the
@@ -669,8 +681,22 @@ static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma
         if (slot) *slot = cap;
     }
     const int grid = static_cast<int>(P.total_items < cap ? P.total_items : cap);
-    kern<<<grid, THREADS, smem, st>>>(P);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (PRIOR) {  // a programmatic dependent launch on the grid before it
+        cudaLaunchConfig_t sc = {};
+        sc.gridDim = dim3(static_cast<unsigned>(grid));
+        sc.blockDim = dim3(THREADS);
+        sc.dynamicSmemBytes = static_cast<size_t>(smem);
+        sc.stream = st;
+        cudaLaunchAttribute sa[1];
+        sa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        sa[0].val.programmaticStreamSerializationAllowed = 1;
+        sc.attrs = sa;
+        sc.numAttrs = 1;
+        if ((e = cudaLaunchKernelEx(&sc, kern, P)) != cudaSuccess) return e;
+    } else {
+        kern<<<grid, THREADS, smem, st>>>(P);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(groups));

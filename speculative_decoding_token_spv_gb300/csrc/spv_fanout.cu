@@ -80,6 +80,40 @@ template <int DT> struct FanoutOp {
         const int base = beta * G;
         float v[32];
         load_block_smem<DT>(v, blk, lane);
+        uint64_t *out = P.cand + (static_cast<size_t>(row) * P.nb + beta) * P.Fmax;
+        uint32_t mask = 0;
+        if (valid == G && !(ex >= base && ex < base + G)) {
+            // A full block without the excluded id: every element is a
+            // candidate unless NaN (then the row is bad).  Lane maximum by
+            // max.NaN, the threshold among the lane maxima as floats (the
+            // order of the keys), then one compare per element.
+            float mx = v[0];
+#pragma unroll
+            for (int e = 1; e < 32; ++e) mx = max_nan(mx, v[e]);
+            if (__any_sync(0xffffffffu, mx != mx)) {
+                if (lane == 0) out[0] = ~0ull;
+                return;
+            }
+            if (F <= 32) {
+                float sv = mx;
+#pragma unroll
+                for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+                    for (int j = kk >> 1; j > 0; j >>= 1) {
+                        const float o = __shfl_xor_sync(0xffffffffu, sv, j);
+                        const bool desc = (lane & kk) == 0, lower = (lane & j) == 0;
+                        sv = (lower == desc) ? fmaxf(sv, o) : fminf(sv, o);
+                    }
+                }
+                const float t = __shfl_sync(0xffffffffu, sv, F - 1);
+#pragma unroll
+                for (int e = 0; e < 32; ++e) mask |= (v[e] >= t ? 1u : 0u) << e;
+            } else {
+                mask = 0xffffffffu;
+            }
+            select_top(P, row, beta, blk, valid, lane, ex, F, mask, out);
+            return;
+        }
         uint32_t key[32];
         bool nan = false;
         uint32_t lmax = 0;
@@ -92,7 +126,6 @@ template <int DT> struct FanoutOp {
             lmax = key[e] > lmax ? key[e] : lmax;
         }
         nan = __any_sync(0xffffffffu, nan);
-        uint64_t *out = P.cand + (static_cast<size_t>(row) * P.nb + beta) * P.Fmax;
         if (nan) {
             if (lane == 0) out[0] = ~0ull;
             return;
@@ -113,13 +146,21 @@ template <int DT> struct FanoutOp {
             const uint32_t t = __shfl_sync(0xffffffffu, sv, F - 1);
             thr = t > 1u ? t : 1u;
         }
-        uint32_t mask = 0;
 #pragma unroll
         for (int e = 0; e < 32; ++e) mask |= (key[e] >= thr ? 1u : 0u) << e;
-        // Usually few elements reach the threshold: compact them (<= 64) into
-        // the warp's shared slots, sort the 64-bit keys once (bitonic, two per
-        // lane, descending) and keep the first F.  Otherwise F rounds of a
-        // warp max over the candidates.
+        select_top(P, row, beta, blk, valid, lane, ex, F, mask, out);
+    }
+
+    // The block's top F among the candidates in mask (keys re-read from the
+    // staged block).  Usually few elements reach the threshold: compact them
+    // (<= 64) into the warp's shared slots, sort the 64-bit keys once
+    // (bitonic, two per lane, descending) and keep the first F.  Otherwise F
+    // rounds of a warp max over the candidates.
+    __device__ static __forceinline__ void select_top(const Params &P, long long row, int beta,
+                                                      const unsigned char *blk, int valid, int lane, int ex, int F,
+                                                      uint32_t mask, uint64_t *out)
+    {
+        const int base = beta * G;
         __shared__ uint64_t slots[NCW][64];
         const int n = __popc(mask);
         int pre = n;

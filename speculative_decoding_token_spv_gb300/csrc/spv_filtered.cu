@@ -236,15 +236,6 @@ __global__ void __launch_bounds__(SAMPLE_BLOCKS * 32) filt_sample_kernel(const F
 }
 
 // ------------------------------------------------------------------ 2. stream
-// max that propagates NaN (PTX max.NaN): one instruction per logit both
-// finds the block's largest logit and flags NaN.
-__device__ __forceinline__ float max_nan(float a, float b)
-{
-    float r;
-    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
-    return r;
-}
-
 // Streaming op: compare every logit with its row's tau0, record how many of
 // each block reach it and the keys of the first CPB, flag NaN / +inf.
 template <int DT> struct FiltOp {

@@ -251,6 +251,15 @@ __device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsign
     return d;
 }
 
+// max that propagates NaN (PTX max.NaN): one instruction per logit both
+// finds the largest logit and flags NaN.
+__device__ __forceinline__ float max_nan(float a, float b)
+{
+    float r;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+}
+
 __device__ __forceinline__ float fast_exp2(float x)
 {
     float y;

@@ -51,7 +51,7 @@ template <int DT> struct FanoutOp {
         return P.draft + static_cast<size_t>(row) * static_cast<size_t>(P.V) * EB;
     }
 
-    static constexpr int CTAS_PER_SM = 2;
+    static constexpr int CTAS_PER_SM = 3;
 
     // Key of element e of the lane from the staged block (the same element
     // lane_index(lane, e) as in the register copy); 0 = not a candidate.
@@ -114,6 +114,20 @@ template <int DT> struct FanoutOp {
             select_top(P, row, beta, blk, valid, lane, ex, F, mask, out);
             return;
         }
+        general_block(P, row, beta, blk, valid, lane, ex, F, out);
+    }
+
+    // The ragged tail block or the block holding the excluded id: keys with
+    // 0 for the elements that are not candidates (out of line: it runs at
+    // most twice per row and keeps its registers out of the fast path).
+    __device__ __noinline__ static void general_block(const Params &P, long long row, int beta,
+                                                      const unsigned char *blk, int valid, int lane, int ex, int F,
+                                                      uint64_t *out)
+    {
+        const int base = beta * G;
+        float v[32];
+        load_block_smem<DT>(v, blk, lane);
+        uint32_t mask = 0;
         uint32_t key[32];
         bool nan = false;
         uint32_t lmax = 0;

@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(SAMPLE_BLOCKS * 32) filt_sample_kernel(const F
 template <int DT> struct FiltOp {
     using Params = FiltParams;
     static constexpr int EB = DType<DT>::BYTES;
-    static constexpr int CTAS_PER_SM = DT == 0 ? 2 : 4;
+    static constexpr int CTAS_PER_SM = DT == 0 ? 3 : 4;
     static constexpr bool WAITS_PRIOR = true;  // tau0 and the cleared flags come from filt_sample_kernel
 
     __device__ static __forceinline__ const void *row_ptr(const Params &P, long long row)

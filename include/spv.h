@@ -341,6 +341,22 @@ double spv_fanout_size(int F0, double a, double r, int k);
  * SPV_OK, or SPV_ERR_TIMEOUT if a bounded wait in an earlier call gave up. */
 spv_status spv_workspace_status(const void *workspace, void *stream);
 
+/*
+ * spv_selftest_timeout -- self-test of the failure path of the bounded waits
+ * (no counterpart on the pages).  Every wait of the library's kernels on
+ * another CTA's progress gives up after a bounded number of polls, records
+ * SPV_ERR_TIMEOUT in the workspace's error word and returns, leaving the
+ * CUDA context usable.  This enqueues one small kernel that runs the same
+ * bounded wait on header word 1 of `workspace` (cleared first, never set),
+ * so it gives up after `polls` polls (each a global load and a short
+ * sleep) and records SPV_ERR_TIMEOUT; spv_workspace_status then reports it.
+ *   workspace        device memory, 256-byte aligned, >= 256 bytes; its
+ *                    header words 0 and 1 are overwritten
+ *   polls            1 .. 2^24
+ * Returns SPV_OK once enqueued.
+ */
+spv_status spv_selftest_timeout(void *workspace, size_t workspace_bytes, unsigned polls, void *stream);
+
 /* Human-readable name of a status code (static string). */
 const char *spv_status_string(spv_status s);
 

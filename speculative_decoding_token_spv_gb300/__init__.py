@@ -78,6 +78,8 @@ def load_library():
     lib.spv_fanout_size.argtypes = [I, ctypes.c_double, ctypes.c_double, I]
     lib.spv_fanout_size.restype = ctypes.c_double
     lib.spv_workspace_status.argtypes = [P, P]
+    lib.spv_selftest_timeout.argtypes = [P, S, ctypes.c_uint, P]
+    lib.spv_selftest_timeout.restype = I
     lib.spv_workspace_status.restype = I
     lib.spv_status_string.argtypes = [I]
     lib.spv_status_string.restype = ctypes.c_char_p
@@ -146,6 +148,16 @@ def new_workspace(nbytes: int, device) -> torch.Tensor:
 def spv_workspace_status(workspace: torch.Tensor, stream=None) -> int:
     """Device error word of a workspace (synchronises the stream)."""
     return load_library().spv_workspace_status(_ptr(workspace), _stream(stream, workspace.device))
+
+
+def spv_selftest_timeout(workspace: torch.Tensor, polls: int = 20000, stream=None) -> None:
+    """Run the library's bounded wait on a flag nothing sets (see
+    spv_selftest_timeout in spv.h): it gives up after `polls` polls and
+    records SPV_ERR_TIMEOUT in the workspace's error word."""
+    workspace = _cuda(workspace, "workspace")
+    st = load_library().spv_selftest_timeout(_ptr(workspace), workspace.numel() * workspace.element_size(),
+                                             int(polls), _stream(stream, workspace.device))
+    _check(st, "spv_selftest_timeout")
 
 
 def spv_verify_chain(target_logits, draft_logits, draft_tokens, r, sample_keys, temperature: float, *,

@@ -298,6 +298,13 @@ double spv_fanout_size(int F0, double a, double r, int k)
     return static_cast<double>(F0) * std::pow(a, static_cast<double>(k) / (1.0 + r));
 }
 
+spv_status spv_selftest_timeout(void *workspace, size_t workspace_bytes, unsigned polls, void *stream)
+{
+    if (!workspace || !aligned256(workspace) || workspace_bytes < spv::WS_HEADER) return SPV_ERR_INVALID_ARG;
+    if (polls < 1 || polls > (1u << 24)) return SPV_ERR_INVALID_ARG;
+    return cuda_status(spv::launch_selftest_wait(workspace, polls, static_cast<cudaStream_t>(stream)));
+}
+
 spv_status spv_workspace_status(const void *workspace, void *stream)
 {
     if (!workspace) return SPV_ERR_INVALID_ARG;

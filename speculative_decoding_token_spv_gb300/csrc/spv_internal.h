@@ -77,6 +77,7 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st);
 cudaError_t launch_greedy(const ChainLaunch &L, cudaStream_t st);
 cudaError_t launch_fanout(const FanoutLaunch &L, cudaStream_t st);
 cudaError_t launch_filtered(const ChainLaunch &L, cudaStream_t st);
+cudaError_t launch_selftest_wait(void *ws, unsigned polls, cudaStream_t st);
 cudaError_t launch_tree(const TreeLaunch &L, cudaStream_t st);
 
 }  // namespace spv

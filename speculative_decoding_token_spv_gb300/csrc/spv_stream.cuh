@@ -159,6 +159,20 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
     return v;
 }
 
+// Bounded wait until *flag >= target (acquire loads, short sleeps between
+// polls); false, with STATUS_TIMEOUT in *err, after `limit` polls.
+__device__ __forceinline__ bool wait_flag_ge(const unsigned *flag, unsigned target, uint32_t limit, unsigned *err)
+{
+    for (uint32_t i = 0; ld_acquire_gpu(flag) < target; ++i) {
+        if (i == limit) {
+            atomicExch(err, STATUS_TIMEOUT);
+            return false;
+        }
+        __nanosleep(32);
+    }
+    return true;
+}
+
 // Barrier of the n CTAs of one thread-block cluster (co-scheduled, so every
 // one of them arrives) through global memory: bar[0] counts arrivals and is
 // reset by the last one, which then advances the generation bar[1].  Called
@@ -179,14 +193,7 @@ template <int THREADS_> __device__ __forceinline__ bool group_barrier(unsigned *
             __threadfence();
             atomicAdd(bar + 1, 1u);
         } else {
-            for (uint32_t i = 0; ld_acquire_gpu(bar + 1) == g0; ++i) {
-                if (i == WAIT_LIMIT) {
-                    atomicExch(err, STATUS_TIMEOUT);
-                    ok = 0;
-                    break;
-                }
-                __nanosleep(32);
-            }
+            ok = wait_flag_ge(bar + 1, g0 + 1u, WAIT_LIMIT, err) ? 1 : 0;
         }
         __threadfence();
         *sh_flag = ok;

@@ -203,3 +203,13 @@ def test_tree_arguments_rejected_on_host(lib):
         assert call(**kw) == 1, kw
     n = spv.spv_tree_workspace_bytes(64, 21, 151936)
     assert n > 0 and spv.spv_tree_workspace_bytes(64, 33, 151936) == 0 and spv.spv_tree_workspace_bytes(0, 4, 10) == 0
+
+
+def test_selftest_arguments_rejected_on_host(lib):
+    P = ctypes.c_void_p
+    ws = P(1 << 20)
+    assert lib.spv_selftest_timeout(None, 4096, 10, None) == 1
+    assert lib.spv_selftest_timeout(ws, 4096, 0, None) == 1
+    assert lib.spv_selftest_timeout(ws, 4096, (1 << 24) + 1, None) == 1
+    assert lib.spv_selftest_timeout(ws, 128, 10, None) == 1
+    assert lib.spv_selftest_timeout(P((1 << 20) + 64), 4096, 10, None) == 1

@@ -24,7 +24,7 @@
  *         F_k = F_0 * a_p^(k/(1+r)), top-ranked draft tokens excluding the
  *         token already sent for verification).
  *
- * Readings where the pages leave a step open (each is listed in the design doc):
+ * Readings where the pages leave a step open:
  *   - Accept test: accept x_i iff p_i(x_i) > 0 and r_i * q_i(x_i) <= p_i(x_i),
  *     r_i in (0,1].  This is [SD] step 3 "r_i <= min(1, p/q)" without the
  *     division; p = 0 always rejects, q == p always accepts.

@@ -45,7 +45,7 @@ typedef enum {
 
 typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
 
-/* Limits of this build. */
+/* Limits of the library. */
 #define SPV_MAX_GAMMA 32     /* draft tokens per sequence */
 #define SPV_MAX_FANOUT 64    /* F_k per position */
 #define SPV_MAX_FANOUT_ROWS 64 /* K + 1 positions in the fan-out */

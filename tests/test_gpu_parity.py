@@ -1,6 +1,6 @@
 """GPU parity: libspv (through the C ABI) against the oracle, element by element.
 
-Rule (the acceptance criterion of this build): accept counts, emitted ids and
+Rule (the acceptance criterion): accept counts, emitted ids and
 fan-out ids are bit-exact, except for sequences whose oracle decision margin
 (|r - p/q| of an accept test, the log-gap of a race, |(1-v) - q/p| of a
 residual trial) is below 1e-6; such near-tie sequences are counted and must

@@ -311,3 +311,12 @@ def test_greedy_bf16_edges(spv, V):
     got, ref = check_chain(spv, w, expect_bad=[1, 2, 3])
     ok = ref["status"] == 0
     assert (ref["accept_count"][ok] == g).all()
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_statistics_not_staged(spv, dtype):
+    """gamma = 32 at V = 151,936: 33 target rows x 149 blocks exceed the
+    finalize's shared-memory staging of block statistics, so the draws read
+    them from the workspace (the other path of the block race)."""
+    w = _random_case(3, 32, 151936, dtype, 1.0, 4242, noise=0.4)
+    check_chain(spv, w, want_Z=True)

@@ -196,3 +196,22 @@ def test_finalize_split_over_clusters(spv, B):
     w = workloads.tree(B=B, shape="w4", V=30000, dtype=torch.float32, device="cuda", d_std=2.0)
     got, ref = check_tree(spv, w)
     assert (ref["accept_count"] == 0).any()
+
+
+def test_statistics_not_staged(spv):
+    """A 32-node path at V = 151,936: 32 target rows x 149 blocks exceed the
+    shared-memory staging of block statistics (the workspace path)."""
+    gen = torch.Generator(device="cpu").manual_seed(90)
+    B, N, V = 2, 32, 151936
+    z = torch.randn(B, N, V, generator=gen) * 2.0
+    d = z + 0.4 * torch.randn(B, N, V, generator=gen)
+    parent = torch.arange(-1, N - 1, dtype=torch.int32).repeat(B, 1)
+    parent[:, 5] = 0   # a second child of the root
+    tok = torch.zeros(B, N, dtype=torch.int32)
+    for v in range(1, N):
+        pv = parent[0, v].item()
+        tok[:, v] = torch.multinomial(torch.softmax(d[:, pv], dim=1), 1, generator=gen)[:, 0].int()
+    r = 1.0 - torch.rand(B, N, generator=gen)
+    keys = torch.arange(B, dtype=torch.int64) * 31337 + 5
+    w = workloads.TreeInputs("unstaged", z.cuda(), d.cuda(), parent.cuda(), tok.cuda(), r.cuda(), keys.cuda(), 1.0)
+    check_tree(spv, w)

@@ -129,3 +129,11 @@ def test_cached_bad_rows_miss(spv):
     st = _np(got["row_status"])
     assert st[1] == 4 and st[2] == 4 and st[0] == 0 and st[3] == 0
     assert _np(got["cache_slot"])[1] == -1 and _np(got["cache_slot"])[2] == -1
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+def test_cached_many_sequences(spv, T):
+    """B = 200 > the SM count: the 8-warp finalize (T > 0) with the lookup."""
+    w = workloads.sweep(B=200, V=20000, gamma=3, device="cuda", temperature=T, bonus_draft=True)
+    F = [9, 7, 5, 3]
+    check_cached(spv, w, F, _oracle_lists(w, F))

@@ -157,3 +157,11 @@ def test_max_gamma(spv):
     """gamma = 32 at B = 1: 65 rows, five row groups in the finalize."""
     w = workloads.sweep(B=1, gamma=32, device="cuda", top_k=64, top_p=0.9)
     check_filtered(spv, w, 64, 0.9)
+
+
+def test_many_sequences_narrow_finalize(spv):
+    """B = 200 > the SM count: the 8-warp finalize, two CTAs per SM."""
+    w = workloads.sweep(B=200, V=20000, gamma=2, device="cuda", top_k=40, top_p=0.95)
+    check_filtered(spv, w, 40, 0.95)
+    wb = workloads.sweep(B=200, V=20000, gamma=2, dtype=torch.bfloat16, device="cuda", top_k=8)
+    check_filtered(spv, wb, 8)

@@ -138,3 +138,12 @@ def test_bad_rows_and_arguments(spv):
     for C in (0.0, -1.0, float("inf"), float("nan")):
         with pytest.raises(spv.SpvError):
             spv.spv_verify_chain_saguaro(w.target, w.draft, w.tokens, w.r, w.keys, 1.0, ids, F, C)
+
+
+def test_many_sequences_narrow_finalize(spv):
+    """B = 200 > the SM count: the 8-warp finalize with Saguaro weights."""
+    w = workloads.sweep(B=200, V=20000, gamma=3, device="cuda", bonus_draft=True)
+    F = [12, 10, 8, 6]
+    lists = _lists(w, F)
+    w = _with_tokens(w, workloads.saguaro_tokens(w, torch.from_numpy(lists).cuda(), F, 4.0))
+    check_saguaro(spv, w, F, lists, 4.0)

@@ -53,7 +53,7 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
 #define SPV_SAMPLER_SUB 32     /* ids per sampler sub-block (part of the sampling rule) */
 #define SPV_MAX_TRIALS 64    /* residual rejection trials before the direct draw */
 #define SPV_MAX_TOP_K 64     /* top_k of spv_verify_chain_filtered */
-#define SPV_MAX_TREE_NODES 32 /* nodes of a spv_verify_tree draft tree (root included) */
+#define SPV_MAX_TREE_NODES 64 /* nodes of a spv_verify_tree draft tree (root included) */
 
 /*
  * spv_verify_chain -- [SD] steps 3 and 4 for B independent sequences.

@@ -27,7 +27,7 @@ SPV_SAMPLER_BLOCK = 1024
 SPV_SAMPLER_SUB = 32
 SPV_MAX_TRIALS = 64
 SPV_MAX_TOP_K = 64
-SPV_MAX_TREE_NODES = 32
+SPV_MAX_TREE_NODES = 64
 
 _lib = None
 

@@ -67,11 +67,11 @@ constexpr int STAT_CACHE = 4096;  // target-row block statistics staged in share
 
 struct ChainSmem {
     float2 st[STAT_CACHE];  // target rows: (block max, race factor 2^((M - m) c2) / S or -1 if empty)
-    float M[2 * 32 + 1];    // row max of the raw logits
-    float S[2 * 32 + 1];    // row sum exp((z - M)/T)
-    int x[32];              // draft tokens
-    float rr[32];           // accept uniforms
-    float zt[32], zd[32];   // target / draft logit of each draft token
+    float M[2 * 64 + 1];    // row max of the raw logits (chain: 2 gamma + 1 rows; tree: 2 N)
+    float S[2 * 64 + 1];    // row sum exp((z - M)/T)
+    int x[64];              // draft tokens (tree: node tokens)
+    float rr[64];           // accept uniforms
+    float zt[64], zd[64];   // target / draft logit of each draft token
     int bad;
     int k;
     int cached;
@@ -82,7 +82,7 @@ struct ChainSmem {
     float Z;
     uint64_t key;
     int sag_id[32][64];  // Saguaro: cached candidates of draft position i (-1: none / repeated)
-    int par[32];         // tree: parent of each node
+    int par[64];         // tree: parent of each node
 };
 
 // Barrier of the FWV warps of a chain finalize CTA.
@@ -807,13 +807,17 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
 template <int DT> struct TreeOp : ChainOp<DT> {
     static constexpr bool SKIPS = true;
 
-    // Draft rows: lane v holds the parent of node v.  Target rows: no load.
+    // Draft rows: lane v holds the parents of nodes v and v + 32 (16 bits
+    // each, 0xffff for none or the root).  Target rows: no load.
     __device__ static __forceinline__ int skip_key(const ChainParams &P, long long row, int lane)
     {
         const long long b = row / P.R;
         const int rho = static_cast<int>(row - b * P.R);
-        if (rho < P.nt || lane >= P.nt) return -1;
-        return __ldg(&P.tree_parent[b * P.nt + lane]);
+        if (rho < P.nt) return -1;
+        const int32_t *pp = P.tree_parent + b * P.nt;
+        const int p0 = lane < P.nt ? __ldg(&pp[lane]) : -1;
+        const int p1 = lane + 32 < P.nt ? __ldg(&pp[lane + 32]) : -1;
+        return (p0 & 0xffff) | (p1 << 16);
     }
 
     __device__ static __forceinline__ bool skip(const ChainParams &P, long long row, int key, int)
@@ -821,7 +825,8 @@ template <int DT> struct TreeOp : ChainOp<DT> {
         const long long b = row / P.R;
         const int u = static_cast<int>(row - b * P.R) - P.nt;
         if (u < 0) return false;
-        return __ballot_sync(0xffffffffu, key == u) == 0u;
+        const bool hit = (key & 0xffff) == u || ((key >> 16) & 0xffff) == u;
+        return __ballot_sync(0xffffffffu, hit) == 0u;
     }
 
     // Before the finalize grid (which waits for this grid) meets in its
@@ -1000,20 +1005,21 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
             sm.key = P.keys[b];
             sm.cached = (N * nb <= STAT_CACHE) ? 1 : 0;
         }
-        if (warp == 0 && lane < N) {
-            const int v = lane;
-            const int pv = P.tree_parent[static_cast<size_t>(b) * N + v];
-            const int x = P.tokens[static_cast<size_t>(b) * N + v];
-            sm.par[v] = pv;
-            sm.x[v] = x;
-            sm.rr[v] = P.r[static_cast<size_t>(b) * N + v];
-            const bool ok = (v == 0) ? (pv == -1) : (pv >= 0 && pv < v && x >= 0 && x < P.V);
-            sm.zt[v] = sm.zd[v] = 0.f;
-            if (v > 0 && ok) {
-                sm.zt[v] = DType<DT>::load(Base::row_of(P, b, pv), x);
-                sm.zd[v] = DType<DT>::load(Base::row_of(P, b, N + pv), x);
+        if (warp == 0) {
+            for (int v = lane; v < N; v += 32) {
+                const int pv = P.tree_parent[static_cast<size_t>(b) * N + v];
+                const int x = P.tokens[static_cast<size_t>(b) * N + v];
+                sm.par[v] = pv;
+                sm.x[v] = x;
+                sm.rr[v] = P.r[static_cast<size_t>(b) * N + v];
+                const bool ok = (v == 0) ? (pv == -1) : (pv >= 0 && pv < v && x >= 0 && x < P.V);
+                sm.zt[v] = sm.zd[v] = 0.f;
+                if (v > 0 && ok) {
+                    sm.zt[v] = DType<DT>::load(Base::row_of(P, b, pv), x);
+                    sm.zd[v] = DType<DT>::load(Base::row_of(P, b, N + pv), x);
+                }
+                if (!ok) atomicOr(&sm.bad, 1);
             }
-            if (!ok) atomicOr(&sm.bad, 1);
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
@@ -1023,9 +1029,11 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
         Base::template merge_stats<FWV>(P, b, sm, N, false, warp, lane);
         fin_sync<FWV>();
         if (warp == 0 && !sm.bad) {
-            bool bad = lane < N && !(sm.S[lane] > 0.f);
-            for (int v = 1; v < N; ++v)
-                if (lane == sm.par[v] && !(sm.S[N + lane] > 0.f)) bad = true;
+            bool bad = false;
+            for (int v = lane; v < N; v += 32) {
+                if (!(sm.S[v] > 0.f)) bad = true;                           // target row of v
+                if (v > 0 && !(sm.S[N + sm.par[v]] > 0.f)) bad = true;      // draft row of v's parent
+            }
             if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(&sm.bad, 1);
         }
         fin_sync<FWV>();
@@ -1037,10 +1045,14 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
         const uint64_t key = sm.key;
         int u = 0, k = 0, res = -1, pass = 0;
         for (;;) {
-            const unsigned kids = __ballot_sync(0xffffffffu, lane < N && lane > u && sm.par[lane] == u);
+            const unsigned long long kids =
+                static_cast<unsigned long long>(__ballot_sync(0xffffffffu, lane < N && lane > u && sm.par[lane] == u)) |
+                (static_cast<unsigned long long>(
+                     __ballot_sync(0xffffffffu, lane + 32 < N && lane + 32 > u && sm.par[lane + 32] == u))
+                 << 32);
             const float Mt = sm.M[u], St = sm.S[u];
             const unsigned char *tp = Base::row_of(P, b, u);
-            if (kids == 0u) {
+            if (kids == 0ull) {
                 // leaf: the bonus token from p_u (warp 0)
                 if (warp == 0) {
                     const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, 0u, static_cast<uint32_t>(u), lane);
@@ -1057,8 +1069,8 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
             const unsigned char *dp = Base::row_of(P, b, N + u);
             float sres = 0.f, Nm = 1.f;
             int next = -1;
-            for (unsigned m = kids; m; m &= m - 1u) {
-                const int c = __ffs(m) - 1;
+            for (unsigned long long m = kids; m; m &= m - 1ull) {
+                const int c = __ffsll(static_cast<long long>(m)) - 1;
                 const float px = expf((sm.zt[c] - Mt) * P.invT) / St;
                 const float qx = expf((sm.zd[c] - Md) * P.invT) / Sd;
                 float Pm = px;
@@ -1074,7 +1086,7 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
                 // next child's test; after the last child the draw below
                 // needs only s (the pass runs there if the trials all fail).
                 sres += Nm;
-                if ((m & (m - 1u)) == 0u) break;
+                if ((m & (m - 1ull)) == 0ull) break;
                 if (!tree_pass(P, b, rank, pass++, tp, dp, Mt, St, Md, Sd, sres, sm, warp, lane)) {
                     write_bad_tree(P, b, rank, lane);  // a CTA of the sequence did not arrive (error flag set)
                     return;
@@ -1176,9 +1188,9 @@ struct GreedyParams {
 };
 
 struct GreedySmem {
-    int a[33];
-    int x[32];
-    int par[32];
+    int a[65];
+    int x[64];
+    int par[64];
     int bad;
 };
 
@@ -1382,13 +1394,15 @@ template <int DT> struct GreedyTreeFin : GreedyOp<DT> {
     {
         const int N = P.R, nb = P.nb;
         if (threadIdx.x == 0) sm.bad = 0;
-        if (warp == 0 && lane < N) {
-            const int pv = P.tree_parent[static_cast<size_t>(b) * N + lane];
-            const int x = P.tokens[static_cast<size_t>(b) * N + lane];
-            sm.par[lane] = pv;
-            sm.x[lane] = x;
-            const bool ok = (lane == 0) ? (pv == -1) : (pv >= 0 && pv < lane && x >= 0 && x < P.V);
-            if (!ok) atomicOr(&sm.bad, 1);
+        if (warp == 0) {
+            for (int v = lane; v < N; v += 32) {
+                const int pv = P.tree_parent[static_cast<size_t>(b) * N + v];
+                const int x = P.tokens[static_cast<size_t>(b) * N + v];
+                sm.par[v] = pv;
+                sm.x[v] = x;
+                const bool ok = (v == 0) ? (pv == -1) : (pv >= 0 && pv < v && x >= 0 && x < P.V);
+                if (!ok) atomicOr(&sm.bad, 1);
+            }
         }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         consumer_sync();
@@ -1431,9 +1445,12 @@ template <int DT> struct GreedyTreeFin : GreedyOp<DT> {
         }
         int u = 0, k = 0;
         for (;;) {
-            const unsigned m = __ballot_sync(0xffffffffu, lane < N && lane > u && sm.par[lane] == u && sm.x[lane] == sm.a[u]);
-            if (!m) break;
-            const int c = __ffs(m) - 1;
+            const int au = sm.a[u];
+            const unsigned m0 = __ballot_sync(0xffffffffu, lane < N && lane > u && sm.par[lane] == u && sm.x[lane] == au);
+            const int w = lane + 32;
+            const unsigned m1 = __ballot_sync(0xffffffffu, w < N && w > u && sm.par[w] == u && sm.x[w] == au);
+            if (!m0 && !m1) break;
+            const int c = m0 ? __ffs(m0) - 1 : 32 + __ffs(m1) - 1;
             if (lane == 0) {
                 P.out_tokens[static_cast<size_t>(b) * N + k] = sm.x[c];
                 if (P.tree_nodes) P.tree_nodes[static_cast<size_t>(b) * N + k] = c;

@@ -36,8 +36,9 @@ FANOUT_SEEDS = (400, 4)
 TREE_SEEDS = (500, 501, 5, 6)
 # Draft-tree shapes: children per node, level by level.  "k21": the 21-node
 # tree (root, 4, 8, 8) of tree-style verification; "w4": width-4 tree drafting
-# (root with 4 children, each continued by a chain of 3).
-TREE_SHAPES = {"k21": [4, 2, 1], "w4": [4, 1, 1, 1], "path4": [1, 1, 1, 1]}
+# (root with 4 children, each continued by a chain of 3); "b63": a binary
+# tree of depth 5 (63 nodes, near the node limit).
+TREE_SHAPES = {"k21": [4, 2, 1], "w4": [4, 1, 1, 1], "path4": [1, 1, 1, 1], "b63": [2, 2, 2, 2, 2]}
 BONUS_SEED_OFFSET = 7919  # seed of the bonus-position draft row = draft seed + this
 
 

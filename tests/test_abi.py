@@ -181,7 +181,7 @@ def test_saguaro_arguments_rejected_on_host(lib):
 
 
 def test_tree_arguments_rejected_on_host(lib):
-    """spv_verify_tree: 1 <= N <= 32 nodes, T >= 0 finite, draft rows,
+    """spv_verify_tree: 1 <= N <= 64 nodes, T >= 0 finite, draft rows,
     uniforms and keys required when T > 0, a large enough workspace."""
     import speculative_decoding_token_spv_gb300 as spv
     P = ctypes.c_void_p
@@ -197,12 +197,12 @@ def test_tree_arguments_rejected_on_host(lib):
                                    a["V"], ctypes.c_float(a["T"]), a["acc"], a["out"], a["nodes"], a["st"], a["ws"],
                                    a["wsb"], a["stream"])
 
-    for kw in (dict(N=0), dict(N=33), dict(B=0), dict(T=-1.0), dict(T=float("inf")), dict(T=float("nan")),
+    for kw in (dict(N=0), dict(N=65), dict(B=0), dict(T=-1.0), dict(T=float("inf")), dict(T=float("nan")),
                dict(T=1e-45), dict(d=None), dict(r=None), dict(keys=None), dict(par=None), dict(tok=None),
                dict(t=None), dict(acc=None), dict(out=None), dict(wsb=16), dict(ws=P((1 << 20) + 8)), dict(dt=7)):
         assert call(**kw) == 1, kw
     n = spv.spv_tree_workspace_bytes(64, 21, 151936)
-    assert n > 0 and spv.spv_tree_workspace_bytes(64, 33, 151936) == 0 and spv.spv_tree_workspace_bytes(0, 4, 10) == 0
+    assert n > 0 and spv.spv_tree_workspace_bytes(64, 65, 151936) == 0 and spv.spv_tree_workspace_bytes(0, 4, 10) == 0
 
 
 def test_selftest_arguments_rejected_on_host(lib):

@@ -85,7 +85,7 @@ def _random_tree(B, N, V, dtype, T, seed):
 def test_tree_random(spv, seed):
     rng = np.random.default_rng(700 + seed)
     B = int(rng.integers(1, 48))
-    N = int(rng.integers(1, 33))
+    N = int(rng.integers(1, 65))
     V = int(rng.choice([int(rng.integers(2, 200)), int(rng.integers(200, 20000))]))
     while B * 2 * N * V > 3_000_000:
         V = max(2, V // 2)

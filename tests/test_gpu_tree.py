@@ -121,9 +121,10 @@ def test_many_children_and_ragged_vocab(spv):
 
 
 def test_single_node_and_deep_path(spv):
-    """N = 1: the bonus token from the root; N = 32 as one path (32 levels)."""
+    """N = 1: the bonus token from the root; N = 32 and N = 64 (the node
+    limit) as one path."""
     gen = torch.Generator(device="cpu").manual_seed(83)
-    for N in (1, 32):
+    for N in (1, 32, 64):
         B, V = 8, 5000
         z = torch.randn(B, N, V, generator=gen)
         d = z + 0.3 * torch.randn(B, N, V, generator=gen)
@@ -181,10 +182,10 @@ def test_invalid_arguments(spv):
         spv.spv_verify_tree(w.target, w.draft, w.parent, w.tokens, w.r, w.keys, -1.0)
     with pytest.raises(spv.SpvError):
         spv.spv_verify_tree(w.target, w.draft, w.parent, w.tokens, w.r, w.keys, float("nan"))
-    big = torch.zeros(1, 33, 64, device="cuda")
-    par = torch.arange(-1, 32, dtype=torch.int32, device="cuda")[None]
+    big = torch.zeros(1, 65, 64, device="cuda")
+    par = torch.arange(-1, 64, dtype=torch.int32, device="cuda")[None]
     with pytest.raises(spv.SpvError):
-        spv.spv_verify_tree(big, big, par, torch.zeros_like(par), torch.ones(1, 33, device="cuda"),
+        spv.spv_verify_tree(big, big, par, torch.zeros_like(par), torch.ones(1, 65, device="cuda"),
                             torch.zeros(1, dtype=torch.int64, device="cuda"), 1.0)
 
 
@@ -215,3 +216,13 @@ def test_statistics_not_staged(spv):
     keys = torch.arange(B, dtype=torch.int64) * 31337 + 5
     w = workloads.TreeInputs("unstaged", z.cuda(), d.cuda(), parent.cuda(), tok.cuda(), r.cuda(), keys.cuda(), 1.0)
     check_tree(spv, w)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.0])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_binary_tree_63_nodes(spv, dtype, T):
+    """A depth-5 binary tree (63 nodes): children masks past 32 nodes, the
+    parents of nodes 32..62 in the leaf-row skip."""
+    w = workloads.tree(B=16, shape="b63", V=20000, dtype=dtype, temperature=T, device="cuda")
+    got, ref = check_tree(spv, w)
+    assert (ref["accept_count"] >= 3).any()

@@ -513,9 +513,10 @@ def run_variants(spv, dev, stream, args):
         res[-1]["sample"] = f"{n} verify outcomes"
     del w, ws, lists
     # Tree verify (multi-round speculative sampling over a draft tree per
-    # sequence): the 21-node tree and the width-4 tree on the spd rows.
+    # sequence): the 21-node tree, the width-4 tree and a 63-node binary tree
+    # on the spd rows.
     tcases = [("k21", 1.0, torch.bfloat16), ("k21", 0.0, torch.bfloat16), ("w4", 1.0, torch.bfloat16),
-              ("k21", 1.0, torch.float32)]
+              ("k21", 1.0, torch.float32), ("b63", 1.0, torch.bfloat16)]
     for shape, T, dt in tcases:
         w = workloads.tree(B=64, shape=shape, dtype=dt, temperature=T, device=dev)
         ws = spv.new_workspace(spv.spv_tree_workspace_bytes(w.B, w.N, w.V), dev)

@@ -798,10 +798,11 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
 // at node v, from which v's children were drawn).  The finalize walks the
 // tree from the root: the children c of node u are tested in index order
 // against P_m = max(0, p_u - s_m q_u) / N_m (s_0 = 0, N_0 = 1, s_{m+1} = s_m +
-// N_m, N_m = sum max(0, p_u - s_m q_u): a residual pass of the whole CTA);
-// the first accepted child is descended into; when all are rejected one
-// token is drawn from P_m (rejection trials from p_u with q scaled by s_m,
-// then the direct residual race), at a leaf the bonus from p_u.
+// N_m, N_m = sum max(0, p_u - s_m q_u): a residual pass split over the
+// sequence's cluster of finalize CTAs); the first accepted child is
+// descended into; when all are rejected one token is drawn from P_m
+// (rejection trials from p_u with q scaled by s_m, then the direct residual
+// race), at a leaf the bonus from p_u.  Up to 64 nodes.
 // The tree's streaming pass: the chain's, except that the draft row of a
 // leaf (a node no other node hangs from) is neither loaded nor reduced.
 template <int DT> struct TreeOp : ChainOp<DT> {

@@ -21,7 +21,12 @@
 //
 // Both finalizers can also key the outcome (k, emitted token) against the
 // sequence's speculation-cache entries ("Speculative Speculative Decoding",
-// Algorithm 1 and Figure 2) and write the hit slot.
+// Algorithm 1 and Figure 2) and write the hit slot, and the chain finalizer
+// verifies Saguaro-sampled drafts (cached candidates down-weighted by C).
+//
+// Tree verify (multi-round speculative sampling over a draft token tree per
+// sequence, greedy descent at T = 0) reuses the streaming pass and the draws;
+// see the tree section below.
 #include "spv_internal.h"
 #include "spv_stream.cuh"
 

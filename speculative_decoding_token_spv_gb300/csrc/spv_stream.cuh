@@ -6,13 +6,17 @@
 //   (cp.async.bulk, global -> shared, completion on an mbarrier), and eight
 //   consumer warps reduce one sampler block (1024 logits) each.  Per-block
 //   partial results go to a small workspace.  A second, dependent grid (one
-//   CTA per sequence or row, programmatic dependent launch) merges them and
-//   writes the outputs, so no streaming CTA ever waits on another's work.
+//   CTA per sequence or row, or a cluster of them; programmatic dependent
+//   launch) merges them and writes the outputs, so no streaming CTA ever
+//   waits on another's work.  Optional per-op hooks: rows skipped by
+//   producer and consumers alike, a per-call reset.
 // * Philox4x32-10 and the uniform / exponential variates of the sampling rule.
-// * Warp reductions and order-preserving float keys.
+// * Warp reductions, order-preserving float keys, packed fp32-pair arithmetic.
+// * Bounded waits: on an mbarrier, on a flag, and a barrier of the CTAs of one
+//   thread-block cluster through global memory.
 //
-// Every wait on an mbarrier is bounded; a wait that gives up records
-// SPV_ERR_TIMEOUT in the workspace error word and the CTA stops cleanly.
+// Every wait is bounded; a wait that gives up records SPV_ERR_TIMEOUT in the
+// workspace error word and the CTA stops cleanly.
 #pragma once
 
 #include <cuda_bf16.h>

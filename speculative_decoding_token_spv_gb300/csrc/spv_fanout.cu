@@ -3,11 +3,14 @@
 // "Speculative Speculative Decoding" (review of arXiv 2603.03251), Figure 2:
 // at each position k the speculation cache takes F_k bonus-token candidates
 // from the top ranks of the draft logits, excluding the token already sent for
-// verification.  One pass over the rows: each warp reduces a 1024-logit block
-// to its own top-F list (F rounds of a warp max over 64-bit keys
-// (order-preserving logit key, inverted id), so logit descending then id
-// ascending, every key distinct); the finalize grid (one CTA per row) merges
-// the per-block lists (which are already sorted) into the row's top-F.
+// verification.  Keys are 64-bit (order-preserving logit key, inverted id), so
+// logit descending then id ascending, every key distinct.  One pass over the
+// rows: each warp reduces a 1024-logit block to its own sorted top-F list (the
+// F-th largest lane maximum bounds the block's F-th largest key from below;
+// the elements that reach it are ranked or sorted once); the finalize grid
+// (one CTA per row) merges the per-block lists into the row's top-F, by the
+// same kind of bound over the list heads when the lists fit in shared memory,
+// else list by list.
 #include "spv_internal.h"
 #include "spv_stream.cuh"
 
@@ -34,11 +37,53 @@ struct FanoutSmem {
     uint64_t cand[FAN_CACHE];
     uint64_t list[NCW][64];
     int bad;
+    int fast;  // the row's ids were written by the threshold merge
 };
 
 __device__ __forceinline__ uint64_t cand_key(uint32_t k32, int id)
 {
     return (static_cast<uint64_t>(k32) << 32) | static_cast<uint64_t>(0xFFFFFFFFu - static_cast<uint32_t>(id));
+}
+
+// Id of a candidate key (0 = no candidate: -1).
+__device__ __forceinline__ int32_t cand_id(uint64_t key)
+{
+    return key ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(key)) : -1;
+}
+
+// Rank of the key a among the keys held by lanes 0..n-1 (one per lane,
+// distinct): the number of larger ones, i.e. its position in descending order.
+__device__ __forceinline__ int rank_desc(uint64_t a, int n)
+{
+    int rank = 0;
+    for (int j = 0; j < n; ++j) rank += __shfl_sync(0xffffffffu, a, j) > a ? 1 : 0;
+    return rank;
+}
+
+// Descending bitonic sort of 64 keys held two per lane (element i = lane in
+// a, element i = lane + 32 in c); afterwards a holds rank lane, c rank lane + 32.
+__device__ __forceinline__ void bitonic64_desc(uint64_t &a, uint64_t &c, int lane)
+{
+#pragma unroll
+    for (int kk = 2; kk <= 64; kk <<= 1) {
+#pragma unroll
+        for (int j = kk >> 1; j > 0; j >>= 1) {
+            if (j == 32) {
+                // partner of i is i + 32 (same lane): i = lane < 32 is the lower one
+                const bool desc = (lane & kk) == 0;  // kk == 64: whole sequence descending
+                const uint64_t hi = a > c ? a : c, lo = a > c ? c : a;
+                a = desc ? hi : lo;
+                c = desc ? lo : hi;
+            } else {
+                const uint64_t oa = __shfl_xor_sync(0xffffffffu, a, j);
+                const uint64_t oc = __shfl_xor_sync(0xffffffffu, c, j);
+                const bool lower = (lane & j) == 0;
+                const bool da = ((lane & kk) == 0), dc = (((lane + 32) & kk) == 0);
+                a = (lower == da) ? (a > oa ? a : oa) : (a < oa ? a : oa);
+                c = (lower == dc) ? (c > oc ? c : oc) : (c < oc ? c : oc);
+            }
+        }
+    }
 }
 
 template <int DT> struct FanoutOp {
@@ -87,9 +132,11 @@ template <int DT> struct FanoutOp {
             // candidate unless NaN (then the row is bad).  Lane maximum by
             // max.NaN, the threshold among the lane maxima as floats (the
             // order of the keys), then one compare per element.
-            float mx = v[0];
+            float m8[8];
 #pragma unroll
-            for (int e = 1; e < 32; ++e) mx = max_nan(mx, v[e]);
+            for (int a = 0; a < 8; ++a) m8[a] = max_nan(max_nan(v[a], v[a + 8]), max_nan(v[a + 16], v[a + 24]));
+            const float mx = max_nan(max_nan(max_nan(m8[0], m8[1]), max_nan(m8[2], m8[3])),
+                                     max_nan(max_nan(m8[4], m8[5]), max_nan(m8[6], m8[7])));
             if (__any_sync(0xffffffffu, mx != mx)) {
                 if (lane == 0) out[0] = ~0ull;
                 return;
@@ -195,27 +242,15 @@ template <int DT> struct FanoutOp {
             __syncwarp();
             uint64_t a = lane < total ? sl[lane] : 0ull, c = lane + 32 < total ? sl[lane + 32] : 0ull;
             __syncwarp();
-            // element i = lane (a) and i = lane + 32 (c); descending bitonic network over 64
-#pragma unroll
-            for (int kk = 2; kk <= 64; kk <<= 1) {
-#pragma unroll
-                for (int j = kk >> 1; j > 0; j >>= 1) {
-                    if (j == 32) {
-                        // partner of i is i + 32 (same lane): i = lane < 32 is the lower one
-                        const bool desc = (lane & kk) == 0;  // kk == 64: whole sequence descending
-                        const uint64_t hi = a > c ? a : c, lo = a > c ? c : a;
-                        a = desc ? hi : lo;
-                        c = desc ? lo : hi;
-                    } else {
-                        const uint64_t oa = __shfl_xor_sync(0xffffffffu, a, j);
-                        const uint64_t oc = __shfl_xor_sync(0xffffffffu, c, j);
-                        const bool lower = (lane & j) == 0;
-                        const bool da = ((lane & kk) == 0), dc = (((lane + 32) & kk) == 0);
-                        a = (lower == da) ? (a > oa ? a : oa) : (a < oa ? a : oa);
-                        c = (lower == dc) ? (c > oc ? c : oc) : (c < oc ? c : oc);
-                    }
-                }
+            if (total <= 32) {
+                // One key per lane: its rank is the number of larger keys
+                // (keys are distinct), which is its position in the list.
+                const int rk = rank_desc(a, total);
+                if (lane < total && rk < F) out[rk] = a;
+                if (lane >= total && lane < F) out[lane] = 0ull;
+                return;
             }
+            bitonic64_desc(a, c, lane);
             if (lane < F) out[lane] = a;
             return;
         }
@@ -279,7 +314,10 @@ template <int DT> struct FanoutOp {
         const int k = row % P.K1, b = row / P.K1;
         const int F = P.F[k];
         const int nb = P.nb;
-        if (threadIdx.x == 0) sm.bad = 0;
+        if (threadIdx.x == 0) {
+            sm.bad = 0;
+            sm.fast = 0;
+        }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         consumer_sync();
         const uint64_t *rc = P.cand + static_cast<size_t>(row) * nb * P.Fmax;
@@ -314,6 +352,56 @@ template <int DT> struct FanoutOp {
             for (int t = threadIdx.x; t < F; t += NCW * 32) ids[t] = -1;
             if (threadIdx.x == 0 && P.row_status) P.row_status[row] = (F > 0 && sm.bad) ? STATUS_BAD_ROW : 0;
             return;
+        }
+        if (cached && F <= 32) {
+            // Threshold merge (one warp): the F-th largest of the lane maxima
+            // of the list heads bounds the row's F-th largest key from below
+            // (F distinct keys reach it), so only entries at or above it can
+            // be in the top F; the lists are sorted, so each is scanned only
+            // down to it.  Up to 64 such entries are sorted once; more fall
+            // through to the level-by-level merge below.
+            if (warp == 0) {
+                uint64_t lm = 0;
+                for (int beta = lane; beta < nb; beta += 32) {
+                    const uint64_t h = sm.cand[beta * F];
+                    lm = h > lm ? h : lm;
+                }
+                const int rk = rank_desc(lm, 32);  // nonzero lane maxima are distinct
+                const unsigned sel = __ballot_sync(0xffffffffu, lm != 0ull && rk == F - 1);
+                const uint64_t t = sel ? __shfl_sync(0xffffffffu, lm, __ffs(sel) - 1) : 1ull;
+                int n = 0;
+                for (int beta = lane; beta < nb; beta += 32)
+                    for (int j = 0; j < F && sm.cand[beta * F + j] >= t; ++j) ++n;
+                int pre = n;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int y = __shfl_up_sync(0xffffffffu, pre, o);
+                    if (lane >= o) pre += y;
+                }
+                const int total = __shfl_sync(0xffffffffu, pre, 31);
+                if (total <= 64) {
+                    uint64_t *sl = sm.list[0];
+                    int pos = pre - n;
+                    for (int beta = lane; beta < nb; beta += 32)
+                        for (int j = 0; j < F && sm.cand[beta * F + j] >= t; ++j) sl[pos++] = sm.cand[beta * F + j];
+                    __syncwarp();
+                    uint64_t a = lane < total ? sl[lane] : 0ull, c = lane + 32 < total ? sl[lane + 32] : 0ull;
+                    if (total <= 32) {
+                        const int r = rank_desc(a, total);
+                        if (lane < total && r < F) ids[r] = cand_id(a);
+                        if (lane >= total && lane < F) ids[lane] = -1;
+                    } else {
+                        bitonic64_desc(a, c, lane);
+                        if (lane < F) ids[lane] = cand_id(a);
+                    }
+                    if (lane == 0) {
+                        sm.fast = 1;
+                        if (P.row_status) P.row_status[row] = 0;
+                    }
+                }
+            }
+            consumer_sync();
+            if (sm.fast) return;
         }
         // Level 1: warp w merges the sorted lists of blocks beta = w + NCW * j.
         auto cand_at = [&](int beta, int t) -> uint64_t {
@@ -355,7 +443,7 @@ template <int DT> struct FanoutOp {
                     ++h;
                     c = h < F ? sm.list[lane][h] : 0ull;
                 }
-                if (lane == 0) ids[t] = best ? static_cast<int32_t>(0xFFFFFFFFu - static_cast<uint32_t>(best)) : -1;
+                if (lane == 0) ids[t] = cand_id(best);
             }
             if (lane == 0 && P.row_status) P.row_status[row] = 0;
         }

@@ -380,9 +380,11 @@ template <int DT> struct ChainOp {
     // per row, all rows at once, up to 16 loads per lane in flight together:
     // sm.M / sm.S = row max / sum exp((z - max) / T).  Target rows rho <
     // ncache keep (m_beta, race factor) in sm.st for the draws (when they
-    // fit).  A bad row (NaN / +inf, no finite logit) gets S = NaN; with
-    // flag_all it also sets sm.bad.  FWV warps.
-    template <int FWV>
+    // fit); with FACTORS their race factors replace S_beta there (else
+    // stage_factors does that once the row statistics are visible).  A bad
+    // row (NaN / +inf, no finite logit) gets S = NaN; with flag_all it also
+    // sets sm.bad.  FWV warps.
+    template <int FWV, bool FACTORS>
     __device__ static void merge_stats(const Params &P, int b, Smem &sm, int ncache, bool flag_all, int warp, int lane)
     {
         const int R = P.R, nb = P.nb;
@@ -432,13 +434,28 @@ template <int DT> struct ChainOp {
                 sm.S[rho] = rowbad ? __int_as_float(0x7fffffff) : s;
                 if (rowbad && flag_all) atomicOr(&sm.bad, 1);
             }
-            if (keep && !rowbad && mw != -INFINITY) {
+            if (FACTORS && keep && !rowbad && mw != -INFINITY) {
                 // entry beta was staged by this lane (beta = hl mod 16): no warp barrier needed
                 for (int beta = hl; beta < nb; beta += 16) {
                     const float2 v = sm.st[rho * nb + beta];
                     sm.st[rho * nb + beta].y = v.y > 0.f ? fast_exp2((mw - v.x) * P.c2) / v.y : -1.f;
                 }
             }
+        }
+    }
+
+    // Race factors 2^((M - m_beta) c2) / S_beta (-1 for an empty block) of the
+    // staged target rows rho < nrows, in place of S_beta in sm.st (all
+    // threads; rows with no mass are left alone).  Needs sm.M / sm.S.
+    template <int FWV> __device__ static void stage_factors(const Params &P, Smem &sm, int nrows)
+    {
+        if (!sm.cached) return;
+        const int nb = P.nb;
+        for (int i = threadIdx.x; i < nrows * nb; i += FWV * 32) {
+            const int rho = i / nb;
+            if (!(sm.S[rho] > 0.f)) continue;
+            const float2 v = sm.st[i];
+            sm.st[i].y = v.y > 0.f ? fast_exp2((sm.M[rho] - v.x) * P.c2) / v.y : -1.f;
         }
     }
 
@@ -667,12 +684,15 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
         // B. Row statistics from the block statistics (all rows at once).
-        Base::template merge_stats<FWV>(P, b, sm, g + 1, true, warp, lane);
+        Base::template merge_stats<FWV, false>(P, b, sm, g + 1, true, warp, lane);
         fin_sync<FWV>();
         if (sm.bad) {
             write_bad_row(P, b, warp, lane);
             return;
         }
+        // Race factors of the target rows (read by the draws after the
+        // barrier that follows the accept tests).
+        Base::template stage_factors<FWV>(P, sm, g + 1);
         if (P.sag) {
             // Saguaro: q_C's normaliser S - (1 - 1/C) * sum over the cached ids (at least S / C)
 #pragma unroll
@@ -1032,7 +1052,7 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
         // B. Row statistics; a bad target row, or a bad draft row of a node
         //    with children, makes the sequence bad (a leaf's draft row was
         //    not streamed and is not looked at).
-        Base::template merge_stats<FWV>(P, b, sm, N, false, warp, lane);
+        Base::template merge_stats<FWV, true>(P, b, sm, N, false, warp, lane);
         fin_sync<FWV>();
         if (warp == 0 && !sm.bad) {
             bool bad = false;

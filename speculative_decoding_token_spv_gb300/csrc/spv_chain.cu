@@ -136,7 +136,7 @@ template <int DT> struct ChainOp {
     }
     __device__ static __forceinline__ const void *row_ptr(const Params &P, long long row)
     {
-        const int b = static_cast<int>(row / P.R);
+        const int b = static_cast<int>(div_row(row, P.R));
         return row_of(P, b, static_cast<int>(row - static_cast<long long>(b) * P.R));
     }
 
@@ -837,7 +837,7 @@ template <int DT> struct TreeOp : ChainOp<DT> {
     // each, 0xffff for none or the root).  Target rows: no load.
     __device__ static __forceinline__ int skip_key(const ChainParams &P, long long row, int lane)
     {
-        const long long b = row / P.R;
+        const long long b = div_row(row, P.R);
         const int rho = static_cast<int>(row - b * P.R);
         if (rho < P.nt) return -1;
         const int32_t *pp = P.tree_parent + b * P.nt;
@@ -848,7 +848,7 @@ template <int DT> struct TreeOp : ChainOp<DT> {
 
     __device__ static __forceinline__ bool skip(const ChainParams &P, long long row, int key, int)
     {
-        const long long b = row / P.R;
+        const long long b = div_row(row, P.R);
         const int u = static_cast<int>(row - b * P.R) - P.nt;
         if (u < 0) return false;
         const bool hit = (key & 0xffff) == u || ((key >> 16) & 0xffff) == u;

@@ -118,7 +118,7 @@ template <int DT> struct FanoutOp {
     __device__ static __forceinline__ void block_smem(const Params &P, long long row, int beta,
                                                       const unsigned char *blk, int valid, int lane)
     {
-        const int k = static_cast<int>(row % P.K1);
+        const int k = static_cast<int>(row - div_row(row, P.K1) * P.K1);
         const int F = P.F[k];
         if (F == 0) return;
         const int ex = P.exclude[row];
@@ -271,7 +271,7 @@ template <int DT> struct FanoutOp {
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int valid,
                                                  int lane)
     {
-        const int k = static_cast<int>(row % P.K1);
+        const int k = static_cast<int>(row - div_row(row, P.K1) * P.K1);
         const int F = P.F[k];
         if (F == 0) return;
         const int ex = P.exclude[row];

@@ -80,7 +80,7 @@ __device__ __forceinline__ int key_id(uint64_t k) { return static_cast<int>(0xFF
 template <int DT> __device__ __forceinline__ const unsigned char *filt_row_ptr(const FiltParams &P, long long row)
 {
     constexpr int EB = DType<DT>::BYTES;
-    const int b = static_cast<int>(row / P.R), rho = static_cast<int>(row - static_cast<long long>(b) * P.R);
+    const int b = static_cast<int>(div_row(row, P.R)), rho = static_cast<int>(row - static_cast<long long>(b) * P.R);
     if (rho <= P.gamma)
         return P.target + (static_cast<size_t>(b) * (P.gamma + 1) + rho) * static_cast<size_t>(P.V) * EB;
     return P.draft + (static_cast<size_t>(b) * P.gamma + (rho - P.gamma - 1)) * static_cast<size_t>(P.V) * EB;

@@ -453,6 +453,39 @@ __device__ __forceinline__ void load_block_global(float v[32], const void *blk, 
     }
 }
 
+// ------------------------------------------------------------------ item positions
+// Quotient of a row index by a small positive divisor: 32-bit unsigned
+// division while the row fits in 32 bits (every call in practice), else the
+// 64-bit one.
+__device__ __forceinline__ long long div_row(long long row, int d)
+{
+    return row <= 0xffffffffLL ? static_cast<long long>(static_cast<uint32_t>(row) / static_cast<uint32_t>(d))
+                               : row / d;
+}
+
+// Position (row, chunk c) of work item it = row * nc + c, advanced by a fixed
+// stride of items without a division per step.
+struct ItemPos {
+    long long row;
+    int c;
+    int nc, dq, dr;  // items per row; stride = dq * nc + dr
+    __device__ __forceinline__ ItemPos(unsigned first, unsigned stride, int nc_)
+        : row(first / static_cast<unsigned>(nc_)), c(static_cast<int>(first % static_cast<unsigned>(nc_))), nc(nc_),
+          dq(static_cast<int>(stride / static_cast<unsigned>(nc_))),
+          dr(static_cast<int>(stride % static_cast<unsigned>(nc_))) {}
+    // Row of the item one stride ahead.
+    __device__ __forceinline__ long long next_row() const { return row + dq + (c + dr >= nc ? 1 : 0); }
+    __device__ __forceinline__ void advance()
+    {
+        row += dq;
+        c += dr;
+        if (c >= nc) {
+            c -= nc;
+            ++row;
+        }
+    }
+};
+
 // ------------------------------------------------------------------ the pipeline
 // Op supplies:
 //   struct Params  -- with total_items, nc (items per row), nb (blocks per
@@ -526,11 +559,12 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                 const uint64_t pol = l2_evict_first_policy();
                 int i = 0;
                 long long it = blockIdx.x;
-                int key = it < total ? Op::skip_key(P, it / nc, lane) : 0;
-                for (; it < total; it += gridDim.x) {
-                    const long long row = it / nc;
+                ItemPos pos(blockIdx.x, gridDim.x, nc);
+                int key = it < total ? Op::skip_key(P, pos.row, lane) : 0;
+                for (; it < total; it += gridDim.x, pos.advance()) {
+                    const long long row = pos.row;
                     const long long nx = it + gridDim.x;
-                    const int nkey = nx < total ? Op::skip_key(P, nx / nc, lane) : 0;
+                    const int nkey = nx < total ? Op::skip_key(P, pos.next_row(), lane) : 0;
                     const bool skip = Op::skip(P, row, key, lane);
                     key = nkey;
                     if (skip) continue;
@@ -545,7 +579,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                         } else if (sh_abort) {
                             stop = 1;
                         } else {
-                            const int c = static_cast<int>(it - row * nc);
+                            const int c = pos.c;
                             const int n = min(CHUNK, P.V - c * CHUNK);
                             const unsigned char *src = reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) +
                                                        static_cast<size_t>(c) * CHUNK_BYTES;
@@ -564,7 +598,8 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
         if (TMA && lane == 0) {
             const uint64_t pol = l2_evict_first_policy();
             int i = 0;
-            for (long long it = blockIdx.x; it < total; it += gridDim.x, ++i) {
+            ItemPos pos(blockIdx.x, gridDim.x, nc);
+            for (long long it = blockIdx.x; it < total; it += gridDim.x, ++i, pos.advance()) {
                 const int s = i % S;
                 const uint32_t ph = (i / S) & 1;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u)) {
@@ -573,8 +608,8 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                     break;
                 }
                 if (sh_abort) break;
-                const long long row = it / nc;
-                const int c = static_cast<int>(it - row * nc);
+                const long long row = pos.row;
+                const int c = pos.c;
                 const int n = min(CHUNK, P.V - c * CHUNK);
                 const unsigned char *src =
                     reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) + static_cast<size_t>(c) * CHUNK_BYTES;
@@ -591,12 +626,13 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
     if constexpr (OpWaitsPrior<Op>::value) asm volatile("griddepcontrol.wait;" ::: "memory");
     int i = 0;
     int key = 0;
-    if constexpr (SK) key = blockIdx.x < total ? Op::skip_key(P, blockIdx.x / nc, lane) : 0;
-    for (long long it = blockIdx.x; it < total; it += gridDim.x) {
+    ItemPos pos(blockIdx.x, gridDim.x, nc);
+    if constexpr (SK) key = blockIdx.x < total ? Op::skip_key(P, pos.row, lane) : 0;
+    for (long long it = blockIdx.x; it < total; it += gridDim.x, pos.advance()) {
         if constexpr (SK) {
             const long long nx = it + gridDim.x;
-            const int nkey = nx < total ? Op::skip_key(P, nx / nc, lane) : 0;
-            const bool skip = Op::skip(P, it / nc, key, lane);
+            const int nkey = nx < total ? Op::skip_key(P, pos.next_row(), lane) : 0;
+            const bool skip = Op::skip(P, pos.row, key, lane);
             key = nkey;
             if (skip) continue;
         }
@@ -610,8 +646,8 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                 sh_abort = 1;
             }
         }
-        const long long row = it / nc;
-        const int c = static_cast<int>(it - row * nc);
+        const long long row = pos.row;
+        const int c = pos.c;
         const int beta = c * CHUNK_BLOCKS + warp;
         if (ok && beta < P.nb) {
             const int valid = min(G, P.V - beta * G);

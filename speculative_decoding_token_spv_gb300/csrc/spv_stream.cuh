@@ -463,6 +463,14 @@ __device__ __forceinline__ long long div_row(long long row, int d)
                                : row / d;
 }
 
+// The work-item counter of a call: 64 bits at byte 8 of the workspace header
+// (after the error word and the self-test flag).  Zero between calls: a
+// zero-filled workspace starts it at 0 and every finalize grid returns it to 0.
+__device__ __forceinline__ unsigned long long *item_counter(unsigned *err)
+{
+    return reinterpret_cast<unsigned long long *>(err + 2);
+}
+
 // Position (row, chunk c) of work item it = row * nc + c, advanced by a fixed
 // stride of items without a division per step.
 struct ItemPos {
@@ -532,6 +540,8 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full_bar[S];
     __shared__ __align__(8) uint64_t empty_bar[S];
+    __shared__ long long stage_row[S];  // item of each ring stage (dynamic assignment): row, -1 = no more
+    __shared__ int stage_c[S];          // and chunk
     __shared__ volatile int sh_abort;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -596,34 +606,90 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
             return;
         }
         if (TMA && lane == 0) {
+            // Work items: this CTA's first S are static (it = blockIdx.x + j * grid, j < S); the rest
+            // are handed out in increasing order by the call's item counter, so the CTAs that stream
+            // faster take more of them (with equal shares the slowest SMs set the end of the pass).
+            // The next item's index is fetched one item ahead: the atomic's latency hides behind the
+            // wait for a free stage.  Each stage carries its item's (row, chunk) to the consumers; the
+            // stage after the last item carries row -1 and no copy.
             const uint64_t pol = l2_evict_first_policy();
+            unsigned long long *ctr = item_counter(P.err);
+            const long long first_dyn = static_cast<long long>(S) * gridDim.x;
             int i = 0;
-            ItemPos pos(blockIdx.x, gridDim.x, nc);
-            for (long long it = blockIdx.x; it < total; it += gridDim.x, ++i, pos.advance()) {
+            bool aborted = false;
+            for (long long it = blockIdx.x; it < total;) {
+                const long long nx = (i + 1 < S) ? blockIdx.x + static_cast<long long>(i + 1) * gridDim.x
+                                                 : first_dyn + static_cast<long long>(atomicAdd(ctr, 1ull));
                 const int s = i % S;
                 const uint32_t ph = (i / S) & 1;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u)) {
                     atomicExch(P.err, STATUS_TIMEOUT);
                     sh_abort = 1;
+                    aborted = true;
                     break;
                 }
-                if (sh_abort) break;
-                const long long row = pos.row;
-                const int c = pos.c;
+                if (sh_abort) {
+                    aborted = true;
+                    break;
+                }
+                const long long row = div_row(it, nc);
+                const int c = static_cast<int>(it - row * nc);
+                stage_row[s] = row;
+                stage_c[s] = c;
                 const int n = min(CHUNK, P.V - c * CHUNK);
                 const unsigned char *src =
                     reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) + static_cast<size_t>(c) * CHUNK_BYTES;
                 mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(n * EB));
                 bulk_g2s(ring + s * CHUNK_BYTES, src, static_cast<uint32_t>(n * EB), &full_bar[s], pol);
+                ++i;
+                it = nx;
             }
-            // No copy may still be writing this CTA's shared memory at exit.
+            // No copy may still be writing this CTA's shared memory at exit.  (Drained before the end
+            // mark: the end mark completes one more phase of the stage of item i - S, after which a
+            // wait on that item's phase parity would name the next, never completed, phase.)
             for (int k = max(0, i - S); k < i; ++k) mbar_wait(&full_bar[k % S], (k / S) & 1);
+            if (!aborted) {
+                const int s = i % S;
+                if (mbar_wait(&empty_bar[s], ((i / S) & 1) ^ 1u)) {
+                    stage_row[s] = -1;
+                    mbar_arrive(&full_bar[s]);
+                } else {
+                    atomicExch(P.err, STATUS_TIMEOUT);
+                    sh_abort = 1;
+                }
+            }
         }
         return;
     }
 
     // ---------------- consumers
     if constexpr (OpWaitsPrior<Op>::value) asm volatile("griddepcontrol.wait;" ::: "memory");
+    if constexpr (TMA && !SK) {  // the items the producer hands over, stage by stage
+        int stage = 0;
+        uint32_t phase = 0;
+        for (;;) {
+            if (!mbar_wait(&full_bar[stage], phase)) {
+                atomicExch(P.err, STATUS_TIMEOUT);
+                sh_abort = 1;
+                break;
+            }
+            const long long row = stage_row[stage];
+            if (row < 0) break;  // no more items (the end mark holds no copy to release)
+            const int beta = stage_c[stage] * CHUNK_BLOCKS + warp;
+            if (beta < P.nb)
+                Op::block_smem(P, row, beta, ring + stage * CHUNK_BYTES + warp * G * EB, min(G, P.V - beta * G),
+                               lane);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[stage]);
+            // A timed-out wait anywhere stops every consumer warp together.
+            if (__any_sync(0xffffffffu, sh_abort != 0)) break;
+            if (++stage == S) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        return;
+    }
     int i = 0;
     int key = 0;
     ItemPos pos(blockIdx.x, gridDim.x, nc);
@@ -681,6 +747,12 @@ __global__ void __launch_bounds__(Op::FIN_WARPS * 32, 1) __maxnreg__(Op::FIN_WAR
     // Op::finalize issues griddepcontrol.wait before it reads anything the
     // streaming grid wrote; reads of the call's inputs may come before it.
     Op::finalize(P, static_cast<int>(blockIdx.x), sm, fin_buf, threadIdx.x >> 5, threadIdx.x & 31);
+    // The streaming grid has completed once the dependent-grid wait returns:
+    // return the call's work-item counter to zero for the next call.
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        *item_counter(P.err) = 0ull;
+    }
 }
 
 // SM count of the current device (queried once per device).

@@ -255,6 +255,35 @@ def test_repeat_calls_reuse_workspace(spv):
     assert spv.spv_workspace_status(ws) == spv.SPV_OK
 
 
+def test_work_item_counter_returns_to_zero(spv):
+    """The streaming pass hands its later work items out through a counter in
+    the workspace header (bytes 8..15); every call leaves it at zero, so one
+    workspace serves calls of different kinds and shapes in any order, each
+    matching a call on a fresh workspace."""
+    w = _random_case(24, 4, 70000, torch.float32, 1.0, 45)
+    wg = _random_case(9, 3, 100000, torch.bfloat16, 0.0, 46)
+    fw = workloads.fanout(device="cuda", B=2, V=50000)
+    n = max(spv.spv_chain_workspace_bytes(24, 4, 70000), spv.spv_greedy_workspace_bytes(9, 3, 100000),
+            spv.spv_fanout_workspace_bytes(2, 4, 50000, 8), spv.spv_filtered_workspace_bytes(24, 4, 70000))
+    ws = spv.new_workspace(n, "cuda")
+    calls = [
+        lambda ws: spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, 1.0, workspace=ws),
+        lambda ws: spv.spv_verify_chain(wg.target, wg.draft, wg.tokens, wg.r, wg.keys, 0.0, workspace=ws),
+        lambda ws: spv.spv_fanout_topk(fw.draft, fw.exclude, fw.fanout, workspace=ws),
+        lambda ws: spv.spv_verify_chain_filtered(w.target, w.draft, w.tokens, w.r, w.keys, 1.0, 50, 0.9,
+                                                 workspace=ws),
+    ]
+    for call in calls + calls[::-1]:
+        got = call(ws)
+        torch.cuda.synchronize()
+        assert int(ws[8:16].count_nonzero()) == 0
+        ref = call(spv.new_workspace(n, "cuda"))
+        torch.cuda.synchronize()
+        for k in ref:
+            assert torch.equal(got[k], ref[k]), k
+    assert spv.spv_workspace_status(ws) == spv.SPV_OK
+
+
 def test_invalid_arguments_raise(spv):
     w = _random_case(2, 2, 100, torch.float32, 1.0, 3)
     with pytest.raises(spv.SpvError):

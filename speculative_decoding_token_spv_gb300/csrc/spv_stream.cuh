@@ -615,11 +615,14 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
             const uint64_t pol = l2_evict_first_policy();
             unsigned long long *ctr = item_counter(P.err);
             const long long first_dyn = static_cast<long long>(S) * gridDim.x;
+            // With fewer than 4 items per CTA left after the static ones, the counter's atomics (all
+            // CTAs at once) cost more than the balance gains: keep the static stride for every item.
+            const bool dyn = total - first_dyn >= 4LL * gridDim.x;
             int i = 0;
             bool aborted = false;
             for (long long it = blockIdx.x; it < total;) {
-                const long long nx = (i + 1 < S) ? blockIdx.x + static_cast<long long>(i + 1) * gridDim.x
-                                                 : first_dyn + static_cast<long long>(atomicAdd(ctr, 1ull));
+                const long long nx = (i + 1 < S || !dyn) ? blockIdx.x + static_cast<long long>(i + 1) * gridDim.x
+                                                         : first_dyn + static_cast<long long>(atomicAdd(ctr, 1ull));
                 const int s = i % S;
                 const uint32_t ph = (i / S) & 1;
                 if (!mbar_wait(&empty_bar[s], ph ^ 1u)) {

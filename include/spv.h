@@ -101,9 +101,11 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
  *   row_status     [B] int32 out, optional: SPV_OK or SPV_ERR_BAD_ROW
  *   workspace      device scratch of >= spv_chain_workspace_bytes(B,gamma,V)
  *                  bytes, 256-byte aligned.  Its first 4 bytes are a sticky
- *                  error word (see spv_workspace_status): zero-fill the
- *                  workspace once before its first use.  One workspace must
- *                  not be shared by calls that may overlap on the GPU.
+ *                  error word (see spv_workspace_status); bytes 8..15 are
+ *                  the counter through which the streaming pass hands out
+ *                  work items, which every call leaves at zero.  Zero-fill
+ *                  the workspace once before its first use.  One workspace
+ *                  must not be shared by calls that may overlap on the GPU.
  *   stream         cudaStream_t (void*).  Two kernels are enqueued: the
  *                  streaming pass and, as a programmatic dependent launch,
  *                  the per-sequence finalize.

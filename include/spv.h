@@ -322,6 +322,8 @@ size_t spv_greedy_workspace_bytes(int B, int gamma, int V);
  *   exclude      [B, K+1] int32 (device)
  *   fanout       K+1 ints, HOST array, 0 <= F_k <= min(SPV_MAX_FANOUT, V-1)
  *   K+1 <= SPV_MAX_FANOUT_ROWS
+ *   V            <= 1,048,576 (else SPV_ERR_UNSUPPORTED: the row merge
+ *                holds up to 1,024 per-block candidate lists)
  *   out_ids      [B, sum_k F_k] int32 out (device), k-major then rank
  *   row_status   [B, K+1] int32 out, optional: SPV_ERR_BAD_ROW for NaN rows
  *                (their ids are -1)

@@ -104,8 +104,10 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
  *                  error word (see spv_workspace_status); bytes 8..15 are
  *                  the counter through which the streaming pass hands out
  *                  work items, which every call leaves at zero.  Zero-fill
- *                  the workspace once before its first use.  One workspace
- *                  must not be shared by calls that may overlap on the GPU.
+ *                  the workspace once before its first use, and again after
+ *                  a call that returned an error (its kernels may not all
+ *                  have run).  One workspace must not be shared by calls
+ *                  that may overlap on the GPU.
  *   stream         cudaStream_t (void*).  Two kernels are enqueued: the
  *                  streaming pass and, as a programmatic dependent launch,
  *                  the per-sequence finalize.

@@ -4,7 +4,9 @@
 //   rows are cut into work items of 8192 contiguous logits; a producer warp
 //   stages items in a ring of shared-memory buffers with TMA bulk copies
 //   (cp.async.bulk, global -> shared, completion on an mbarrier), and eight
-//   consumer warps reduce one sampler block (1024 logits) each.  Per-block
+//   consumer warps reduce one sampler block (1024 logits) each.  After a
+//   few static items per CTA, the items are handed out by a per-call counter
+//   in the workspace header, so faster CTAs take more of them.  Per-block
 //   partial results go to a small workspace.  A second, dependent grid (one
 //   CTA per sequence or row, or a cluster of them; programmatic dependent
 //   launch) merges them and writes the outputs, so no streaming CTA ever

@@ -42,6 +42,12 @@ def test_workspace_sizes(lib):
     assert spv.spv_chain_workspace_bytes(0, 4, 100) == 0
     assert spv.spv_chain_workspace_bytes(1, 33, 100) == 0
     assert spv.spv_fanout_workspace_bytes(1, 64, 100, 1) == 0
+    # every workspace holds the 256-byte header (error word, self-test flag,
+    # work-item counter at bytes 8..15) even at the smallest shapes
+    for n in (spv.spv_chain_workspace_bytes(1, 1, 2), spv.spv_greedy_workspace_bytes(1, 1, 2),
+              spv.spv_fanout_workspace_bytes(1, 0, 2, 0), spv.spv_filtered_workspace_bytes(1, 1, 2),
+              spv.spv_tree_workspace_bytes(1, 1, 2)):
+        assert n >= 256
 
 
 def test_fanout_size_and_status_strings(lib):

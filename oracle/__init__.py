@@ -13,6 +13,7 @@ around each call); the arithmetic of each sequence is the single-threaded C.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import subprocess
@@ -77,6 +78,8 @@ def _load():
                                                ctypes.c_int, ctypes.c_double, P, P, P, P, P, P]
         lib.spvo_verify_greedy_batch.argtypes = [P, P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                                  P, P, P]
+        lib.spvo_set_uniform_override.argtypes = [P]
+        lib.spvo_set_uniform_override.restype = None
         _lib = lib
     return _lib
 
@@ -106,6 +109,25 @@ def philox4x32_10(counter, key) -> np.ndarray:
 def uniform(seq_key: int, stream: int, trial: int, pos: int, n: int) -> float:
     """The (0,1] uniform both sides derive for draw n of (stream, trial, pos)."""
     return _load().spvo_uniform(seq_key, stream, trial, pos, n)
+
+
+UNIFORM_FN = ctypes.CFUNCTYPE(ctypes.c_double, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32,
+                              ctypes.c_uint64)
+
+
+@contextlib.contextmanager
+def uniform_override(fn):
+    """Within the block, every uniform the oracle's draws consume is
+    ``fn(seq_key, stream, trial, pos, n)`` (a float in (0, 1]) instead of the
+    Philox value -- for tests that enumerate a draw's variates on a grid or
+    build a decision with a known margin.  Use with ``threads=1``."""
+    lib = _load()
+    cb = UNIFORM_FN(fn)
+    lib.spvo_set_uniform_override(ctypes.cast(cb, ctypes.c_void_p))
+    try:
+        yield
+    finally:
+        lib.spvo_set_uniform_override(None)
 
 
 def softmax_stats(z, T: float):

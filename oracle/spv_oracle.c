@@ -111,10 +111,26 @@ double spvo_uniform(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t 
     return (double)((w >> 8) + 1u) * ldexp(1.0, -24);
 }
 
+/* Test hook (tests only; NULL in every other use): when set, every uniform a
+ * draw consumes comes from this function instead of Philox, with the same
+ * arguments.  The tests use it to enumerate a draw's variates on a grid and
+ * to build decisions whose margin is known in advance.  spvo_uniform itself
+ * is never overridden. */
+typedef double (*spvo_uniform_fn)(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t pos, uint64_t n);
+static spvo_uniform_fn uniform_override = NULL;
+void spvo_set_uniform_override(spvo_uniform_fn fn) { uniform_override = fn; }
+
+/* The uniform of draw n of (stream, trial, position), as the draws use it. */
+static double draw_uniform(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t pos, uint64_t n)
+{
+    if (uniform_override) return uniform_override(seq_key, stream, trial, pos, n);
+    return spvo_uniform(seq_key, stream, trial, pos, n);
+}
+
 /* Exp(1) variate from the same draw: E = -ln U. */
 static double expo(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t pos, uint64_t n)
 {
-    return -log(spvo_uniform(seq_key, stream, trial, pos, n));
+    return -log(draw_uniform(seq_key, stream, trial, pos, n));
 }
 
 /* ------------------------------------------------------------------------ */
@@ -324,7 +340,7 @@ int spvo_verify_chain_seq(const float *tgt, const float *drf, const int32_t *tok
         for (t = 0; t < SPVO_MAX_TRIALS; ++t) {
             int x = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, (uint32_t)t,
                                 (uint32_t)k, &margin);
-            double v = spvo_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
+            double v = draw_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
             double p = w[x], q = prob(dj, x, T, Md[k], Sd[k]);
             note_margin(&margin, fabs((1.0 - v) - q / p));
             if (q <= (1.0 - v) * p) { emitted = x; break; }
@@ -648,7 +664,7 @@ int spvo_verify_saguaro_seq(const float *tgt, const float *drf, const int32_t *t
         for (t = 0; t < SPVO_MAX_TRIALS; ++t) {
             int x = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, (uint32_t)t,
                                 (uint32_t)k, &margin);
-            double v = spvo_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
+            double v = draw_uniform(seq_key, SPVO_STREAM_ACCEPT, (uint32_t)t, (uint32_t)k, 0);
             double p = w[x], q = sag_prob(dj, sj, x, T, Md[k], Sd[k], invC);
             note_margin(&margin, fabs((1.0 - v) - q / p));
             if (q <= (1.0 - v) * p) {
@@ -726,7 +742,7 @@ static int tree_trials(const double *w, const float *dj, int V, double T, double
     int t;
     for (t = 0; t < SPVO_MAX_TRIALS; ++t) {
         int x = race_sample(w, V, key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, (uint32_t)t, pos, margin);
-        double v = spvo_uniform(key, SPVO_STREAM_ACCEPT, (uint32_t)t, pos, 0);
+        double v = draw_uniform(key, SPVO_STREAM_ACCEPT, (uint32_t)t, pos, 0);
         double p = w[x], q = sres * prob(dj, x, T, Md, Sd);
         note_margin(margin, fabs((1.0 - v) - q / p));
         if (q <= (1.0 - v) * p) { *trials = t + 1; return x; }

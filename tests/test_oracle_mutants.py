@@ -10,6 +10,7 @@ import subprocess
 import pytest
 
 import oracle
+import test_oracle_enumeration as enum
 import test_oracle_pins as pins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "spv_oracle.c")
@@ -17,7 +18,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "spv_oracle.c")
 MUTANTS = {
     "accept_transposed": ("int acc = (p > 0) && ((double)r[i] * q <= p);",
                           "int acc = (p > 0) && ((double)r[i] * p <= q);",
-                          ["test_acceptance_rate_is_one_minus_tvd", "test_target_above_draft_always_accepts"]),
+                          ["test_acceptance_rate_is_one_minus_tvd", "test_target_above_draft_always_accepts",
+                           "test_enumeration_designed_thresholds"]),
     "residual_sign": ("double d = w[x] - prob(dj, x, T, Md[k], Sd[k]);",
                       "double d = prob(dj, x, T, Md[k], Sd[k]) - w[x];",
                       ["test_residual_fallback_is_exact"]),
@@ -25,12 +27,13 @@ MUTANTS = {
                         "const float *tb = tgt + (size_t)(gamma - 1) * V;",
                         ["test_bonus_is_distributed_as_last_target_row"]),
     "no_first_rejection_stop": ("if (i < k) { /* decisions", "if (1) { /* decisions",
-                                ["test_expected_tokens_per_iteration", "test_output_length_and_padding"]),
+                                ["test_expected_tokens_per_iteration", "test_output_length_and_padding",
+                                 "test_enumeration_arbitrary_pairs"]),
     "temperature_dropped": ("return exp((double)z[x] / T - M) / S;", "return exp((double)z[x] - M) / S;",
                             ["test_acceptance_rate_is_one_minus_tvd"]),
     "trial_accept_inverted": ("if (q <= (1.0 - v) * p) { emitted = x; break; }",
                               "if (p <= (1.0 - v) * q) { emitted = x; break; }",
-                              ["test_residual_distribution_on_forced_rejection"]),
+                              ["test_residual_distribution_on_forced_rejection", "test_trial_acceptance_enumerated"]),
     "block_race_weight": ("arr[b] = Wb > 0 ? expo(key, s_block, trial, pos, (uint64_t)b) / Wb : INFINITY;",
                           "arr[b] = Wb > 0 ? expo(key, s_block, trial, pos, (uint64_t)b) * Wb : INFINITY;",
                           ["test_first_token_is_distributed_as_target", "test_bonus_is_distributed_as_last_target_row"]),
@@ -95,13 +98,37 @@ MUTANTS = {
     "tree_draw_ignores_shift": ("emitted = tree_trials(w, du, V, T, Md, Sd, s, seq_key,",
                                 "emitted = tree_trials(w, du, V, T, Md, Sd, 1.0, seq_key,",
                                 ["test_tree_first_token_is_exact"]),
+    "accept_margin_transposed": ("double m = (q > 0) ? fabs((double)r[i] - p / q) : INFINITY;",
+                                 "double m = (q > 0) ? fabs((double)r[i] - q / p) : INFINITY;",
+                                 ["test_accept_margin_is_the_ratio_gap"]),
+    "accept_margin_off_path": ("        if (i < k) { /* decisions up to the first rejection decide the output */\n"
+                               "            double m = (q > 0) ? fabs((double)r[i] - p / q) : INFINITY;\n"
+                               "            note_margin(&margin, m);\n",
+                               "        double m = (q > 0) ? fabs((double)r[i] - p / q) : INFINITY;\n"
+                               "        note_margin(&margin, m);\n"
+                               "        if (i < k) { /* decisions up to the first rejection decide the output */\n",
+                               ["test_margin_counts_only_the_decisions_on_the_output_path"]),
+    "race_margin_linear_gap": ("else m = log(a2) - log(a1);", "else m = a2 - a1;",
+                               ["test_race_margin_is_the_log_gap_of_the_two_earliest_arrivals"]),
+    "trial_margin_wrong_side": ("note_margin(&margin, fabs((1.0 - v) - q / p));\n            if (q <= (1.0 - v) * p) { emitted = x; break; }",
+                                "note_margin(&margin, fabs(v - q / p));\n            if (q <= (1.0 - v) * p) { emitted = x; break; }",
+                                ["test_trial_margin_is_the_gap_of_one_minus_v_to_q_over_p"]),
+    "accept_ignores_draft": ("int acc = (p > 0) && ((double)r[i] * q <= p);",
+                             "int acc = (p > 0) && ((double)r[i] <= p);",
+                             ["test_enumeration_designed_thresholds"]),
     "fanout_formula": ("return (double)F0 * pow(a, (double)k / (1.0 + r));", "return (double)F0 * pow(a, (double)k / r);",
                        ["test_fanout_sizes_golden"]),
 }
 
 
 def _calls(name):
-    fn = getattr(pins, name)
+    fn = getattr(pins, name, None) or getattr(enum, name)
+    if name == "test_enumeration_designed_thresholds":
+        return [lambda: fn(1, 4, 0), lambda: fn(2, 3, 2)]
+    if name == "test_enumeration_arbitrary_pairs":
+        return [lambda: fn(1, 5, 4096, 11)]
+    if name == "test_trial_acceptance_enumerated":
+        return [lambda: fn(5, 21)]
     if name == "test_acceptance_rate_is_one_minus_tvd":
         return [lambda: fn(1.0), lambda: fn(0.6)]
     if name == "test_fanout_vs_numpy_lexsort":

@@ -98,7 +98,10 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
  *   out_resid_norm [B] fp32 out, optional: sum_x max(0, p_k - q_k) when
  *                  k < gamma, 1 for the bonus.  Costs one extra read of the
  *                  rejected row pair per sequence; pass NULL on the hot path.
- *   row_status     [B] int32 out, optional: SPV_OK or SPV_ERR_BAD_ROW
+ *   row_status     [B] int32 out, optional: SPV_OK, SPV_ERR_BAD_ROW, or
+ *                  SPV_ERR_TIMEOUT when the workspace's error word records a
+ *                  bounded wait that gave up (the sequence's statistics may be
+ *                  incomplete; its accept_count and out_tokens are then -1)
  *   workspace      device scratch of >= spv_chain_workspace_bytes(B,gamma,V)
  *                  bytes, 256-byte aligned.  Its first 4 bytes are a sticky
  *                  error word (see spv_workspace_status); bytes 8..15 are
@@ -282,17 +285,26 @@ size_t spv_tree_workspace_bytes(int B, int N, int V);
  * library's own device memory.  The call allocates and frees nothing.
  *
  *   - Returns SPV_ERR_UNSUPPORTED when the call needs more scratch than the
- *     array holds (spv_chain_workspace_bytes(B, gamma, V) >
- *     SPV_NOALLOC_SCRATCH_BYTES; e.g. B = 64, gamma = 4, V = 151,936 needs
- *     about 0.7 MB, B = 256 about 2.9 MB).
+ *     array holds: spv_chain_workspace_bytes(B, gamma, V) >
+ *     SPV_NOALLOC_SCRATCH_BYTES for T > 0, spv_greedy_workspace_bytes(B,
+ *     gamma, V) > SPV_NOALLOC_SCRATCH_BYTES for T == 0 (e.g. B = 64,
+ *     gamma = 4, V = 151,936 needs about 0.7 MB at T > 0, B = 256 about
+ *     2.9 MB).  Other argument errors are those of spv_verify_chain.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current) and keeps it; make
  *     that first call before any stream capture.
  *   - Every call on a device uses the same array, and the array keeps the
  *     last call's contents.  Calls whose kernels may overlap on the GPU (on
  *     different streams, or from different host threads) race on it and
- *     must be serialised by the caller.  Each call clears the array's error
- *     word first (an asynchronous 4-byte memset on `stream`).
+ *     must be serialised by the caller.  Each call first clears the array's
+ *     16-byte call header -- the error word, the self-test flag and the
+ *     streaming pass's work-item counter -- with an asynchronous memset on
+ *     `stream`, so a call that failed part-way (the caller cannot zero-fill
+ *     this array) leaves nothing that changes the next call's results.
+ *   - A bounded wait of the call's streaming pass that gave up cannot be read
+ *     back with spv_workspace_status (the caller has no pointer to the
+ *     array); the call reports it in its outputs instead: accept_count -1,
+ *     out_tokens -1 and row_status SPV_ERR_TIMEOUT for every sequence.
  */
 spv_status spv_verify_chain_noalloc(const void *target_logits, const void *draft_logits, spv_dtype dtype,
                                     const int32_t *draft_tokens, const float *r, const uint64_t *sample_keys,
@@ -339,9 +351,21 @@ spv_status spv_fanout_topk(const void *draft_logits, spv_dtype dtype, const int3
 
 size_t spv_fanout_workspace_bytes(int B, int K, int V, int max_fanout);
 
-/* [SSD] "Core Technical Barrier" (Theorem 12): F_0 * a^(k/(1+r)); the caller
- * rounds (the fan-out workload rounds half away from zero). */
+/* [SSD] "Core Technical Barrier" (Theorem 12): F_0 * a^(k/(1+r)), unrounded. */
 double spv_fanout_size(int F0, double a, double r, int k);
+
+/*
+ * spv_fanout_sizes -- the integer fan-out of [SSD] "Core Technical Barrier"
+ * (Theorem 12) for positions k = 0..K: F_k = F_0 * a^(k/(1+r)) rounded half
+ * away from zero (the page gives the real-valued law; the rounding is this
+ * library's reading) and clamped to [0, V-1] (at most V-1 ids remain once
+ * the verified token is excluded).  Host function, no CUDA call.
+ *   F0 >= 0, a > 0 finite, r > -1 finite, 0 <= K < SPV_MAX_FANOUT_ROWS, V >= 2
+ *   out   K+1 int32, HOST array
+ * Returns SPV_OK, or SPV_ERR_INVALID_ARG (out untouched).  The result can be
+ * passed to spv_fanout_topk when every F_k <= SPV_MAX_FANOUT.
+ */
+spv_status spv_fanout_sizes(int F0, double a, double r, int K, int V, int32_t *out);
 
 /* Reads the device error word of a workspace (synchronises `stream`):
  * SPV_OK, or SPV_ERR_TIMEOUT if a bounded wait in an earlier call gave up. */

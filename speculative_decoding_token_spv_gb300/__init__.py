@@ -28,6 +28,7 @@ SPV_SAMPLER_SUB = 32
 SPV_MAX_TRIALS = 64
 SPV_MAX_TOP_K = 64
 SPV_MAX_TREE_NODES = 64
+SPV_NOALLOC_SCRATCH_BYTES = 4 * 1024 * 1024
 
 _lib = None
 
@@ -77,6 +78,8 @@ def load_library():
     lib.spv_fanout_workspace_bytes.restype = S
     lib.spv_fanout_size.argtypes = [I, ctypes.c_double, ctypes.c_double, I]
     lib.spv_fanout_size.restype = ctypes.c_double
+    lib.spv_fanout_sizes.argtypes = [I, ctypes.c_double, ctypes.c_double, I, I, P]
+    lib.spv_fanout_sizes.restype = I
     lib.spv_workspace_status.argtypes = [P, P]
     lib.spv_selftest_timeout.argtypes = [P, S, ctypes.c_uint, P]
     lib.spv_selftest_timeout.restype = I
@@ -412,7 +415,13 @@ def spv_fanout_topk(draft_logits, exclude, fanout, *, workspace=None, out=None, 
     return out
 
 
-def fanout_sizes(F0: int, a: float, r: float, K: int, V: int) -> list:
-    """F_k = round(F0 * a^(k/(1+r))) for k = 0..K, half away from zero, clamped to [0, V-1]."""
-    import math
-    return [max(0, min(V - 1, int(math.floor(spv_fanout_size(F0, a, r, k) + 0.5)))) for k in range(K + 1)]
+def spv_fanout_sizes(F0: int, a: float, r: float, K: int, V: int) -> list:
+    """F_k for k = 0..K from the C library (rounded half away from zero,
+    clamped to [0, V-1])."""
+    out = (ctypes.c_int32 * (max(int(K), 0) + 1))()
+    _check(load_library().spv_fanout_sizes(int(F0), float(a), float(r), int(K), int(V), ctypes.addressof(out)),
+           "spv_fanout_sizes")
+    return list(out)
+
+
+fanout_sizes = spv_fanout_sizes

@@ -602,8 +602,9 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
     static constexpr int FIN_WARPS = FWV;
     static constexpr int FIN_BUF_FLOATS = 2 * FWV * G;  // per warp: one target and one draft block
 
-    // Outputs of a bad row: -1 ids and count, NaN p / q / Z, status, cache miss.
-    __device__ static void write_bad_row(const Params &P, int b, int warp, int lane)
+    // Outputs of a bad row: -1 ids and count, NaN p / q / Z, status (bad row,
+    // or timeout when a bounded wait of the streaming pass gave up), cache miss.
+    __device__ static void write_bad_row(const Params &P, int b, int warp, int lane, int status = STATUS_BAD_ROW)
     {
         constexpr int NT = FWV * 32;
         const int g = P.gamma;
@@ -613,7 +614,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 P.out_pq[static_cast<size_t>(b) * 2 * g + i] = __int_as_float(0x7fffffff);
         if (threadIdx.x == 0) {
             P.accept_count[b] = -1;
-            if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
+            if (P.row_status) P.row_status[b] = status;
             if (P.out_Z) P.out_Z[b] = __int_as_float(0x7fffffff);
         }
         if (warp == 0) cache_lookup(P.cache, b, -1, -1, lane);
@@ -683,11 +684,12 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
+        if (threadIdx.x == 32 && workspace_timed_out(P.err)) atomicOr(&sm.bad, 2);  // statistics incomplete
         // B. Row statistics from the block statistics (all rows at once).
         Base::template merge_stats<FWV, false>(P, b, sm, g + 1, true, warp, lane);
         fin_sync<FWV>();
         if (sm.bad) {
-            write_bad_row(P, b, warp, lane);
+            write_bad_row(P, b, warp, lane, (sm.bad & 2) ? STATUS_TIMEOUT : STATUS_BAD_ROW);
             return;
         }
         // Race factors of the target rows (read by the draws after the
@@ -1346,6 +1348,7 @@ template <int DT> struct GreedyOp {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         consumer_sync();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
+        if (threadIdx.x == 32 && workspace_timed_out(P.err)) atomicOr(&sm.bad, 2);  // block results incomplete
         for (int rho = warp; rho < R; rho += NCW) {
             const int2 *bb = P.best + (static_cast<long long>(b) * R + rho) * nb;
             float bv = -INFINITY;
@@ -1384,7 +1387,7 @@ template <int DT> struct GreedyOp {
                 for (int i = lane; i <= g; i += 32) P.out_tokens[static_cast<size_t>(b) * (g + 1) + i] = -1;
                 if (lane == 0) {
                     P.accept_count[b] = -1;
-                    if (P.row_status) P.row_status[b] = STATUS_BAD_ROW;
+                    if (P.row_status) P.row_status[b] = (sm.bad & 2) ? STATUS_TIMEOUT : STATUS_BAD_ROW;
                 }
                 cache_lookup(P.cache, b, -1, -1, lane);
             } else {

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "spv.h"
+
 namespace spv {
 
 // Workspace header: word 0 is the device error word (SPV_OK or
@@ -66,6 +68,31 @@ struct FanoutLaunch {
     void *ws;
     bool tma;
 };
+
+// The arguments spv_verify_chain shares with spv_verify_chain_noalloc.
+struct ChainArgs {
+    const void *target_logits, *draft_logits;
+    spv_dtype dtype;
+    const int32_t *draft_tokens;
+    const float *r;
+    const uint64_t *sample_keys;
+    int B, gamma, V;
+    float temperature;
+    int32_t *accept_count, *out_tokens;
+    float *out_pq, *out_resid_norm;
+    int32_t *row_status;
+};
+
+// Host checks of those arguments (pointers, dtype, sizes, temperature):
+// SPV_OK or the status the call returns before any launch.
+spv_status check_chain_args(const ChainArgs &a);
+// Scratch bytes the call needs (greedy layout at T == 0).
+size_t chain_call_ws_bytes(const ChainArgs &a);
+// The launch description of a checked call on scratch `ws` (no cache lookup,
+// no Saguaro weights).
+ChainLaunch chain_launch(const ChainArgs &a, void *ws);
+// Enqueues the call: the greedy kernels at T == 0, else the chain kernels.
+cudaError_t launch_chain_or_greedy(const ChainLaunch &L, cudaStream_t st);
 
 size_t chain_ws_bytes(int B, int gamma, int V);
 size_t greedy_ws_bytes(int B, int gamma, int V);

@@ -19,7 +19,6 @@
 #include "spv_internal.h"
 
 #include <atomic>
-#include <cmath>
 #include <cstdint>
 
 namespace {
@@ -27,6 +26,7 @@ namespace {
 static __device__ __align__(256) unsigned char spv_noalloc_scratch[SPV_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+constexpr size_t kHeaderClearBytes = 16;  // error word, self-test flag, work-item counter
 std::atomic<void *> g_scratch_ptr[kMaxDevices];
 
 // Device address of this device's copy of the scratch array (set up once per
@@ -44,8 +44,6 @@ cudaError_t scratch_address(int dev, void **out)
     return cudaSuccess;
 }
 
-bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
 }  // namespace
 
 extern "C" spv_status spv_verify_chain_noalloc(const void *target_logits, const void *draft_logits,
@@ -55,45 +53,40 @@ extern "C" spv_status spv_verify_chain_noalloc(const void *target_logits, const 
                                                float *out_pq, float *out_resid_norm, int32_t *row_status,
                                                void *stream)
 {
-    if ((dtype != SPV_F32 && dtype != SPV_BF16) || !target_logits || !draft_tokens || !accept_count ||
-        !out_tokens)
-        return SPV_ERR_INVALID_ARG;
-    if (gamma < 1 || gamma > SPV_MAX_GAMMA || B < 1 || V < 2) return SPV_ERR_INVALID_ARG;
-    if (static_cast<double>(B) * (2 * gamma + 1) * V >= 9.0e15) return SPV_ERR_INVALID_ARG;
-    if (!(temperature >= 0.0f) || std::isinf(temperature)) return SPV_ERR_INVALID_ARG;
-    const bool greedy = temperature == 0.0f;
-    if (!greedy && (!draft_logits || !r || !sample_keys)) return SPV_ERR_INVALID_ARG;
-    if (!greedy && !(1.0f / temperature < INFINITY)) return SPV_ERR_INVALID_ARG;
-    const size_t need = greedy ? spv::greedy_ws_bytes(B, gamma, V) : spv::chain_ws_bytes(B, gamma, V);
-    if (need > static_cast<size_t>(SPV_NOALLOC_SCRATCH_BYTES)) return SPV_ERR_UNSUPPORTED;
+    const spv::ChainArgs a{target_logits, draft_logits, dtype, draft_tokens, r, sample_keys, B, gamma, V,
+                           temperature, accept_count, out_tokens, out_pq, out_resid_norm, row_status};
+    const spv_status chk = spv::check_chain_args(a);
+    if (chk != SPV_OK) return chk;
+    if (spv::chain_call_ws_bytes(a) > static_cast<size_t>(SPV_NOALLOC_SCRATCH_BYTES)) return SPV_ERR_UNSUPPORTED;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return SPV_ERR_CUDA;
     void *scratch = nullptr;
     if (scratch_address(dev, &scratch) != cudaSuccess) return SPV_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The first word of the scratch is the timeout flag: start each call clear.
-    if (cudaMemsetAsync(scratch, 0, sizeof(unsigned), st) != cudaSuccess) return SPV_ERR_CUDA;
+    // Start every call from a clear header: the error word, the self-test
+    // flag and the streaming pass's work-item counter (bytes 0..15).  A caller
+    // owning a workspace zero-fills it after a failed call; nobody can do that
+    // for this array, so a counter left behind by a call whose finalize never
+    // ran would otherwise make every later call skip work items.
+    if (cudaMemsetAsync(scratch, 0, kHeaderClearBytes, st) != cudaSuccess) return SPV_ERR_CUDA;
+    return spv::launch_chain_or_greedy(spv::chain_launch(a, scratch), st) == cudaSuccess ? SPV_OK : SPV_ERR_CUDA;
+}
 
-    spv::ChainLaunch L{};
-    L.target = target_logits;
-    L.draft = draft_logits;
-    L.dtype = dtype == SPV_F32 ? 0 : 1;
-    L.tokens = draft_tokens;
-    L.r = r;
-    L.keys = sample_keys;
-    L.B = B;
-    L.gamma = gamma;
-    L.V = V;
-    L.T = temperature;
-    L.accept_count = accept_count;
-    L.out_tokens = out_tokens;
-    L.out_pq = out_pq;
-    L.out_Z = out_resid_norm;
-    L.row_status = row_status;
-    L.ws = scratch;
-    const int eb = dtype == SPV_F32 ? 4 : 2;
-    L.tma = (static_cast<size_t>(V) * eb) % 16 == 0 && aligned16(target_logits) && (greedy || aligned16(draft_logits));
-    const cudaError_t e = greedy ? spv::launch_greedy(L, st) : spv::launch_chain(L, st);
-    return e == cudaSuccess ? SPV_OK : SPV_ERR_CUDA;
+// Test hook, not part of the ABI (spv.h does not declare it): writes `value`
+// into the scratch array's work-item counter on `stream`, the state a call
+// that failed between its two launches would leave behind, so a test can
+// check that the next call still starts from a clear header.
+extern "C" spv_status spv_internal_noalloc_set_item_counter(unsigned long long value, void *stream)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPV_ERR_CUDA;
+    void *scratch = nullptr;
+    if (scratch_address(dev, &scratch) != cudaSuccess) return SPV_ERR_CUDA;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // `value` lives on this stack frame: wait for the copy before returning.
+    if (cudaMemcpyAsync(static_cast<unsigned char *>(scratch) + 8, &value, sizeof(value), cudaMemcpyHostToDevice,
+                        st) != cudaSuccess)
+        return SPV_ERR_CUDA;
+    return cudaStreamSynchronize(st) == cudaSuccess ? SPV_OK : SPV_ERR_CUDA;
 }

@@ -165,6 +165,15 @@ __device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned *p)
     return v;
 }
 
+// Whether a bounded wait gave up on this workspace: the error word holds
+// STATUS_TIMEOUT (set by this call's streaming grid, or by an earlier call on
+// the same workspace until it is zero-filled).  Read after the dependent-grid
+// wait, so the streaming grid's writes are visible.
+__device__ __forceinline__ bool workspace_timed_out(const unsigned *err)
+{
+    return *reinterpret_cast<const volatile unsigned *>(err) == static_cast<unsigned>(STATUS_TIMEOUT);
+}
+
 // Bounded wait until *flag >= target (acquire loads, short sleeps between
 // polls); false, with STATUS_TIMEOUT in *err, after `limit` polls.
 __device__ __forceinline__ bool wait_flag_ge(const unsigned *flag, unsigned target, uint32_t limit, unsigned *err)

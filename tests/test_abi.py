@@ -50,6 +50,32 @@ def test_workspace_sizes(lib):
         assert n >= 256
 
 
+def test_binding_constants_match_header():
+    """The binding's copies of the header's limits are the header's values."""
+    import speculative_decoding_token_spv_gb300 as spv
+    src = open(os.path.join(ROOT, "include", "spv.h")).read()
+    defs = dict(re.findall(r"#define[ \t]+(SPV_[A-Z_]+)[ \t]+([^/\n]+?)[ \t]*(?:/\*.*)?$", src, flags=re.M))
+    assert defs, "no limits found in spv.h"
+    for name, val in defs.items():
+        assert getattr(spv, name) == eval(val), name
+
+
+def test_fanout_sizes_in_c(lib):
+    """spv_fanout_sizes rounds F_0 a^(k/(1+r)) half away from zero and clamps to
+    [0, V-1] in C; the golden fan-out of the SSD workload is [8, 7, 6, 5, 4]."""
+    import speculative_decoding_token_spv_gb300 as spv
+    assert spv.spv_fanout_sizes(8, 0.8, 0.5, 4, 128256) == [8, 7, 6, 5, 4]
+    # half away from zero: 2.5 -> 3 (a^(k/(1+r)) = 0.5 at k = 1, r = 0 with F0 = 5)
+    assert spv.spv_fanout_sizes(5, 0.5, 0.0, 2, 1000) == [5, 3, 1]
+    assert spv.spv_fanout_sizes(100, 1.0, 0.0, 1, 40) == [39, 39]       # clamped to V - 1
+    assert spv.spv_fanout_sizes(0, 0.8, 0.5, 3, 100) == [0, 0, 0, 0]
+    out = (ctypes.c_int32 * 2)()
+    for args in ((8, 0.8, 0.5, -1, 100), (8, 0.0, 0.5, 1, 100), (8, 0.8, -1.0, 1, 100), (-1, 0.8, 0.5, 1, 100),
+                 (8, 0.8, 0.5, 1, 1), (8, float("inf"), 0.5, 1, 100), (8, 0.8, 0.5, 64, 100)):
+        assert lib.spv_fanout_sizes(*args, ctypes.addressof(out)) == 1, args
+    assert lib.spv_fanout_sizes(8, 0.8, 0.5, 1, 100, None) == 1
+
+
 def test_fanout_size_and_status_strings(lib):
     import speculative_decoding_token_spv_gb300 as spv
     assert spv.fanout_sizes(8, 0.8, 0.5, 4, 128256) == [8, 7, 6, 5, 4]
@@ -219,3 +245,35 @@ def test_selftest_arguments_rejected_on_host(lib):
     assert lib.spv_selftest_timeout(ws, 4096, (1 << 24) + 1, None) == 1
     assert lib.spv_selftest_timeout(ws, 128, 10, None) == 1
     assert lib.spv_selftest_timeout(P((1 << 20) + 64), 4096, 10, None) == 1
+
+
+def test_noalloc_rejects_calls_beyond_its_scratch(lib):
+    """spv_verify_chain_noalloc refuses, before any CUDA call, a call whose
+    scratch would not fit its fixed array: the chain layout at T > 0, the
+    (smaller) greedy layout at T = 0; other argument errors as
+    spv_verify_chain."""
+    import speculative_decoding_token_spv_gb300 as spv
+    P, I = ctypes.c_void_p, ctypes.c_int
+    f = lib.spv_verify_chain_noalloc
+    f.argtypes = [P, P, I, P, P, P, I, I, I, ctypes.c_float, P, P, P, P, P, P]
+    f.restype = I
+    lim = spv.SPV_NOALLOC_SCRATCH_BYTES
+    fake = P(256)  # never dereferenced: the checks come first
+    g, V = 4, 151936
+
+    def call(B, T, **kw):
+        a = dict(t=fake, tok=fake, k=fake)
+        a.update(kw)
+        return f(a["t"], fake, 0, a["tok"], fake, fake, B, g, V, ctypes.c_float(T), a["k"], fake, None, None, None,
+                 None)
+
+    assert spv.spv_chain_workspace_bytes(600, g, V) > lim >= spv.spv_greedy_workspace_bytes(600, g, V)
+    assert call(600, 1.0) == spv.SPV_ERR_UNSUPPORTED      # chain layout too large
+    assert spv.spv_greedy_workspace_bytes(1024, g, V) > lim
+    assert call(1024, 0.0) == spv.SPV_ERR_UNSUPPORTED     # greedy layout too large
+    assert call(2048, 1.0) == spv.SPV_ERR_UNSUPPORTED
+    assert call(4, 1.0, t=None) == spv.SPV_ERR_INVALID_ARG
+    assert call(4, 1.0, tok=None) == spv.SPV_ERR_INVALID_ARG
+    assert call(4, -1.0) == spv.SPV_ERR_INVALID_ARG
+    assert call(4, float("nan")) == spv.SPV_ERR_INVALID_ARG
+    assert call(0, 1.0) == spv.SPV_ERR_INVALID_ARG

@@ -103,6 +103,27 @@ def test_eagle(spv, gamma, T):
     check_chain(spv, w)
 
 
+@pytest.mark.parametrize("case", ["spd_B64_bf16", "sweep_B256_fp32"])
+def test_greedy_entry_point(spv, case):
+    """spv_verify_greedy itself (its own argument checks and greedy-sized
+    workspace), bit-exact against the oracle's argmax rule: the SPD gamma = 1
+    workload (B = 64, V = 151,936, bf16) and the batch sweep's largest point
+    (B = 256, gamma = 4, fp32)."""
+    if case == "spd_B64_bf16":
+        w = workloads.spd(device="cuda", temperature=0.0)
+    else:
+        w = workloads.sweep(B=256, dtype=torch.float32, device="cuda", temperature=0.0)
+    ws = spv.new_workspace(spv.spv_greedy_workspace_bytes(w.B, w.gamma, w.V), "cuda")
+    got = spv.spv_verify_greedy(w.target, w.tokens, workspace=ws)
+    torch.cuda.synchronize()
+    ref = oracle.verify_greedy(_np(w.target), _np(w.tokens))
+    assert np.array_equal(_np(got["accept_count"]), ref["accept_count"])
+    assert np.array_equal(_np(got["out_tokens"]), ref["out_tokens"])
+    assert np.array_equal(_np(got["row_status"]), ref["status"])
+    k = ref["accept_count"]
+    assert (k == 0).any() and (k > 0).any()  # both a mismatch and an accepted draft token occur
+
+
 def test_fanout_config(spv):
     fw = workloads.fanout(device="cuda")
     sizes = spv.fanout_sizes(8, 0.8, 0.5, 4, fw.draft.shape[2])

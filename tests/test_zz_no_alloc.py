@@ -77,12 +77,40 @@ def test_noalloc_matches_workspace_entry_point(lib, case):
             np.testing.assert_allclose(got["pq"].cpu().numpy(), ref["pq"].cpu().numpy(), rtol=RTOL)
 
 
-def test_noalloc_rejects_calls_beyond_its_scratch(lib):
+def test_noalloc_starts_from_a_clear_header(lib):
+    """A work-item counter left nonzero in the scratch array (what a call that
+    failed between its two launches leaves) changes nothing: every call clears
+    the array's header before its kernels run."""
     import speculative_decoding_token_spv_gb300 as spv
-    limit = 4 * 1024 * 1024
-    B, g, V = 2048, 4, 151936  # needs about 23 MB of scratch
-    assert spv.spv_chain_workspace_bytes(B, g, V) > limit
-    fake = ctypes.c_void_p(256)  # never dereferenced: the size check comes first
-    st = lib.spv_verify_chain_noalloc(fake, fake, 0, fake, fake, fake, B, g, V, ctypes.c_float(1.0), fake, fake,
-                                      None, None, None, None)
-    assert st == spv.SPV_ERR_UNSUPPORTED
+    lib.spv_internal_noalloc_set_item_counter.argtypes = [ctypes.c_ulonglong, ctypes.c_void_p]
+    lib.spv_internal_noalloc_set_item_counter.restype = ctypes.c_int
+    w = workloads.sweep(B=64, dtype=torch.float32, device="cuda", temperature=1.0)
+    ref = spv.spv_verify_chain(w.target, w.draft, w.tokens, w.r, w.keys, w.temperature)
+    torch.cuda.synchronize()
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    for planted in (1000, 1 << 40):
+        assert lib.spv_internal_noalloc_set_item_counter(planted, stream) == 0
+        got = _noalloc(lib, w)
+        torch.cuda.synchronize()
+        assert torch.equal(got["accept_count"], ref["accept_count"])
+        assert torch.equal(got["out_tokens"], ref["out_tokens"])
+        assert torch.equal(got["row_status"], ref["row_status"])
+        np.testing.assert_allclose(got["pq"].cpu().numpy(), ref["pq"].cpu().numpy(), rtol=RTOL)
+
+
+def test_noalloc_greedy_uses_the_greedy_scratch_bound(lib):
+    """At T = 0 the call needs only the greedy layout: B = 600, gamma = 4,
+    V = 151,936 fits the array at T = 0 (about 3.6 MB) although the chain
+    layout would not, and matches spv_verify_greedy."""
+    import speculative_decoding_token_spv_gb300 as spv
+    B, g, V = 600, 4, 151936
+    assert spv.spv_greedy_workspace_bytes(B, g, V) <= spv.SPV_NOALLOC_SCRATCH_BYTES
+    assert spv.spv_chain_workspace_bytes(B, g, V) > spv.SPV_NOALLOC_SCRATCH_BYTES
+    w = workloads.sweep(B=B, dtype=torch.bfloat16, device="cuda", temperature=0.0)
+    ref = spv.spv_verify_greedy(w.target, w.tokens)
+    torch.cuda.synchronize()
+    got = _noalloc(lib, w)
+    torch.cuda.synchronize()
+    assert torch.equal(got["accept_count"], ref["accept_count"])
+    assert torch.equal(got["out_tokens"], ref["out_tokens"])
+    assert torch.equal(got["row_status"], ref["row_status"])

@@ -80,10 +80,14 @@ typedef enum { SPV_F32 = 0, SPV_BF16 = 1 } spv_dtype;
  * q_k(x) <= (1 - v) p_k(x)), then, if none is accepted, by the same race over
  * max(0, p_k - q_k) directly.  U = ((w >> 8) + 1) * 2^-24 for one 32-bit
  * word w of Philox4x32-10 with key (low, high half of sample_keys[b]) and
- * counter (n / 4, stream, trial, position), word n % 4, where n is the
- * block, global sub-block (id / 32) or id index; streams 1 / 2 / 3 block /
- * sub-block / id race, 4 trial acceptance, 5 / 6 / 7 the direct residual
- * race.  Trials are numbered from 0; the bonus is trial 0 at position gamma.
+ * counter (n / 4, stream, trial, 0), word n % 4, where n is the block index,
+ * the sub-block's index within its block (0..31) or the id's offset within
+ * its sub-block (0..31); streams 1 / 2 / 3 block / sub-block / id race, 4
+ * trial acceptance (n = 0), 5 / 6 / 7 the direct residual race.  Trials are
+ * numbered from 0; the bonus is trial 0.  The position of the draw is not in
+ * the counter: a sequence makes exactly one draw, so its variates are i.i.d.
+ * whatever the position, and given the winning block (sub-block) the
+ * sub-block (id) variates are fresh -- every level of the race stays exact.
  *
  * Arguments (all device pointers unless noted):
  *   target_logits  [B, gamma+1, V] dtype
@@ -200,7 +204,7 @@ spv_status spv_verify_chain_cached(const void *target_logits, const void *draft_
  * bonus from p'_gamma.  The draw is an exponential race over the kept ids
  * of target row k: the id x with the smallest E_x / w(x) wins (w the
  * residual or bonus mass, E_x = -ln U with U from Philox4x32-10 as for
- * spv_verify_chain, counter (x / 4, 8, 0, k), word x % 4; ties to the lower
+ * spv_verify_chain, counter (x / 4, 8, 0, 0), word x % 4; ties to the lower
  * id).  A rejection whose residual has no mass (a draft token outside q's
  * support with p' = q' elsewhere) makes the row bad.
  *
@@ -241,7 +245,7 @@ size_t spv_filtered_workspace_bytes(int B, int gamma, int V);
  * of u is rejected one token is drawn from P_m (the chain's rejection trials
  * from p_u with q scaled by s_m, then the direct residual race); at a leaf
  * the bonus token from p_u.  Draws follow spv_verify_chain's sampling rule
- * with position = the node index.  A tree that is one path is
+ * (one draw per sequence).  A tree that is one path is
  * spv_verify_chain exactly (r[b, i+1] <-> r[b, i]).  T == 0: descend into the
  * first child whose token is the argmax of p_u (lowest id on ties), emit the
  * last node's argmax; draft_logits, r and sample_keys are then not read.

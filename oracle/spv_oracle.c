@@ -43,7 +43,12 @@
  *         failed trials the residual is drawn directly by the same race over
  *         the residual masses, so the output stays exact.
  *     Every exponential comes from E = -ln U, U = ((w >> 8) + 1) * 2^-24,
- *     w one 32-bit word of Philox4x32-10 keyed by the sequence's 64-bit key.
+ *     w one 32-bit word of Philox4x32-10 keyed by the sequence's 64-bit key,
+ *     counter (n / 4, stream, trial, 0), word n % 4, where n is the block
+ *     index, the sub-block's index within its block, or the id's offset
+ *     within its sub-block.  The position of the draw is not in the counter
+ *     (a sequence makes one draw), and given the winning block the sub-block
+ *     and id variates are fresh, so every level stays exact.
  *   - Ties in a race, in an argmax and in the fan-out order go to the lower
  *     index; -0.0 ranks equal to +0.0.
  *   - NaN or +inf in any row read, a row without a finite entry (in the
@@ -120,11 +125,15 @@ typedef double (*spvo_uniform_fn)(uint64_t seq_key, uint32_t stream, uint32_t tr
 static spvo_uniform_fn uniform_override = NULL;
 void spvo_set_uniform_override(spvo_uniform_fn fn) { uniform_override = fn; }
 
-/* The uniform of draw n of (stream, trial, position), as the draws use it. */
+/* The uniform of draw n of (stream, trial) for a draw made at position pos.
+ * The counter's fourth word is 0, not the position: a sequence makes exactly
+ * one draw (the residual at its first rejection, or the bonus), so the
+ * variates it uses are i.i.d. whatever the position, and they can be
+ * generated before the position is known. */
 static double draw_uniform(uint64_t seq_key, uint32_t stream, uint32_t trial, uint32_t pos, uint64_t n)
 {
     if (uniform_override) return uniform_override(seq_key, stream, trial, pos, n);
-    return spvo_uniform(seq_key, stream, trial, pos, n);
+    return spvo_uniform(seq_key, stream, trial, 0, n);
 }
 
 /* Exp(1) variate from the same draw: E = -ln U. */
@@ -213,20 +222,21 @@ static int race_sample(const double *w, int V, uint64_t key, uint32_t s_block, u
     }
     int bw = race_winner(arr, nb, margin);
     int lo = bw * SPVO_BLOCK, hi = lo + SPVO_BLOCK < V ? lo + SPVO_BLOCK : V;
-    /* level 2: sub-blocks of the winning block (global sub-block index s0 / SPVO_SUB) */
+    /* level 2: sub-blocks of the winning block; variate n = j, the sub-block's
+     * index within the block (given the block, i.i.d. whichever block won) */
     int ns = (hi - lo + SPVO_SUB - 1) / SPVO_SUB;
     for (int j = 0; j < ns; ++j) {
         int s0 = lo + j * SPVO_SUB, s1 = s0 + SPVO_SUB < hi ? s0 + SPVO_SUB : hi;
         ksum W = { 0, 0 };
         for (int x = s0; x < s1; ++x) ksum_add(&W, w[x]);
         double Ws = ksum_val(&W);
-        arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)(s0 / SPVO_SUB)) / Ws : INFINITY;
+        arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)j) / Ws : INFINITY;
     }
     int sw = race_winner(arr, ns, margin);
     int s0 = lo + sw * SPVO_SUB, s1 = s0 + SPVO_SUB < hi ? s0 + SPVO_SUB : hi;
-    /* level 3: ids of the winning sub-block */
+    /* level 3: ids of the winning sub-block; variate n = the id's offset in it */
     for (int x = s0; x < s1; ++x)
-        arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)x) / w[x] : INFINITY;
+        arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)(x - s0)) / w[x] : INFINITY;
     int xw = s0 + race_winner(arr, s1 - s0, margin);
     free(arr);
     return xw;

@@ -122,6 +122,49 @@ __device__ __forceinline__ float resid_mass_w(float zt, float zd, float Mt, floa
     return fmaxf(__fsub_rn(p, q), 0.f);
 }
 
+// Word j (0..3) of a Philox group without indexing the register array.
+__device__ __forceinline__ uint32_t word_of(const uint32_t w[4], int j)
+{
+    return j == 0 ? w[0] : (j == 1 ? w[1] : (j == 2 ? w[2] : w[3]));
+}
+
+// The variates of one draw -- a residual trial, or the bonus (trial 0) --
+// held by one warp.  Lane l holds the exponentials E = -ln U of blocks
+// 4 (l + 32 h) + e (h < 2, e < 4: rows of up to PRE_BLOCKS blocks), of
+// sub-block l of the winning block, of id offset l in the winning sub-block,
+// and the trial's acceptance word.  None depends on the row, the position or
+// the statistics, so a finalize computes the first round's before its
+// dependent-grid wait.
+constexpr int PRE_BLOCKS = 256;
+struct DrawVariates {
+    float eb[2][4];
+    float es, ex;
+    uint32_t aw;
+};
+
+__device__ __forceinline__ void draw_variates(DrawVariates &dv, uint64_t key, uint32_t trial, int nb, int lane)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int g = lane + 32 * h;
+        if (nb <= PRE_BLOCKS && 4 * g < nb) {
+            philox_group(w, key, STREAM_BLOCK, trial, static_cast<uint32_t>(g));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dv.eb[h][e] = expo(w[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dv.eb[h][e] = 0.f;
+        }
+    }
+    philox_group(w, key, STREAM_SUB, trial, static_cast<uint32_t>(lane) >> 2);
+    dv.es = expo(word_of(w, lane & 3));
+    philox_group(w, key, STREAM_TOKEN, trial, static_cast<uint32_t>(lane) >> 2);
+    dv.ex = expo(word_of(w, lane & 3));
+    philox_group(w, key, STREAM_ACCEPT, trial, 0u);
+    dv.aw = w[0];
+}
+
 template <int DT> struct ChainOp {
     using Params = ChainParams;
     using Smem = ChainSmem;
@@ -249,37 +292,45 @@ template <int DT> struct ChainOp {
     // smallest E_beta / W_beta, W_beta = 2^((m_beta - M) c2) S_beta up to the
     // row normaliser, i.e. arrival E_beta * f_beta with the factor
     // f_beta = 2^((M - m_beta) c2) / S_beta staged by the merge (computed here
-    // when the statistics were not staged).  Every lane gets the winner.
+    // when the statistics were not staged).  The exponentials E_beta come from
+    // dv when it holds them (rows of up to PRE_BLOCKS blocks), else from
+    // Philox here.  Every lane gets the winner.
     __device__ static int race_blocks_p(const Params &P, const Smem &sm, int b, int rho, float M, uint64_t key,
-                                        uint32_t trial, uint32_t pos, int lane)
+                                        uint32_t trial, int lane, const DrawVariates &dv)
     {
         float best = INFINITY;
         int bi = INT_MAX;
-        for (int g = lane; 4 * g < P.nb; g += 32) {
-            float f[4];
+        auto visit = [&](int g, const float E[4]) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int beta = 4 * g + e;
+                float f;
                 if (beta >= P.nb) {
-                    f[e] = -1.f;
+                    f = -1.f;
                 } else if (sm.cached) {
-                    f[e] = sm.st[rho * P.nb + beta].y;
+                    f = sm.st[rho * P.nb + beta].y;
                 } else {
                     const float2 st = __ldcg(&P.stats[(static_cast<long long>(b) * P.R + rho) * P.nb + beta]);
-                    f[e] = st.y > 0.f ? fast_exp2((M - st.x) * P.c2) / st.y : -1.f;
+                    f = st.y > 0.f ? fast_exp2((M - st.x) * P.c2) / st.y : -1.f;
                 }
-            }
-            uint32_t w[4];
-            philox_group(w, key, STREAM_BLOCK, trial, pos, static_cast<uint32_t>(g));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (f[e] >= 0.f) {
-                    const float A = arrival(expo(w[e]), f[e]);
+                if (f >= 0.f) {
+                    const float A = arrival(E[e], f);
                     if (A < best) {
                         best = A;
-                        bi = 4 * g + e;
+                        bi = beta;
                     }
                 }
+            }
+        };
+        if (P.nb <= PRE_BLOCKS) {
+            if (4 * lane < P.nb) visit(lane, dv.eb[0]);
+            if (4 * (lane + 32) < P.nb) visit(lane + 32, dv.eb[1]);
+        } else {
+            for (int g = lane; 4 * g < P.nb; g += 32) {
+                uint32_t w[4];
+                philox_group(w, key, STREAM_BLOCK, trial, static_cast<uint32_t>(g));
+                const float E[4] = {expo(w[0]), expo(w[1]), expo(w[2]), expo(w[3])};
+                visit(g, E);
             }
         }
         warp_argmin(best, bi);
@@ -328,49 +379,25 @@ template <int DT> struct ChainOp {
         __syncwarp();
     }
 
-    // One Philox call per lane: lane l computes draw group g0 + (l & 7) of
-    // `stream` (8 distinct groups, 32 draws), lane 8 instead computes group 0
-    // of `extra` when extra != 0.  spread_word fetches word j of lane src.
-    __device__ static __forceinline__ void philox_spread(uint32_t w[4], uint64_t key, uint32_t stream, uint32_t extra,
-                                                         uint32_t trial, uint32_t pos, uint32_t g0, int lane)
-    {
-        const bool ex = (lane == 8) && extra != 0u;
-        philox_group(w, key, ex ? extra : stream, trial, pos, ex ? 0u : g0 + static_cast<uint32_t>(lane & 7));
-    }
-    __device__ static __forceinline__ uint32_t spread_word(const uint32_t w[4], int src, int j)
-    {
-        const uint32_t a = __shfl_sync(0xffffffffu, w[0], src), b = __shfl_sync(0xffffffffu, w[1], src);
-        const uint32_t c = __shfl_sync(0xffffffffu, w[2], src), d = __shfl_sync(0xffffffffu, w[3], src);
-        return j == 0 ? a : (j == 1 ? b : (j == 2 ? c : d));
-    }
-
     // Levels 2 and 3 of a draw from softmax(row / T) inside block beta (block
     // max mb) whose logits are in buf: lane l owns sub-block l (ids
     // base + 32 l + i) for the sub-block race, then id base + 32 s* + l for
-    // the id race.  If accept != 0 the acceptance word of the trial (group 0
-    // of stream `accept`) is returned in *accept_word.
-    __device__ static int race_in_block_p(const Params &P, const float *buf, int beta, float mb, uint64_t key,
-                                          uint32_t s_sub, uint32_t s_tok, uint32_t trial, uint32_t pos, int lane,
-                                          uint32_t accept = 0u, uint32_t *accept_word = nullptr)
+    // the id race, with the exponentials of dv (sub-block l, id offset l).
+    __device__ static int race_in_block_p(const Params &P, const float *buf, int beta, float mb,
+                                          const DrawVariates &dv, int lane)
     {
         const int base = beta * G;
         // sub-block mass relative to the block max (skewed reads: no bank conflicts)
         float ws = 0.f;
 #pragma unroll 8
         for (int i = 0; i < SUB; ++i) ws += fast_exp2((buf[SUB * lane + ((i + lane) & (SUB - 1))] - mb) * P.c2);
-        uint32_t w[4];
-        philox_spread(w, key, s_sub, accept, trial, pos, static_cast<uint32_t>(base / (4 * SUB)), lane);
-        if (accept_word) *accept_word = __shfl_sync(0xffffffffu, w[0], 8);
-        const uint32_t us = spread_word(w, lane >> 2, lane & 3);  // sub-block n = base/32 + lane: word n & 3
-        float A = ws > 0.f ? arrival(expo(us), 1.f / ws) : INFINITY;
+        float A = ws > 0.f ? arrival(dv.es, 1.f / ws) : INFINITY;
         int si = lane;
         warp_argmin(A, si);
         const int x = base + SUB * si + lane;
         const float z = buf[SUB * si + lane];
         const float msw = warp_max(z);  // max of the winning sub-block
-        philox_spread(w, key, s_tok, 0u, trial, pos, static_cast<uint32_t>(base + SUB * si) >> 2, lane);
-        const uint32_t ut = spread_word(w, lane >> 2, lane & 3);  // id x: group x >> 2, word x & 3
-        float Ax = (x < P.V && z != -INFINITY) ? arrival(expo(ut), fast_exp2((msw - z) * P.c2)) : INFINITY;
+        float Ax = (x < P.V && z != -INFINITY) ? arrival(dv.ex, fast_exp2((msw - z) * P.c2)) : INFINITY;
         int xi = x;
         warp_argmin(Ax, xi);
         return xi;
@@ -463,7 +490,7 @@ template <int DT> struct ChainOp {
     // trials all failed): block masses from residual_pass, then sub-blocks
     // and ids of the winning block (target and draft logits in tb / db).
     __device__ static int race_resid(const Params &P, int b, const unsigned char *tp, const unsigned char *dp, float Mt,
-                                     float St, float Md, float Sd, uint64_t key, uint32_t pos, float *tb, float *db,
+                                     float St, float Md, float Sd, uint64_t key, float *tb, float *db,
                                      const int *sids, float qs, int lane, const float *rb = nullptr)
     {
         if (!rb) rb = P.resid + static_cast<size_t>(b) * P.nb;  // the block masses of the residual
@@ -477,7 +504,7 @@ template <int DT> struct ChainOp {
                 W[e] = beta < P.nb ? __ldcg(&rb[beta]) : 0.f;
             }
             uint32_t w[4];
-            philox_group(w, key, STREAM_FB_BLOCK, 0, pos, static_cast<uint32_t>(g));
+            philox_group(w, key, STREAM_FB_BLOCK, 0, static_cast<uint32_t>(g));
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 if (W[e] > 0.f) {
@@ -508,10 +535,9 @@ template <int DT> struct ChainOp {
             const int e = (i + lane) & (SUB - 1), o = SUB * lane + e;
             ws += resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((smask >> e) & 1u) ? P.invC * qs : qs);
         }
-        const uint32_t n = static_cast<uint32_t>(base / SUB + lane);
         uint32_t w[4];
-        philox_group(w, key, STREAM_FB_SUB, 0, pos, n >> 2);
-        float A = ws > 0.f ? arrival(expo(w[n & 3]), 1.f / ws) : INFINITY;
+        philox_group(w, key, STREAM_FB_SUB, 0, static_cast<uint32_t>(lane) >> 2);  // sub-block lane of the block
+        float A = ws > 0.f ? arrival(expo(word_of(w, lane & 3)), 1.f / ws) : INFINITY;
         int si = lane;
         warp_argmin(A, si);
         const int x = base + SUB * si + lane;
@@ -520,8 +546,8 @@ template <int DT> struct ChainOp {
         const float wx =
             x < P.V ? resid_mass_w(tb[o], db[o], Mt, it, Md, id, P.invT, ((wmask >> lane) & 1u) ? P.invC * qs : qs)
                     : 0.f;
-        philox_group(w, key, STREAM_FB_TOKEN, 0, pos, static_cast<uint32_t>(x) >> 2);
-        float Ax = wx > 0.f ? arrival(expo(w[x & 3]), 1.f / wx) : INFINITY;
+        philox_group(w, key, STREAM_FB_TOKEN, 0, static_cast<uint32_t>(lane) >> 2);  // id offset lane of the sub-block
+        float Ax = wx > 0.f ? arrival(expo(word_of(w, lane & 3)), 1.f / wx) : INFINITY;
         int xi = x;
         warp_argmin(Ax, xi);
         return xi;
@@ -681,6 +707,11 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 }
             }
         }
+        // The variates of the first round of residual trials (trial = warp;
+        // warp 0's are also the bonus draw's): inputs only, so they are drawn
+        // while the streaming grid drains.
+        DrawVariates dv0;
+        draw_variates(dv0, __ldg(&P.keys[b]), static_cast<uint32_t>(warp), nb, lane);
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
@@ -745,10 +776,9 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         if (k == g) {
             // Bonus: one draw from p_gamma (warp 0).
             if (warp == 0) {
-                const int beta = race_blocks_p(P, sm, b, k, Mt, key, 0u, static_cast<uint32_t>(g), lane);
+                const int beta = race_blocks_p(P, sm, b, k, Mt, key, 0u, lane, dv0);
                 load_block(P, tp, beta, tb, lane);
-                const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), key, STREAM_SUB, STREAM_TOKEN,
-                                              0u, static_cast<uint32_t>(g), lane);
+                const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), dv0, lane);
                 if (lane == 0) sm.result = x;
             }
             fin_sync<FWV>();
@@ -758,15 +788,16 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             const float Md = sm.M[g + 1 + k], Sd = sm.S[g + 1 + k];
             for (int round = 0; round < MAX_TRIALS / FWV; ++round) {
                 const uint32_t t = static_cast<uint32_t>(round * FWV + warp);
-                const int beta = race_blocks_p(P, sm, b, k, Mt, key, t, static_cast<uint32_t>(k), lane);
+                DrawVariates dv;
+                if (round == 0) dv = dv0;
+                else draw_variates(dv, key, t, nb, lane);
+                const int beta = race_blocks_p(P, sm, b, k, Mt, key, t, lane, dv);
                 load_block(P, tp, beta, tb, lane);
                 load_block(P, dp, beta, db, lane);
-                uint32_t aw = 0;
-                const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), key, STREAM_SUB, STREAM_TOKEN, t,
-                                              static_cast<uint32_t>(k), lane, STREAM_ACCEPT, &aw);
+                const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), dv, lane);
                 const float wq = (P.sag && sag_member(sm.sag_id[k], x, lane)) ? P.invC : 1.f;
                 if (lane == 0) {
-                    const float v = uniform24(aw);
+                    const float v = uniform24(dv.aw);
                     const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
                     const float q = __fmul_rn(expf((db[x - beta * G] - Md) * P.invT) / Sd, wq);
                     sm.trial_x[warp] = x;
@@ -788,7 +819,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 residual_pass(P, b, tp, dp, Mt, St, Md, Sd, sm, warp, lane, tb, k);
                 if (fallback) {
                     if (warp == 0) {
-                        const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(k), tb, db,
+                        const int x = race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, tb, db,
                                                  P.sag ? sm.sag_id[k] : nullptr, 1.f, lane);
                         if (lane == 0) sm.result = x;
                     }
@@ -1083,10 +1114,11 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
             if (kids == 0ull) {
                 // leaf: the bonus token from p_u (warp 0)
                 if (warp == 0) {
-                    const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, 0u, static_cast<uint32_t>(u), lane);
+                    DrawVariates dv;
+                    draw_variates(dv, key, 0u, nb, lane);
+                    const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, 0u, lane, dv);
                     Base::load_block(P, tp, beta, tb, lane);
-                    const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), key, STREAM_SUB,
-                                                        STREAM_TOKEN, 0u, static_cast<uint32_t>(u), lane);
+                    const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), dv, lane);
                     if (lane == 0) sm.result = x;
                 }
                 fin_sync<FWV>();
@@ -1139,14 +1171,14 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
             fin_sync<FWV>();
             for (int round = 0; round < MAX_TRIALS / FWV; ++round) {
                 const uint32_t t = static_cast<uint32_t>(round * FWV + warp);
-                const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, t, static_cast<uint32_t>(u), lane);
+                DrawVariates dv;
+                draw_variates(dv, key, t, nb, lane);
+                const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, t, lane, dv);
                 Base::load_block(P, tp, beta, tb, lane);
                 Base::load_block(P, dp, beta, db, lane);
-                uint32_t aw = 0;
-                const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), key, STREAM_SUB,
-                                                    STREAM_TOKEN, t, static_cast<uint32_t>(u), lane, STREAM_ACCEPT, &aw);
+                const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), dv, lane);
                 if (lane == 0) {
-                    const float v = uniform24(aw);
+                    const float v = uniform24(dv.aw);
                     const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
                     const float q = __fmul_rn(expf((db[x - beta * G] - Md) * P.invT) / Sd, sres);
                     sm.trial_x[warp] = x;
@@ -1172,8 +1204,7 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
                 }
                 if (warp == 0) {
                     const float *rb = P.resid + (static_cast<size_t>(b) * 2 + ((pass - 1) & 1)) * nb;
-                    const int x = Base::race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, static_cast<uint32_t>(u), tb, db,
-                                                   nullptr, sres, lane, rb);
+                    const int x = Base::race_resid(P, b, tp, dp, Mt, St, Md, Sd, key, tb, db, nullptr, sres, lane, rb);
                     if (lane == 0) sm.result = x;
                 }
                 fin_sync<FWV>();

@@ -746,7 +746,7 @@ template <int FW> struct FiltFin {
                 z += w;
                 if (w > 0.f) {
                     uint32_t wd[4];
-                    philox_group(wd, key, STREAM_FILTERED, 0u, static_cast<uint32_t>(k), static_cast<uint32_t>(id) >> 2);
+                    philox_group(wd, key, STREAM_FILTERED, 0u, static_cast<uint32_t>(id) >> 2);
                     const float A = arrival(expo(wd[id & 3]), 1.f / w);
                     if (A < best || (A == best && id < bid)) {
                         best = A;

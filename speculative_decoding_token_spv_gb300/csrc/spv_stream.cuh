@@ -361,14 +361,17 @@ __device__ __forceinline__ void philox4x32_10(uint32_t c[4], uint32_t k0, uint32
 }
 
 // The four words of draw group `grp` (draws 4*grp .. 4*grp+3) of one
-// stream: counter (grp, stream, trial, pos), key (low, high half of `key`).
+// stream: counter (grp, stream, trial, 0), key (low, high half of `key`).
+// The position a draw is made at is not part of the counter: a sequence
+// makes one draw, so its variates can be generated before the position (the
+// first rejection) is known.
 __device__ __forceinline__ void philox_group(uint32_t w[4], uint64_t key, uint32_t stream, uint32_t trial,
-                                             uint32_t pos, uint32_t grp)
+                                             uint32_t grp)
 {
     w[0] = grp;
     w[1] = stream;
     w[2] = trial;
-    w[3] = pos;
+    w[3] = 0u;
     philox4x32_10(w, static_cast<uint32_t>(key), static_cast<uint32_t>(key >> 32));
 }
 

@@ -37,12 +37,12 @@ MUTANTS = {
     "block_race_weight": ("arr[b] = Wb > 0 ? expo(key, s_block, trial, pos, (uint64_t)b) / Wb : INFINITY;",
                           "arr[b] = Wb > 0 ? expo(key, s_block, trial, pos, (uint64_t)b) * Wb : INFINITY;",
                           ["test_first_token_is_distributed_as_target", "test_bonus_is_distributed_as_last_target_row"]),
-    "sub_block_race_weight": ("arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)(s0 / SPVO_SUB)) / Ws : INFINITY;",
-                              "arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)(s0 / SPVO_SUB)) : INFINITY;",
+    "sub_block_race_weight": ("arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)j) / Ws : INFINITY;",
+                              "arr[j] = Ws > 0 ? expo(key, s_sub, trial, pos, (uint64_t)j) : INFINITY;",
                               ["test_first_token_is_distributed_as_target",
                                "test_bonus_is_distributed_as_last_target_row"]),
-    "token_race_weight": ("arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)x) / w[x] : INFINITY;",
-                          "arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)x) : INFINITY;",
+    "token_race_weight": ("arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)(x - s0)) / w[x] : INFINITY;",
+                          "arr[x - s0] = w[x] > 0 ? expo(key, s_tok, trial, pos, (uint64_t)(x - s0)) : INFINITY;",
                           ["test_first_token_is_distributed_as_target", "test_bonus_is_distributed_as_last_target_row"]),
     "philox_constant": ("uint64_t p0 = (uint64_t)0xD2511F53u * c0;", "uint64_t p0 = (uint64_t)0xD2511F55u * c0;",
                         ["test_philox_known_answer_vectors"]),
@@ -90,11 +90,10 @@ MUTANTS = {
     "tree_greedy_last_child": ("if (parent[c] == u && tok[c] == a) { next = c; break; }",
                                "if (parent[c] == u && tok[c] == a) { next = c; }",
                                ["test_tree_greedy_walk"]),
-    "tree_bonus_position": ("emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,\n"
-                            "                                  (uint32_t)u, &margin);",
-                            "emitted = race_sample(w, V, seq_key, SPVO_STREAM_BLOCK, SPVO_STREAM_SUB, SPVO_STREAM_TOKEN, 0,\n"
-                            "                                  (uint32_t)0, &margin);",
-                            ["test_tree_path_is_the_chain"]),
+    "tree_bonus_wrong_row": ("        if (nkids == 0) { /* leaf: the bonus token from p_u */\n",
+                             "        if (nkids == 0) { /* leaf: the bonus token from p_u */\n"
+                             "            for (int x = 0; x < V; ++x) w[x] = prob(tgt, x, T, Mt, St);\n",
+                             ["test_tree_path_is_the_chain"]),
     "tree_draw_ignores_shift": ("emitted = tree_trials(w, du, V, T, Md, Sd, s, seq_key,",
                                 "emitted = tree_trials(w, du, V, T, Md, Sd, 1.0, seq_key,",
                                 ["test_tree_first_token_is_exact"]),

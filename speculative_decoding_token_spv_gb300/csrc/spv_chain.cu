@@ -71,7 +71,8 @@ constexpr int FW = 16;            // widest chain finalize CTA (warps; one resid
 constexpr int STAT_CACHE = 4096;  // target-row block statistics staged in shared memory when they fit
 
 struct ChainSmem {
-    float2 st[STAT_CACHE];  // target rows: (block max, race factor 2^((M - m) c2) / S or -1 if empty)
+    float2 st[STAT_CACHE];  // target rows: (block max, S_beta), or the race factor 2^((M - m) c2) / S_beta
+                            // (-1 if empty) in place of S_beta when the merge staged factors (tree)
     float M[2 * 64 + 1];    // row max of the raw logits (chain: 2 gamma + 1 rows; tree: 2 N)
     float S[2 * 64 + 1];    // row sum exp((z - M)/T)
     int x[64];              // draft tokens (tree: node tokens)
@@ -141,6 +142,28 @@ struct DrawVariates {
     float es, ex;
     uint32_t aw;
 };
+
+// A warp's DrawVariates parked in shared memory, lane-major: the values of
+// lane l at [i * 32 + l].  Computing a round's variates before the
+// dependent-grid wait only helps if they stay computed: in registers the
+// compiler may recompute them where they are used.
+constexpr int DRAW_SLOT_FLOATS = 11 * 32;
+__device__ __forceinline__ void store_draw(float *slot, const DrawVariates &dv, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) slot[i * 32 + lane] = dv.eb[i >> 2][i & 3];
+    slot[8 * 32 + lane] = dv.es;
+    slot[9 * 32 + lane] = dv.ex;
+    slot[10 * 32 + lane] = __uint_as_float(dv.aw);
+}
+__device__ __forceinline__ void load_draw(DrawVariates &dv, const float *slot, int lane)
+{
+#pragma unroll
+    for (int i = 0; i < 8; ++i) dv.eb[i >> 2][i & 3] = slot[i * 32 + lane];
+    dv.es = slot[8 * 32 + lane];
+    dv.ex = slot[9 * 32 + lane];
+    dv.aw = __float_as_uint(slot[10 * 32 + lane]);
+}
 
 __device__ __forceinline__ void draw_variates(DrawVariates &dv, uint64_t key, uint32_t trial, int nb, int lane)
 {
@@ -223,8 +246,7 @@ template <int DT> struct ChainOp {
 #pragma unroll
         for (int a = 0; a < 4; ++a) mx[a] = __hmax2(mx[a], mx[a + 4]);
         mx[0] = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
-        float m = fmaxf(__low2float(mx[0]), __high2float(mx[0]));
-        m = warp_max(m);
+        const float m = warp_max_redux(fmaxf(__low2float(mx[0]), __high2float(mx[0])));
         const float mu = (m == -INFINITY) ? 0.f : m;
         const float mc = mu * P.c2;
         const float delta = fmaf(mu, P.c2, -mc);
@@ -249,17 +271,19 @@ template <int DT> struct ChainOp {
     }
 
     // Block statistics: m = max z (raw), s = sum exp((z - m) / T).
-    // The max runs as 8 independent chains and the sum as 4; each term is
+    // The max is a tree of three-input maxima and one warp redux (NaN
+    // ignored, like fmaxf: a NaN shows up in the sum); the sum runs as 4
+    // independent chains; each term is
     // ex2(z * c2 - mc) with mc = m * c2 rounded, one FFMA, and the rounding
     // of mc (delta = m * c2 - mc, exact by FMA) is removed from the sum once:
     // sum ex2((z - m) c2) = 2^-delta * sum ex2(z c2 - mc).
     __device__ static __forceinline__ void block(const Params &P, long long row, int beta, float v[32], int, int lane)
     {
-        float mx[8];
+        float t[10];
 #pragma unroll
-        for (int a = 0; a < 8; ++a) mx[a] = fmaxf(fmaxf(v[a], v[a + 8]), fmaxf(v[a + 16], v[a + 24]));
-        float m = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-        m = warp_max(m);
+        for (int a = 0; a < 10; ++a) t[a] = fmax3(v[3 * a], v[3 * a + 1], v[3 * a + 2]);
+        const float u = fmax3(fmax3(t[0], t[1], t[2]), fmax3(t[3], t[4], t[5]), fmax3(t[6], t[7], t[8]));
+        const float m = warp_max_redux(fmax3(u, t[9], fmaxf(v[30], v[31])));
         const float mu = (m == -INFINITY) ? 0.f : m;
         const float mc = mu * P.c2;
         const float delta = fmaf(mu, P.c2, -mc);
@@ -291,12 +315,13 @@ template <int DT> struct ChainOp {
     // Level 1 of a draw from softmax(row rho / T): the block with the
     // smallest E_beta / W_beta, W_beta = 2^((m_beta - M) c2) S_beta up to the
     // row normaliser, i.e. arrival E_beta * f_beta with the factor
-    // f_beta = 2^((M - m_beta) c2) / S_beta staged by the merge (computed here
-    // when the statistics were not staged).  The exponentials E_beta come from
-    // dv when it holds them (rows of up to PRE_BLOCKS blocks), else from
-    // Philox here.  Every lane gets the winner.
+    // f_beta = 2^((M - m_beta) c2) / S_beta, staged by the merge when
+    // `staged` (else computed here from the block statistics, in shared
+    // memory when they fit).  The exponentials E_beta come from dv when it
+    // holds them (rows of up to PRE_BLOCKS blocks), else from Philox here.
+    // Every lane gets the winner.
     __device__ static int race_blocks_p(const Params &P, const Smem &sm, int b, int rho, float M, uint64_t key,
-                                        uint32_t trial, int lane, const DrawVariates &dv)
+                                        uint32_t trial, int lane, const DrawVariates &dv, bool staged)
     {
         float best = INFINITY;
         int bi = INT_MAX;
@@ -308,7 +333,8 @@ template <int DT> struct ChainOp {
                 if (beta >= P.nb) {
                     f = -1.f;
                 } else if (sm.cached) {
-                    f = sm.st[rho * P.nb + beta].y;
+                    const float2 st = sm.st[rho * P.nb + beta];
+                    f = staged ? st.y : (st.y > 0.f ? __fdividef(fast_exp2((M - st.x) * P.c2), st.y) : -1.f);
                 } else {
                     const float2 st = __ldcg(&P.stats[(static_cast<long long>(b) * P.R + rho) * P.nb + beta]);
                     f = st.y > 0.f ? fast_exp2((M - st.x) * P.c2) / st.y : -1.f;
@@ -322,7 +348,34 @@ template <int DT> struct ChainOp {
                 }
             }
         };
-        if (P.nb <= PRE_BLOCKS) {
+        if (P.nb <= PRE_BLOCKS && sm.cached && !staged) {
+            // the lane's eight blocks 4 lane + 128 h + e as independent
+            // arrivals (loads, exponentials and divisions all in flight),
+            // then a pairwise minimum in index order (ties to the lower one)
+            float A[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int beta = 4 * lane + 128 * (j >> 2) + (j & 3);
+                A[j] = INFINITY;
+                if (beta < P.nb) {
+                    const float2 st = sm.st[rho * P.nb + beta];
+                    if (st.y > 0.f) A[j] = arrival(dv.eb[j >> 2][j & 3], __fdividef(fast_exp2((M - st.x) * P.c2), st.y));
+                }
+            }
+            int I[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) I[j] = 4 * lane + 128 * (j >> 2) + (j & 3);
+#pragma unroll
+            for (int w = 1; w < 8; w *= 2)
+#pragma unroll
+                for (int j = 0; j + w < 8; j += 2 * w)
+                    if (A[j + w] < A[j]) {
+                        A[j] = A[j + w];
+                        I[j] = I[j + w];
+                    }
+            best = A[0];
+            bi = best == INFINITY ? INT_MAX : I[0];
+        } else if (P.nb <= PRE_BLOCKS) {
             if (4 * lane < P.nb) visit(lane, dv.eb[0]);
             if (4 * (lane + 32) < P.nb) visit(lane + 32, dv.eb[1]);
         } else {
@@ -387,16 +440,19 @@ template <int DT> struct ChainOp {
                                           const DrawVariates &dv, int lane)
     {
         const int base = beta * G;
-        // sub-block mass relative to the block max (skewed reads: no bank conflicts)
-        float ws = 0.f;
+        // sub-block mass relative to the block max (skewed reads: no bank
+        // conflicts), four partial sums in flight
+        float w4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 8
-        for (int i = 0; i < SUB; ++i) ws += fast_exp2((buf[SUB * lane + ((i + lane) & (SUB - 1))] - mb) * P.c2);
+        for (int i = 0; i < SUB; ++i)
+            w4[i & 3] += fast_exp2((buf[SUB * lane + ((i + lane) & (SUB - 1))] - mb) * P.c2);
+        const float ws = (w4[0] + w4[1]) + (w4[2] + w4[3]);
         float A = ws > 0.f ? arrival(dv.es, 1.f / ws) : INFINITY;
         int si = lane;
         warp_argmin(A, si);
         const int x = base + SUB * si + lane;
         const float z = buf[SUB * si + lane];
-        const float msw = warp_max(z);  // max of the winning sub-block
+        const float msw = warp_max_redux(z);  // max of the winning sub-block
         float Ax = (x < P.V && z != -INFINITY) ? arrival(dv.ex, fast_exp2((msw - z) * P.c2)) : INFINITY;
         int xi = x;
         warp_argmin(Ax, xi);
@@ -406,9 +462,9 @@ template <int DT> struct ChainOp {
     // Row statistics of sequence b from its block statistics: one half-warp
     // per row, all rows at once, up to 16 loads per lane in flight together:
     // sm.M / sm.S = row max / sum exp((z - max) / T).  Target rows rho <
-    // ncache keep (m_beta, race factor) in sm.st for the draws (when they
-    // fit); with FACTORS their race factors replace S_beta there (else
-    // stage_factors does that once the row statistics are visible).  A bad
+    // ncache keep (m_beta, S_beta) in sm.st for the draws (when they fit);
+    // with FACTORS their race factors replace S_beta there (else the draws
+    // compute the factors from (m_beta, S_beta) themselves).  A bad
     // row (NaN / +inf, no finite logit) gets S = NaN; with flag_all it also
     // sets sm.bad.  FWV warps.
     template <int FWV, bool FACTORS>
@@ -440,10 +496,13 @@ template <int DT> struct ChainOp {
                 }
                 const float nm = fmaxf(m, cm);
                 if (nm != -INFINITY) {
-                    float acc = s > 0.f ? s * expf((m - nm) * P.invT) : 0.f;
+                    // ex2.approx of arguments <= 0 (relative error ~2e-7 for the
+                    // blocks near the row max, which carry the sum); a compact
+                    // instruction stream matters more here than expf's last bit
+                    float acc = s > 0.f ? s * fast_exp2((m - nm) * P.c2) : 0.f;
 #pragma unroll
                     for (int u = 0; u < 16; ++u)
-                        if (v[u].y > 0.f) acc += v[u].y * expf((v[u].x - nm) * P.invT);
+                        if (v[u].y > 0.f) acc = fmaf(v[u].y, fast_exp2((v[u].x - nm) * P.c2), acc);
                     s = acc;
                     m = nm;
                 }
@@ -451,7 +510,7 @@ template <int DT> struct ChainOp {
             float mw = m;
 #pragma unroll
             for (int o = 8; o; o >>= 1) mw = fmaxf(mw, __shfl_xor_sync(0xffffffffu, mw, o));
-            s = (s > 0.f) ? s * expf((m - mw) * P.invT) : 0.f;
+            s = (s > 0.f) ? s * fast_exp2((m - mw) * P.c2) : 0.f;
 #pragma unroll
             for (int o = 8; o; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
             const unsigned badm = __ballot_sync(0xffffffffu, bad);
@@ -468,21 +527,6 @@ template <int DT> struct ChainOp {
                     sm.st[rho * nb + beta].y = v.y > 0.f ? fast_exp2((mw - v.x) * P.c2) / v.y : -1.f;
                 }
             }
-        }
-    }
-
-    // Race factors 2^((M - m_beta) c2) / S_beta (-1 for an empty block) of the
-    // staged target rows rho < nrows, in place of S_beta in sm.st (all
-    // threads; rows with no mass are left alone).  Needs sm.M / sm.S.
-    template <int FWV> __device__ static void stage_factors(const Params &P, Smem &sm, int nrows)
-    {
-        if (!sm.cached) return;
-        const int nb = P.nb;
-        for (int i = threadIdx.x; i < nrows * nb; i += FWV * 32) {
-            const int rho = i / nb;
-            if (!(sm.S[rho] > 0.f)) continue;
-            const float2 v = sm.st[i];
-            sm.st[i].y = v.y > 0.f ? fast_exp2((sm.M[rho] - v.x) * P.c2) / v.y : -1.f;
         }
     }
 
@@ -626,7 +670,9 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
     }
 
     static constexpr int FIN_WARPS = FWV;
-    static constexpr int FIN_BUF_FLOATS = 2 * FWV * G;  // per warp: one target and one draft block
+    static constexpr bool PRE_DRAW = FWV >= 16;  // first round's variates drawn before the wait
+    // per warp: one target and one draft block (and its parked variates)
+    static constexpr int FIN_BUF_FLOATS = 2 * FWV * G + (PRE_DRAW ? FWV * DRAW_SLOT_FLOATS : 0);
 
     // Outputs of a bad row: -1 ids and count, NaN p / q / Z, status (bad row,
     // or timeout when a bounded wait of the streaming pass gave up), cache miss.
@@ -708,10 +754,16 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             }
         }
         // The variates of the first round of residual trials (trial = warp;
-        // warp 0's are also the bonus draw's): inputs only, so they are drawn
-        // while the streaming grid drains.
-        DrawVariates dv0;
-        draw_variates(dv0, __ldg(&P.keys[b]), static_cast<uint32_t>(warp), nb, lane);
+        // warp 0's are also the bonus draw's) depend on inputs only: the wide
+        // CTA draws them while the streaming grid drains and parks them in
+        // shared memory (the narrow one, two CTAs per SM, has no room: it
+        // draws them where they are used).
+        float *slot = buf + 2 * FWV * G + warp * DRAW_SLOT_FLOATS;
+        if constexpr (PRE_DRAW) {
+            DrawVariates dv;
+            draw_variates(dv, __ldg(&P.keys[b]), static_cast<uint32_t>(warp), nb, lane);
+            store_draw(slot, dv, lane);
+        }
         asm volatile("griddepcontrol.wait;" ::: "memory");
         fin_sync<FWV>();
         if (warp == 0 && lane < g && (sm.x[lane] < 0 || sm.x[lane] >= P.V)) atomicOr(&sm.bad, 1);
@@ -723,9 +775,6 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             write_bad_row(P, b, warp, lane, (sm.bad & 2) ? STATUS_TIMEOUT : STATUS_BAD_ROW);
             return;
         }
-        // Race factors of the target rows (read by the draws after the
-        // barrier that follows the accept tests).
-        Base::template stage_factors<FWV>(P, sm, g + 1);
         if (P.sag) {
             // Saguaro: q_C's normaliser S - (1 - 1/C) * sum over the cached ids (at least S / C)
 #pragma unroll
@@ -776,7 +825,10 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
         if (k == g) {
             // Bonus: one draw from p_gamma (warp 0).
             if (warp == 0) {
-                const int beta = race_blocks_p(P, sm, b, k, Mt, key, 0u, lane, dv0);
+                DrawVariates dv0;
+                if constexpr (PRE_DRAW) load_draw(dv0, slot, lane);
+                else draw_variates(dv0, key, 0u, nb, lane);
+                const int beta = race_blocks_p(P, sm, b, k, Mt, key, 0u, lane, dv0, false);
                 load_block(P, tp, beta, tb, lane);
                 const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), dv0, lane);
                 if (lane == 0) sm.result = x;
@@ -789,9 +841,9 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             for (int round = 0; round < MAX_TRIALS / FWV; ++round) {
                 const uint32_t t = static_cast<uint32_t>(round * FWV + warp);
                 DrawVariates dv;
-                if (round == 0) dv = dv0;
+                if (PRE_DRAW && round == 0) load_draw(dv, slot, lane);
                 else draw_variates(dv, key, t, nb, lane);
-                const int beta = race_blocks_p(P, sm, b, k, Mt, key, t, lane, dv);
+                const int beta = race_blocks_p(P, sm, b, k, Mt, key, t, lane, dv, false);
                 load_block(P, tp, beta, tb, lane);
                 load_block(P, dp, beta, db, lane);
                 const int x = race_in_block_p(P, tb, beta, block_max(P, sm, b, k, beta), dv, lane);
@@ -1116,7 +1168,7 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
                 if (warp == 0) {
                     DrawVariates dv;
                     draw_variates(dv, key, 0u, nb, lane);
-                    const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, 0u, lane, dv);
+                    const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, 0u, lane, dv, true);
                     Base::load_block(P, tp, beta, tb, lane);
                     const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), dv, lane);
                     if (lane == 0) sm.result = x;
@@ -1173,7 +1225,7 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
                 const uint32_t t = static_cast<uint32_t>(round * FWV + warp);
                 DrawVariates dv;
                 draw_variates(dv, key, t, nb, lane);
-                const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, t, lane, dv);
+                const int beta = Base::race_blocks_p(P, sm, b, u, Mt, key, t, lane, dv, true);
                 Base::load_block(P, tp, beta, tb, lane);
                 Base::load_block(P, dp, beta, db, lane);
                 const int x = Base::race_in_block_p(P, tb, beta, Base::block_max(P, sm, b, u, beta), dv, lane);
@@ -1311,7 +1363,7 @@ template <int DT> struct GreedyOp {
         mx[0] = __hmax2_nan(__hmax2_nan(mx[0], mx[1]), __hmax2_nan(mx[2], mx[3]));
         const float lo = __low2float(mx[0]), hi = __high2float(mx[0]);
         const bool nan = __any_sync(0xffffffffu, isnan(lo) || isnan(hi));
-        const float m = warp_max(fmaxf(lo, hi));
+        const float m = warp_max_redux(fmaxf(lo, hi));
         int i = INT_MAX;
         if (!nan && m != -INFINITY && m != INFINITY) {
             const __nv_bfloat162 mm = __float2bfloat162_rn(m);  // exact: m is one of the bf16 values

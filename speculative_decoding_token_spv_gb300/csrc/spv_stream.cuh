@@ -297,6 +297,23 @@ __device__ __forceinline__ float warp_max(float v)
     return v;
 }
 
+// Warp max in one instruction (redux.sync, sm_100 and later): NaN inputs are
+// ignored like fmaxf; every lane gets the result.
+__device__ __forceinline__ float warp_max_redux(float v)
+{
+    float r;
+    asm("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+// Max of three in one instruction (sm_100 and later); NaN ignored like fmaxf.
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float warp_sum(float v)
 {
 #pragma unroll
@@ -394,18 +411,16 @@ __device__ __forceinline__ float arrival(float E, float f)
     return E == 0.f ? 0.f : E * f;
 }
 
-// argmin of (arrival, index) across the warp, ties to the lower index.
+// argmin of (arrival, index) across the warp, ties to the lower index, for
+// arrivals >= 0 or +inf (never NaN): their bit patterns order like their
+// values, so two single-instruction reductions replace a shuffle tree (the
+// draws run on one warp, where every step of a dependent chain counts).
 __device__ __forceinline__ void warp_argmin(float &a, int &i)
 {
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        const float a2 = __shfl_xor_sync(0xffffffffu, a, o);
-        const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-        if (a2 < a || (a2 == a && i2 < i)) {
-            a = a2;
-            i = i2;
-        }
-    }
+    const unsigned ab = __float_as_uint(a) & 0x7fffffffu;  // -0.0 ranks as +0.0
+    const unsigned mn = __reduce_min_sync(0xffffffffu, ab);
+    i = static_cast<int>(__reduce_min_sync(0xffffffffu, ab == mn ? static_cast<unsigned>(i) : 0xffffffffu));
+    a = __uint_as_float(mn);
 }
 
 // ------------------------------------------------------------------ block loads

@@ -81,8 +81,8 @@ struct ChainSmem {
     int bad;
     int k;
     int cached;
-    int trial_x[FW];
-    int trial_acc[FW];
+    int trial_x[2][FW];     // trial outcomes of a round (two buffers: rounds alternate)
+    int trial_acc[2][FW];
     int result;
     int gflag;              // tree: outcome of the last barrier of the sequence's CTAs
     float Z;
@@ -486,24 +486,27 @@ template <int DT> struct ChainOp {
                     const int beta = base + 16 * u + hl;
                     v[u] = (active && beta < nb) ? __ldcg(&st[beta]) : make_float2(-INFINITY, 0.f);
                 }
-                float cm = -INFINITY;
 #pragma unroll
                 for (int u = 0; u < 16; ++u) {
                     const int beta = base + 16 * u + hl;
-                    if (isnan(v[u].x)) bad = true;
-                    else cm = fmaxf(cm, v[u].x);
+                    bad |= isnan(v[u].x);
                     if (keep && beta < nb) sm.st[rho * nb + beta] = v[u];
                 }
-                const float nm = fmaxf(m, cm);
+                // the max as a tree of three-input maxima (NaN ignored, like
+                // fmaxf), the sum as four partial sums: short dependent chains
+                float t6[6];
+#pragma unroll
+                for (int j = 0; j < 5; ++j) t6[j] = fmax3(v[3 * j].x, v[3 * j + 1].x, v[3 * j + 2].x);
+                t6[5] = fmaxf(v[15].x, m);
+                const float nm = fmax3(fmax3(t6[0], t6[1], t6[2]), fmax3(t6[3], t6[4], t6[5]), -INFINITY);
                 if (nm != -INFINITY) {
                     // ex2.approx of arguments <= 0 (relative error ~2e-7 for the
-                    // blocks near the row max, which carry the sum); a compact
-                    // instruction stream matters more here than expf's last bit
-                    float acc = s > 0.f ? s * fast_exp2((m - nm) * P.c2) : 0.f;
+                    // blocks near the row max, which carry the sum)
+                    float acc[4] = {s > 0.f ? s * fast_exp2((m - nm) * P.c2) : 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int u = 0; u < 16; ++u)
-                        if (v[u].y > 0.f) acc = fmaf(v[u].y, fast_exp2((v[u].x - nm) * P.c2), acc);
-                    s = acc;
+                        if (v[u].y > 0.f) acc[u & 3] = fmaf(v[u].y, fast_exp2((v[u].x - nm) * P.c2), acc[u & 3]);
+                    s = (acc[0] + acc[1]) + (acc[2] + acc[3]);
                     m = nm;
                 }
             }
@@ -792,8 +795,12 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             }
             fin_sync<FWV>();
         }
-        // C. Accept tests for every draft position; first rejection by ballot.
-        if (warp == 0) {
+        // C. Accept tests for every draft position and the first rejection by
+        //    ballot, in every warp (the same values from shared memory give
+        //    every warp the same k: no barrier between the tests and the
+        //    draws); warp 0 writes p and q.
+        int k;
+        {
             bool acc = false;
             if (lane < g) {
                 const float p = expf((sm.zt[lane] - sm.M[lane]) * P.invT) / sm.S[lane];
@@ -804,23 +811,19 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                     if (in) q = __fmul_rn(q, P.invC);
                 }
                 acc = (p > 0.f) && (sm.rr[lane] * q <= p);
-                if (P.out_pq) {
+                if (warp == 0 && P.out_pq) {
                     P.out_pq[(static_cast<size_t>(b) * g + lane) * 2] = p;
                     P.out_pq[(static_cast<size_t>(b) * g + lane) * 2 + 1] = q;
                 }
             }
             const unsigned mask = __ballot_sync(0xffffffffu, acc);
             const unsigned all = (g == 32) ? 0xffffffffu : ((1u << g) - 1u);
-            if (lane == 0) {
-                sm.k = ((mask & all) == all) ? g : (__ffs(~mask) - 1);
-                sm.result = -1;
-            }
+            k = ((mask & all) == all) ? g : (__ffs(~mask) - 1);
         }
-        fin_sync<FWV>();
-        const int k = sm.k;
         const uint64_t key = sm.key;
         const unsigned char *tp = row_of(P, b, k);
         const float Mt = sm.M[k], St = sm.S[k];
+        int res = -1;
         // D. The emitted token.
         if (k == g) {
             // Bonus: one draw from p_gamma (warp 0).
@@ -834,12 +837,17 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                 if (lane == 0) sm.result = x;
             }
             fin_sync<FWV>();
+            res = sm.result;
         } else {
-            // Residual: rejection trials from p_k, FWV at a time (one per warp).
+            // Residual: rejection trials from p_k, FWV at a time (one per warp);
+            // every thread reads the round's outcomes after one barrier (the
+            // rounds alternate between two buffers, so the next round's
+            // writes cannot meet a slower warp's reads).
             const unsigned char *dp = row_of(P, b, g + 1 + k);
             const float Md = sm.M[g + 1 + k], Sd = sm.S[g + 1 + k];
             for (int round = 0; round < MAX_TRIALS / FWV; ++round) {
                 const uint32_t t = static_cast<uint32_t>(round * FWV + warp);
+                const int buf2 = round & 1;
                 DrawVariates dv;
                 if (PRE_DRAW && round == 0) load_draw(dv, slot, lane);
                 else draw_variates(dv, key, t, nb, lane);
@@ -852,21 +860,18 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                     const float v = uniform24(dv.aw);
                     const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
                     const float q = __fmul_rn(expf((db[x - beta * G] - Md) * P.invT) / Sd, wq);
-                    sm.trial_x[warp] = x;
-                    sm.trial_acc[warp] = (q <= (1.0f - v) * p) ? 1 : 0;
+                    sm.trial_x[buf2][warp] = x;
+                    sm.trial_acc[buf2][warp] = (q <= (1.0f - v) * p) ? 1 : 0;
                 }
                 fin_sync<FWV>();
-                if (threadIdx.x == 0) {
-                    for (int w = 0; w < FWV; ++w)
-                        if (sm.trial_acc[w]) {
-                            sm.result = sm.trial_x[w];
-                            break;
-                        }
-                }
-                fin_sync<FWV>();
-                if (sm.result >= 0) break;
+                for (int w = 0; w < FWV; ++w)
+                    if (sm.trial_acc[buf2][w]) {
+                        res = sm.trial_x[buf2][w];
+                        break;
+                    }
+                if (res >= 0) break;
             }
-            const bool fallback = sm.result < 0;
+            const bool fallback = res < 0;
             if (fallback || P.out_Z) {
                 residual_pass(P, b, tp, dp, Mt, St, Md, Sd, sm, warp, lane, tb, k);
                 if (fallback) {
@@ -876,12 +881,12 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
                         if (lane == 0) sm.result = x;
                     }
                     fin_sync<FWV>();
+                    res = sm.result;
                 }
             }
         }
         // E. Outputs.  No residual mass at all (a draft token outside q's
         //    support with p = q elsewhere) leaves nothing to draw: bad row.
-        const int res = sm.result;
         if (res < 0) {
             write_bad_row(P, b, warp, lane);
             return;
@@ -1233,14 +1238,14 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
                     const float v = uniform24(dv.aw);
                     const float p = expf((tb[x - beta * G] - Mt) * P.invT) / St;
                     const float q = __fmul_rn(expf((db[x - beta * G] - Md) * P.invT) / Sd, sres);
-                    sm.trial_x[warp] = x;
-                    sm.trial_acc[warp] = (q <= (1.0f - v) * p) ? 1 : 0;
+                    sm.trial_x[0][warp] = x;
+                    sm.trial_acc[0][warp] = (q <= (1.0f - v) * p) ? 1 : 0;
                 }
                 fin_sync<FWV>();
                 if (threadIdx.x == 0) {
                     for (int w = 0; w < FWV; ++w)
-                        if (sm.trial_acc[w]) {
-                            sm.result = sm.trial_x[w];
+                        if (sm.trial_acc[0][w]) {
+                            sm.result = sm.trial_x[0][w];
                             break;
                         }
                 }

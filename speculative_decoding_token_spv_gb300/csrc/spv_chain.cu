@@ -922,6 +922,12 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
 // leaf (a node no other node hangs from) is neither loaded nor reduced.
 template <int DT> struct TreeOp : ChainOp<DT> {
     static constexpr bool SKIPS = true;
+    // bf16: items of 16 blocks (32 KB) on two CTAs per SM.  Measured against
+    // 8-block items on four (same-box A/B, B = 64): k21 tree 183 -> 170 us,
+    // w4 160 -> 148 us, 63-node tree 445 -> 396 us; the chain and greedy
+    // streams keep 8-block items (both slower with 16).
+    static constexpr int CTAS_PER_SM = 2;
+    static constexpr int ITEM_BLOCKS = DT == 0 ? 8 : 16;
 
     // Draft rows: lane v holds the parents of nodes v and v + 32 (16 bits
     // each, 0xffff for none or the root).  Target rows: no load.

@@ -107,12 +107,13 @@ template <> struct DType<1> {  // bf16
     }
 };
 
-// Ring stages of one CTA when `ctas` CTAs share an SM (at least 2).
-template <int DT> constexpr int stages(int ctas)
+// Ring stages of one CTA when `ctas` CTAs share an SM (at least 2), for work
+// items of `chunk` logits.
+template <int DT> constexpr int stages(int ctas, int chunk = CHUNK)
 {
-    return RING_BYTES_PER_SM / ctas / (CHUNK * DType<DT>::BYTES) < 2
+    return RING_BYTES_PER_SM / ctas / (chunk * DType<DT>::BYTES) < 2
                ? 2
-               : RING_BYTES_PER_SM / ctas / (CHUNK * DType<DT>::BYTES);
+               : RING_BYTES_PER_SM / ctas / (chunk * DType<DT>::BYTES);
 }
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -553,6 +554,16 @@ template <class Op> struct OpWaitsPrior<Op, std::void_t<decltype(Op::WAITS_PRIOR
     static constexpr bool value = Op::WAITS_PRIOR;
 };
 
+// Sampler blocks per work item (Op::ITEM_BLOCKS, a multiple of the consumer
+// warps, else CHUNK_BLOCKS): each consumer warp reduces ITEM_BLOCKS / NCW
+// blocks of a staged item.
+template <class Op, class = void> struct OpItemBlocks {
+    static constexpr int value = CHUNK_BLOCKS;
+};
+template <class Op> struct OpItemBlocks<Op, std::void_t<decltype(Op::ITEM_BLOCKS)>> {
+    static constexpr int value = Op::ITEM_BLOCKS;
+};
+
 template <class Op, class = void> struct OpSkips {
     static constexpr bool value = false;
 };
@@ -564,8 +575,11 @@ template <class Op, int DT, bool TMA>
 __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const typename Op::Params P)
 {
     constexpr int EB = DType<DT>::BYTES;
-    constexpr int S = stages<DT>(Op::CTAS_PER_SM);
-    constexpr int CHUNK_BYTES = CHUNK * EB;
+    constexpr int CB = OpItemBlocks<Op>::value;  // blocks per work item
+    static_assert(CB % NCW == 0, "work items hold a whole number of blocks per consumer warp");
+    constexpr int CH = G * CB;                   // logits per work item
+    constexpr int S = stages<DT>(Op::CTAS_PER_SM, CH);
+    constexpr int CHUNK_BYTES = CH * EB;
     extern __shared__ __align__(128) unsigned char ring[];
     __shared__ __align__(8) uint64_t full_bar[S];
     __shared__ __align__(8) uint64_t empty_bar[S];
@@ -619,7 +633,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                             stop = 1;
                         } else {
                             const int c = pos.c;
-                            const int n = min(CHUNK, P.V - c * CHUNK);
+                            const int n = min(CH, P.V - c * CH);
                             const unsigned char *src = reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) +
                                                        static_cast<size_t>(c) * CHUNK_BYTES;
                             mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(n * EB));
@@ -668,7 +682,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                 const int c = static_cast<int>(it - row * nc);
                 stage_row[s] = row;
                 stage_c[s] = c;
-                const int n = min(CHUNK, P.V - c * CHUNK);
+                const int n = min(CH, P.V - c * CH);
                 const unsigned char *src =
                     reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) + static_cast<size_t>(c) * CHUNK_BYTES;
                 mbar_arrive_expect_tx(&full_bar[s], static_cast<uint32_t>(n * EB));
@@ -707,10 +721,13 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
             }
             const long long row = stage_row[stage];
             if (row < 0) break;  // no more items (the end mark holds no copy to release)
-            const int beta = stage_c[stage] * CHUNK_BLOCKS + warp;
-            if (beta < P.nb)
-                Op::block_smem(P, row, beta, ring + stage * CHUNK_BYTES + warp * G * EB, min(G, P.V - beta * G),
-                               lane);
+#pragma unroll
+            for (int q = warp; q < CB; q += NCW) {
+                const int beta = stage_c[stage] * CB + q;
+                if (beta < P.nb)
+                    Op::block_smem(P, row, beta, ring + stage * CHUNK_BYTES + q * G * EB, min(G, P.V - beta * G),
+                                   lane);
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty_bar[stage]);
             // A timed-out wait anywhere stops every consumer warp together.
@@ -746,17 +763,20 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
         }
         const long long row = pos.row;
         const int c = pos.c;
-        const int beta = c * CHUNK_BLOCKS + warp;
-        if (ok && beta < P.nb) {
-            const int valid = min(G, P.V - beta * G);
-            if (TMA) {
-                Op::block_smem(P, row, beta, ring + s * CHUNK_BYTES + warp * G * EB, valid, lane);
-            } else {
-                float v[32];
-                const unsigned char *blk = reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) +
-                                           static_cast<size_t>(beta) * G * EB;
-                load_block_global<DT>(v, blk, lane, valid);
-                Op::block(P, row, beta, v, valid, lane);
+#pragma unroll
+        for (int q = warp; q < CB; q += NCW) {
+            const int beta = c * CB + q;
+            if (ok && beta < P.nb) {
+                const int valid = min(G, P.V - beta * G);
+                if (TMA) {
+                    Op::block_smem(P, row, beta, ring + s * CHUNK_BYTES + q * G * EB, valid, lane);
+                } else {
+                    float v[32];
+                    const unsigned char *blk = reinterpret_cast<const unsigned char *>(Op::row_ptr(P, row)) +
+                                               static_cast<size_t>(beta) * G * EB;
+                    load_block_global<DT>(v, blk, lane, valid);
+                    Op::block(P, row, beta, v, valid, lane);
+                }
             }
         }
         if (TMA) {
@@ -810,12 +830,18 @@ static inline cudaError_t device_sm_count(int *out)
 // by the item count) and then the finalize grid of Fin, `groups` CTAs, as a
 // programmatic dependent launch on the same stream.
 template <class Op, class Fin, int DT>
-static cudaError_t launch_stream_finalize(const typename Op::Params &P, bool tma, int groups, cudaStream_t st,
+static cudaError_t launch_stream_finalize(const typename Op::Params &P0, bool tma, int groups, cudaStream_t st,
                                           int cluster = 1)
 {
     constexpr bool PRIOR = OpWaitsPrior<Op>::value;
+    constexpr int CH = G * OpItemBlocks<Op>::value;
+    // Work items of this op: P0 counts them in items of CHUNK logits.
+    typename Op::Params P = P0;
+    const long long rows = P0.total_items / P0.nc;
+    P.nc = (P0.V + CH - 1) / CH;
+    P.total_items = rows * P.nc;
     void (*kern)(const typename Op::Params) = tma ? stream_kernel<Op, DT, true> : stream_kernel<Op, DT, false>;
-    const int smem = tma ? stages<DT>(Op::CTAS_PER_SM) * CHUNK * DType<DT>::BYTES : 0;
+    const int smem = tma ? stages<DT>(Op::CTAS_PER_SM, CH) * CH * DType<DT>::BYTES : 0;
     // Per device and kernel variant: the shared-memory attributes and the
     // resident CTA count are set / queried once (the function-local static
     // is per template instantiation; the TMA / plain-load variant is chosen

@@ -136,7 +136,7 @@ __device__ __forceinline__ uint32_t word_of(const uint32_t w[4], int j)
 // and the trial's acceptance word.  None depends on the row, the position or
 // the statistics, so a finalize computes the first round's before its
 // dependent-grid wait.
-constexpr int PRE_BLOCKS = 256;
+constexpr int PRE_BLOCKS = 160;  // 40 Philox groups: every lane's first, lanes 0..7's second
 struct DrawVariates {
     float eb[2][4];
     float es, ex;
@@ -165,27 +165,46 @@ __device__ __forceinline__ void load_draw(DrawVariates &dv, const float *slot, i
     dv.aw = __float_as_uint(slot[10 * 32 + lane]);
 }
 
+// At most two Philox calls per lane: every lane its block group (lane), then
+// lanes 0..7 block group lane + 32, lanes 8..15 sub-block group lane - 8,
+// lanes 16..23 id group lane - 16, lane 24 the acceptance group; the
+// sub-block, id and acceptance words then reach their lanes by shuffles.
 __device__ __forceinline__ void draw_variates(DrawVariates &dv, uint64_t key, uint32_t trial, int nb, int lane)
 {
-    uint32_t w[4];
+    const bool pre = nb <= PRE_BLOCKS;
+    uint32_t w[4] = {0u, 0u, 0u, 0u};
+    if (pre && 4 * lane < nb) philox_group(w, key, STREAM_BLOCK, trial, static_cast<uint32_t>(lane));
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int g = lane + 32 * h;
-        if (nb <= PRE_BLOCKS && 4 * g < nb) {
-            philox_group(w, key, STREAM_BLOCK, trial, static_cast<uint32_t>(g));
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dv.eb[h][e] = expo(w[e]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) dv.eb[h][e] = 0.f;
-        }
+    for (int e = 0; e < 4; ++e) dv.eb[0][e] = expo(w[e]);
+    uint32_t stream = STREAM_ACCEPT, grp = 0u;
+    bool run = true;
+    if (lane < 8) {
+        stream = STREAM_BLOCK;
+        grp = static_cast<uint32_t>(lane + 32);
+        run = pre && 4 * (lane + 32) < nb;
+    } else if (lane < 16) {
+        stream = STREAM_SUB;
+        grp = static_cast<uint32_t>(lane - 8);
+    } else if (lane < 24) {
+        stream = STREAM_TOKEN;
+        grp = static_cast<uint32_t>(lane - 16);
+    } else {
+        run = lane == 24;
     }
-    philox_group(w, key, STREAM_SUB, trial, static_cast<uint32_t>(lane) >> 2);
-    dv.es = expo(word_of(w, lane & 3));
-    philox_group(w, key, STREAM_TOKEN, trial, static_cast<uint32_t>(lane) >> 2);
-    dv.ex = expo(word_of(w, lane & 3));
-    philox_group(w, key, STREAM_ACCEPT, trial, 0u);
-    dv.aw = w[0];
+    uint32_t v[4] = {0u, 0u, 0u, 0u};
+    if (run) philox_group(v, key, stream, trial, grp);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dv.eb[1][e] = expo(v[e]);
+    const int ss = 8 + (lane >> 2), st = 16 + (lane >> 2);  // lanes holding this lane's sub-block / id group
+    uint32_t ws[4], wt[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        ws[e] = __shfl_sync(0xffffffffu, v[e], ss);
+        wt[e] = __shfl_sync(0xffffffffu, v[e], st);
+    }
+    dv.es = expo(word_of(ws, lane & 3));
+    dv.ex = expo(word_of(wt, lane & 3));
+    dv.aw = __shfl_sync(0xffffffffu, v[0], 24);
 }
 
 template <int DT> struct ChainOp {

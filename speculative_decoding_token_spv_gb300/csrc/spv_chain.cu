@@ -623,7 +623,7 @@ template <int DT> struct ChainOp {
 
 // The chain finalize at a given width: FWV warps, FWV residual trials per
 // round.  Wider CTAs draw in fewer rounds; narrower ones fit two per SM.
-template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
+template <int DT, int FWV, bool PRE = (FWV >= 16)> struct ChainFin : ChainOp<DT> {
     using Base = ChainOp<DT>;
     using Params = ChainParams;
     using Smem = ChainSmem;
@@ -692,7 +692,7 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
     }
 
     static constexpr int FIN_WARPS = FWV;
-    static constexpr bool PRE_DRAW = FWV >= 16;  // first round's variates drawn before the wait
+    static constexpr bool PRE_DRAW = PRE;  // first round's variates drawn before the wait
     // per warp: one target and one draft block (and its parked variates)
     static constexpr int FIN_BUF_FLOATS = 2 * FWV * G + (PRE_DRAW ? FWV * DRAW_SLOT_FLOATS : 0);
 
@@ -776,9 +776,9 @@ template <int DT, int FWV> struct ChainFin : ChainOp<DT> {
             }
         }
         // The variates of the first round of residual trials (trial = warp;
-        // warp 0's are also the bonus draw's) depend on inputs only: the wide
-        // CTA draws them while the streaming grid drains and parks them in
-        // shared memory (the narrow one, two CTAs per SM, has no room: it
+        // warp 0's are also the bonus draw's) depend on inputs only: a CTA
+        // with PRE_DRAW draws them while the streaming grid drains and parks
+        // them in shared memory (the CTA that runs two per SM has no room: it
         // draws them where they are used).
         float *slot = buf + 2 * FWV * G + warp * DRAW_SLOT_FLOATS;
         if constexpr (PRE_DRAW) {
@@ -1678,16 +1678,25 @@ cudaError_t launch_chain(const ChainLaunch &L, cudaStream_t st)
     fill_cache(P.cache, L);
     P.sag = L.sag;
     P.invC = L.sag ? 1.0f / L.sag_C : 1.0f;
-    // One finalize CTA per sequence: the 16-warp CTA (one per SM) while the
-    // sequences fit on the SMs at once, else the 8-warp CTA (two per SM).
+    // One finalize CTA per sequence.  While the sequences fit on the SMs at
+    // once: the 16-warp CTA (16 residual trials per round) for fp32 batches
+    // above 32, else the 8-warp CTA; both draw the first round's variates
+    // before the dependent-grid wait.  Measured (same-box A/B against the
+    // 16-warp CTA everywhere): 8 warps for bf16 B = 64 -2.7 %, spd gamma = 1
+    // -5.6 %, fp32 B = 8 -8 %, B = 1 -15 %, but fp32 B = 64 +0.1 to +1.2 %
+    // (a smaller CTA starts sooner after the stream; fewer trials per round
+    // more often need a second round).  Beyond the SM count: the 8-warp CTA
+    // without the parked variates, two per SM.
     int sms = 0;
     cudaError_t e = device_sm_count(&sms);
     if (e != cudaSuccess) return e;
-    const bool wide = L.B <= sms;
-    if (L.dtype == 0)
-        return wide ? launch_stream_finalize<ChainOp<0>, ChainFin<0, FW>, 0>(P, L.tma, L.B, st)
+    const bool fits = L.B <= sms;
+    if (L.dtype == 0) {
+        if (fits && L.B > 32) return launch_stream_finalize<ChainOp<0>, ChainFin<0, FW>, 0>(P, L.tma, L.B, st);
+        return fits ? launch_stream_finalize<ChainOp<0>, ChainFin<0, NCW, true>, 0>(P, L.tma, L.B, st)
                     : launch_stream_finalize<ChainOp<0>, ChainFin<0, NCW>, 0>(P, L.tma, L.B, st);
-    return wide ? launch_stream_finalize<ChainOp<1>, ChainFin<1, FW>, 1>(P, L.tma, L.B, st)
+    }
+    return fits ? launch_stream_finalize<ChainOp<1>, ChainFin<1, NCW, true>, 1>(P, L.tma, L.B, st)
                 : launch_stream_finalize<ChainOp<1>, ChainFin<1, NCW>, 1>(P, L.tma, L.B, st);
 }
 

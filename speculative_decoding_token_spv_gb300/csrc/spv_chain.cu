@@ -947,6 +947,13 @@ template <int DT> struct TreeOp : ChainOp<DT> {
     // streams keep 8-block items (both slower with 16).
     static constexpr int CTAS_PER_SM = 2;
     static constexpr int ITEM_BLOCKS = DT == 0 ? 8 : 16;
+    // bf16: items numbered over the rows read and handed out by the call's
+    // counter (table below); fp32 keeps the static stride over all rows with
+    // the skip vote.  Measured (same-box A/B, B = 64, V = 151,936): bf16 k21
+    // 167 -> 155 us, w4 146 -> 138, 63-node tree 393 -> 363; fp32 k21 229 ->
+    // 243 (the balanced stream itself ended later than the static one's
+    // slowest CTA).
+    static constexpr bool TABLE = DT == 1;
 
     // Draft rows: lane v holds the parents of nodes v and v + 32 (16 bits
     // each, 0xffff for none or the root).  Target rows: no load.
@@ -968,6 +975,65 @@ template <int DT> struct TreeOp : ChainOp<DT> {
         if (u < 0) return false;
         const bool hit = (key & 0xffff) == u || ((key >> 16) & 0xffff) == u;
         return __ballot_sync(0xffffffffu, hit) == 0u;
+    }
+
+    // The rows read, numbered (at most SKIP_TABLE_MAX sequences; built by the
+    // whole CTA before the stream starts): bit u of mask[b] is set when node
+    // u of sequence b is the parent of some node (then its draft row is read:
+    // the same rows as the skip vote above), and first[b] counts the rows
+    // that sequences 0 .. b-1 read (first[B]: all of them).  A sequence reads
+    // its N target rows, then the draft rows of its set bits in node order.
+    __device__ static void build_table(const ChainParams &P, unsigned long long *mask, int *first)
+    {
+        for (int b = threadIdx.x; b < P.B; b += blockDim.x) mask[b] = 0ull;
+        __syncthreads();
+        const int n = P.B * P.nt;
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+            const int p = __ldg(&P.tree_parent[i]);
+            if (p >= 0 && p < P.nt) atomicOr(&mask[i / P.nt], 1ull << p);
+        }
+        __syncthreads();
+        if (threadIdx.x < 32) {  // exclusive prefix sum of the rows read, 32 sequences at a time
+            const int lane = threadIdx.x;
+            int run = 0;
+            for (int base = 0; base < P.B; base += 32) {
+                const int b = base + lane;
+                const int cnt = b < P.B ? P.nt + __popcll(mask[b]) : 0;
+                int incl = cnt;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int v = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += v;
+                }
+                if (b < P.B) first[b] = run + incl - cnt;
+                run += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) first[P.B] = run;
+        }
+        __syncthreads();
+    }
+
+    // Item `it` of the rows read: its row and chunk (binary search for the
+    // sequence, then the k-th row read within it).
+    __device__ static __forceinline__ void item_row(const ChainParams &P, const unsigned long long *mask,
+                                                    const int *first, long long it, int nc, long long &row, int &c)
+    {
+        const int r = static_cast<int>(div_row(it, nc));
+        c = static_cast<int>(it - static_cast<long long>(r) * nc);
+        int lo = 0, hi = P.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (first[mid] <= r) lo = mid;
+            else hi = mid - 1;
+        }
+        const int k = r - first[lo];
+        int rho = k;
+        if (k >= P.nt) {
+            unsigned long long m = mask[lo];
+            for (int j = k - P.nt; j > 0; --j) m &= m - 1ull;
+            rho = P.nt + __ffsll(static_cast<long long>(m)) - 1;
+        }
+        row = static_cast<long long>(lo) * P.R + rho;
     }
 
     // Before the finalize grid (which waits for this grid) meets in its
@@ -1118,9 +1184,14 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
             const float part = warp_sum(block_resid(P, tp, dp, beta, rc, lane));
             if (lane == 0) rb[beta] = part;
         }
+        if (lane == 0) __threadfence();  // this warp's masses, before the barrier's arrival
         bool ok = true;
-        if (P.cs > 1) ok = group_barrier<FWV * 32>(P.tree_bar + 2 * b, static_cast<unsigned>(P.cs), P.err, &sm.gflag);
-        else fin_sync<FWV>();
+        if (P.cs > 1)
+            ok = group_barrier<FWV * 32>(P.tree_bar + 2 * b, static_cast<unsigned>(P.cs), static_cast<unsigned>(j),
+                                         P.err, &sm.gflag);
+        else
+            fin_sync<FWV>();
+        if (!ok) return false;
         if (warp == 0) {
             float z = 0.f;
             for (int beta = lane; beta < P.nb; beta += 32) z += __ldcg(&rb[beta]);
@@ -1128,7 +1199,7 @@ template <int DT, int FWV> struct TreeFin : ChainFin<DT, FWV> {
             if (lane == 0) sm.Z = z;
         }
         fin_sync<FWV>();
-        return ok;
+        return true;
     }
 
     // Group g = b * cs + rank: CTA `rank` of sequence b.  Every CTA of the

@@ -36,6 +36,7 @@ constexpr int NCW = 8;                        // consumer warps (one block each)
 constexpr int THREADS = (NCW + 1) * 32;       // + one producer warp
 constexpr int RING_BYTES_PER_SM = 192 * 1024; // shared-memory ring of all resident CTAs of an SM
 constexpr uint32_t WAIT_LIMIT = 1u << 22;     // try_wait polls before giving up
+constexpr int SKIP_TABLE_MAX = 1024;          // sequences whose row-skip table fits shared memory (8 KB)
 constexpr int MAX_TRIALS = 64;                // residual rejection trials
 constexpr int STATUS_BAD_ROW = 4;
 constexpr int STATUS_TIMEOUT = 5;
@@ -190,27 +191,22 @@ __device__ __forceinline__ bool wait_flag_ge(const unsigned *flag, unsigned targ
 }
 
 // Barrier of the n CTAs of one thread-block cluster (co-scheduled, so every
-// one of them arrives) through global memory: bar[0] counts arrivals and is
-// reset by the last one, which then advances the generation bar[1].  Called
-// by all `threads` threads of each CTA (named barrier 1); global writes made
-// before it are visible to every CTA after it.  The wait is bounded: false
-// (and STATUS_TIMEOUT in *err) if it gave up.
-template <int THREADS_> __device__ __forceinline__ bool group_barrier(unsigned *bar, unsigned n, unsigned *err,
-                                                                      int *sh_flag)
+// one of them arrives) through global memory: *ctr counts the arrivals of
+// all the group's barriers of the call (zeroed before the group starts), so
+// the group's j-th barrier (from 0) is complete once it reaches n (j + 1).
+// One atomic per CTA and acquire polls by the waiting ones, no reset.  Called
+// by all `threads` threads of each CTA (named barrier 1); global writes that
+// each writer fenced (__threadfence) before it are visible to every CTA after
+// it.  The wait is bounded: false (and STATUS_TIMEOUT in *err) if it gave up.
+template <int THREADS_> __device__ __forceinline__ bool group_barrier(unsigned *ctr, unsigned n, unsigned j,
+                                                                      unsigned *err, int *sh_flag)
 {
-    __threadfence();
     asm volatile("bar.sync 1, %0;" ::"n"(THREADS_) : "memory");
     if (threadIdx.x == 0) {
-        int ok = 1;
-        const unsigned g0 = ld_acquire_gpu(bar + 1);
+        const unsigned target = n * (j + 1u);
         __threadfence();
-        if (atomicAdd(bar, 1u) == n - 1u) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
-        } else {
-            ok = wait_flag_ge(bar + 1, g0 + 1u, WAIT_LIMIT, err) ? 1 : 0;
-        }
+        int ok = 1;
+        if (atomicAdd(ctr, 1u) + 1u < target) ok = wait_flag_ge(ctr, target, WAIT_LIMIT, err) ? 1 : 0;
         __threadfence();
         *sh_flag = ok;
     }
@@ -541,9 +537,15 @@ struct ItemPos {
 //   skip_key(P, row, lane)               a per-lane input of skip(), read
 //                                        from global memory one item ahead;
 //   skip(P, row, key, lane)              warp-uniform: the row is skipped;
-//   reset(P)                             run by every thread at the start.
+//   reset(P)                             run by every thread at the start;
+//   TABLE                                number the items over the rows read
+//                                        instead (rows staged by TMA, at most
+//                                        SKIP_TABLE_MAX sequences), with
+//   build_table(P, mask, first)          the CTA's table of rows read, and
+//   item_row(P, mask, first, it, nc, row, c)  the row and chunk of item it.
 // Producer and consumers take the same decisions, so a skipped item uses
-// no ring stage.
+// no ring stage; with the table the skipped rows have no items at all and
+// the producer hands items out through the call's counter.
 // and optionally (WAITS_PRIOR = true) the consumers wait for the grid
 // launched before this one (programmatic dependent launch): the producer's
 // copies start while that grid finishes.
@@ -601,14 +603,29 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
     // up; it waits (griddepcontrol.wait) for this grid's results itself.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    const long long total = P.total_items;
+    long long total = P.total_items;
     const int nc = P.nc;
-    if constexpr (OpSkips<Op>::value) Op::reset(P);
-
     constexpr bool SK = OpSkips<Op>::value;
+    // A row-skipping op with staged rows, Op::TABLE and at most SKIP_TABLE_MAX sequences: the whole CTA
+    // first builds a table of the rows it reads (per sequence: a bit per node, and the rows read
+    // before the sequence), and the items are numbered over those rows alone; the producer then
+    // hands them out through the call's counter like the other ops.  Otherwise every item of
+    // every row is taken on the static stride with a warp vote on its row (skip_key / skip).
+    __shared__ unsigned long long skip_mask[SK ? SKIP_TABLE_MAX : 1];
+    __shared__ int skip_first[SK ? SKIP_TABLE_MAX + 1 : 1];
+    bool table = false;
+    if constexpr (SK) {
+        Op::reset(P);
+        table = TMA && Op::TABLE && P.B <= SKIP_TABLE_MAX;
+        if (table) {
+            Op::build_table(P, skip_mask, skip_first);  // ends with __syncthreads
+            total = static_cast<long long>(skip_first[P.B]) * nc;
+        }
+    }
+
     if (warp == NCW) {  // ---------------- producer
         if constexpr (SK) {
-            if (TMA) {  // the whole warp walks the items (skip() is a warp vote); lane 0 copies
+            if (TMA && !table) {  // the whole warp walks the items (skip() is a warp vote); lane 0 copies
                 const uint64_t pol = l2_evict_first_policy();
                 int i = 0;
                 long long it = blockIdx.x;
@@ -646,7 +663,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                 if (lane == 0)
                     for (int k = max(0, i - S); k < i; ++k) mbar_wait(&full_bar[k % S], (k / S) & 1);
             }
-            return;
+            if (!table) return;
         }
         if (TMA && lane == 0) {
             // Work items: this CTA's first S are static (it = blockIdx.x + j * grid, j < S); the rest
@@ -654,7 +671,8 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
             // faster take more of them (with equal shares the slowest SMs set the end of the pass).
             // The next item's index is fetched one item ahead: the atomic's latency hides behind the
             // wait for a free stage.  Each stage carries its item's (row, chunk) to the consumers; the
-            // stage after the last item carries row -1 and no copy.
+            // stage after the last item carries row -1 and no copy.  (A row-skipping op numbers its
+            // items over the rows it reads: table above.)
             const uint64_t pol = l2_evict_first_policy();
             unsigned long long *ctr = item_counter(P.err);
             const long long first_dyn = static_cast<long long>(S) * gridDim.x;
@@ -678,8 +696,14 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
                     aborted = true;
                     break;
                 }
-                const long long row = div_row(it, nc);
-                const int c = static_cast<int>(it - row * nc);
+                long long row;
+                int c;
+                if constexpr (SK) {
+                    Op::item_row(P, skip_mask, skip_first, it, nc, row, c);
+                } else {
+                    row = div_row(it, nc);
+                    c = static_cast<int>(it - row * nc);
+                }
                 stage_row[s] = row;
                 stage_c[s] = c;
                 const int n = min(CH, P.V - c * CH);
@@ -710,7 +734,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
 
     // ---------------- consumers
     if constexpr (OpWaitsPrior<Op>::value) asm volatile("griddepcontrol.wait;" ::: "memory");
-    if constexpr (TMA && !SK) {  // the items the producer hands over, stage by stage
+    if (TMA && (!SK || table)) {  // the items the producer hands over, stage by stage
         int stage = 0;
         uint32_t phase = 0;
         for (;;) {

@@ -226,3 +226,40 @@ def test_binary_tree_63_nodes(spv, dtype, T):
     w = workloads.tree(B=16, shape="b63", V=20000, dtype=dtype, temperature=T, device="cuda")
     got, ref = check_tree(spv, w)
     assert (ref["accept_count"] >= 3).any()
+
+
+def _random_trees(B, N, V, dtype, seed, T=1.0):
+    """A different random recursive tree per sequence (parent of node v
+    uniform over 0 .. v-1), so the sequences read different numbers of draft
+    rows; children's tokens drawn from their parent's draft distribution."""
+    gen = torch.Generator(device="cpu").manual_seed(seed)
+    z = torch.randn(B, N, V, generator=gen) * 2.0
+    d = z + torch.randn(B, N, V, generator=gen)
+    parent = torch.full((B, N), -1, dtype=torch.int32)
+    for v in range(1, N):
+        parent[:, v] = torch.randint(0, v, (B,), generator=gen, dtype=torch.int32)
+    tok = torch.zeros(B, N, dtype=torch.int32)
+    for v in range(1, N):
+        q = torch.softmax(d[torch.arange(B), parent[:, v].long()], dim=1)
+        tok[:, v] = torch.multinomial(q, 1, generator=gen)[:, 0].int()
+    r = 1.0 - torch.rand(B, N, generator=gen)
+    keys = torch.randint(-(2 ** 62), 2 ** 62, (B,), generator=gen, dtype=torch.int64)
+    return workloads.TreeInputs(f"random{N}_B{B}", z.to(dtype).cuda(), d.to(dtype).cuda(), parent.cuda(), tok.cuda(),
+                                r.cuda(), keys.cuda(), T)
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_random_tree_per_sequence(spv, dtype):
+    """Every sequence its own tree (different rows read per sequence, the
+    streaming pass numbering only the rows it reads), at T = 1 and T = 0."""
+    w = _random_trees(B=48, N=24, V=12288, dtype=dtype, seed=91)
+    check_tree(spv, w)
+    check_tree(spv, workloads.TreeInputs(w.name, w.target, w.draft, w.parent, w.tokens, w.r, w.keys, 0.0))
+
+
+def test_more_sequences_than_the_skip_table(spv):
+    """B = 1100 bf16 sequences, above the 1024 the streaming pass's
+    shared-memory table of rows read holds: the rows are taken on the static
+    stride with a vote per row instead; same outputs as the oracle."""
+    w = _random_trees(B=1100, N=9, V=2048, dtype=torch.bfloat16, seed=92)
+    check_tree(spv, w)

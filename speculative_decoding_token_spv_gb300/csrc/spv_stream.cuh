@@ -214,6 +214,18 @@ template <int THREADS_> __device__ __forceinline__ bool group_barrier(unsigned *
     return *reinterpret_cast<volatile int *>(sh_flag) != 0;
 }
 
+// 16-byte asynchronous copy global -> shared by the executing thread (both
+// addresses 16-byte aligned), and its commit / wait groups.
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait()
+{
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ uint64_t l2_evict_first_policy()
 {
     uint64_t pol;

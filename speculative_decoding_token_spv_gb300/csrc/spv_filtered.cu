@@ -210,24 +210,44 @@ __global__ void __launch_bounds__(SAMPLE_BLOCKS * 32) filt_sample_kernel(const F
         const long long mm = (7LL * P.top_k * sampled + 2LL * P.V - 1) / (2LL * P.V);
         m = static_cast<int>(mm < 1 ? 1 : (mm < P.top_k ? mm : P.top_k));
     }
-    unsigned taken = 0u;
+    // The m-th largest: every lane's values as order-preserving bit patterns
+    // (NaN as -inf), sorted descending in registers by a bitonic network;
+    // then m rounds, each taking the warp's largest head (one redux) from the
+    // first lane that holds it.  -inf is never taken: fewer than m finite
+    // sampled logits leave t = -inf.
+    constexpr uint32_t KEY_NEG_INF = 0x007fffffu;  // the pattern of -inf
+    uint32_t key[NS];
+#pragma unroll
+    for (int j = 0; j < NS; ++j) {
+        const uint32_t u = __float_as_uint(isnan(gm[j]) ? -INFINITY : gm[j]);
+        key[j] = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    }
+#pragma unroll
+    for (int size = 2; size <= NS; size <<= 1)
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1)
+#pragma unroll
+            for (int i = 0; i < NS; ++i) {
+                const int j = i ^ stride;
+                if (j > i) {
+                    const uint32_t hi = max(key[i], key[j]), lo = min(key[i], key[j]);
+                    const bool desc = (i & size) == 0;
+                    key[i] = desc ? hi : lo;
+                    key[j] = desc ? lo : hi;
+                }
+            }
     float t = -INFINITY;
     for (int round = 0; round < m; ++round) {
-        float best = -INFINITY;
-        int bi = INT_MAX;
-#pragma unroll
-        for (int j = 0; j < NS; ++j)
-            if (!(taken & (1u << j)) && gm[j] > best) {
-                best = gm[j];
-                bi = lane * NS + j;
-            }
-        warp_argmax(best, bi);
-        if (bi == INT_MAX) {  // fewer than m finite sampled logits
+        const uint32_t mx = __reduce_max_sync(0xffffffffu, key[0]);
+        if (mx <= KEY_NEG_INF) {  // fewer than m finite sampled logits
             t = -INFINITY;
             break;
         }
-        if (bi / NS == lane) taken |= 1u << (bi % NS);
-        t = best;
+        const bool mine = lane == __ffs(__ballot_sync(0xffffffffu, key[0] == mx)) - 1;
+#pragma unroll
+        for (int j = 0; j + 1 < NS; ++j) key[j] = mine ? key[j + 1] : key[j];
+        key[NS - 1] = mine ? 0u : key[NS - 1];
+        t = __uint_as_float((mx & 0x80000000u) ? (mx & 0x7fffffffu) : ~mx);
     }
     if (lane == 0) {
         P.tau[row] = t;

@@ -263,3 +263,13 @@ def test_more_sequences_than_the_skip_table(spv):
     stride with a vote per row instead; same outputs as the oracle."""
     w = _random_trees(B=1100, N=9, V=2048, dtype=torch.bfloat16, seed=92)
     check_tree(spv, w)
+
+
+def test_bf16_rows_not_16_byte_aligned(spv):
+    """bf16 rows of V = 12,289 logits (not a multiple of 8 ids, so not
+    16-byte aligned): the streaming pass loads the rows without TMA and
+    votes on the skipped rows, the residual passes use plain loads; same
+    outputs as the oracle at T = 1 and T = 0."""
+    w = _random_trees(B=24, N=12, V=12289, dtype=torch.bfloat16, seed=93)
+    check_tree(spv, w)
+    check_tree(spv, workloads.TreeInputs(w.name, w.target, w.draft, w.parent, w.tokens, w.r, w.keys, 0.0))

@@ -828,7 +828,7 @@ __global__ void __launch_bounds__(THREADS, Op::CTAS_PER_SM) stream_kernel(const 
 // One CTA (Op::FIN_WARPS warps) per group: merges the group's partial results once the
 // streaming grid it depends on has finished, and writes the outputs.
 template <class Op, int DT>
-__global__ void __launch_bounds__(Op::FIN_WARPS * 32, 1) __maxnreg__(Op::FIN_WARPS >= 16 ? 96 : 128) finalize_kernel(const typename Op::Params P)
+__global__ void __launch_bounds__(Op::FIN_WARPS * 32, 1) __maxnreg__(Op::FIN_WARPS >= 32 ? 64 : (Op::FIN_WARPS >= 16 ? 96 : 128)) finalize_kernel(const typename Op::Params P)
 {
     __shared__ typename Op::Smem sm;
     extern __shared__ __align__(16) float fin_buf[];  // Op::FIN_BUF_FLOATS floats

@@ -86,6 +86,20 @@ def test_eagle_nucleus(spv):
     check_filtered(spv, w, 40, 0.9)
 
 
+@pytest.mark.parametrize("gamma", [8, 15])
+def test_more_rows_than_sixteen(spv, gamma):
+    """2 gamma + 1 > 16 rows per sequence (the finalize selects every row's
+    top k at once with one warp per row): the EAGLE gamma = 15 workload with
+    top-k 50 and top-p 0.9, and gamma = 8 on a smaller vocabulary."""
+    if gamma == 15:
+        w = workloads.eagle(gamma=15, device="cuda", top_k=50, top_p=0.9)
+        check_filtered(spv, w, 50, 0.9)
+    else:
+        w = workloads.sweep(B=24, dtype=torch.float32, device="cuda", V=30000, gamma=8, top_k=50)
+        check_filtered(spv, w, 50)
+        check_filtered(spv, w, 64, 0.9)
+
+
 @pytest.mark.parametrize("V", [20, 1001, 1025, 8193, 50000])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_ragged_vocab_and_plain_loads(spv, V, dtype):
